@@ -1,0 +1,195 @@
+"""fp64 CPU oracle for the speculative-sampling verification step.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+bench's CPU-baseline leg are the only callers.  The product library never
+imports this package, and this package never imports the product.
+
+The arithmetic lives in ``sv_oracle.c`` (plain C, fp64, sequential sums in
+token-id order); this module only compiles it with gcc and marshals numpy
+arrays through ctypes.  See the header of ``sv_oracle.c`` for the pages and
+sections each step follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sv_oracle.c")
+_LIB_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_LIB_DIR, "libsvoracle.so")
+
+# per-sequence status bits, as the oracle reports them
+ORC_BAD_U = 1
+ORC_BAD_TOKEN = 2
+ORC_BAD_Q = 4
+ORC_BAD_ROW = 8
+ORC_DEGENERATE_RESIDUAL = 16
+
+_c_i32p = ctypes.POINTER(ctypes.c_int32)
+_c_i8p = ctypes.POINTER(ctypes.c_int8)
+_c_f64p = ctypes.POINTER(ctypes.c_double)
+
+
+def compile_oracle(src: str = _SRC, out: str = _LIB) -> str:
+    """Compile an oracle source file into a shared library (gcc, -O2).
+
+    ``-ffp-contract=off`` keeps gcc from fusing multiply-adds, so x86 and
+    aarch64 builds round identically.
+    """
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+           "-pthread", "-o", out, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def build() -> str:
+    """Compile ``sv_oracle.c`` if the library is missing or stale."""
+    if (not os.path.exists(_LIB)
+            or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)):
+        compile_oracle()
+    return _LIB
+
+
+def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    lib.sv_oracle_verify.restype = ctypes.c_int
+    lib.sv_oracle_verify.argtypes = [
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_double, ctypes.c_int64, ctypes.c_int32,
+        ctypes.c_int32, _c_i32p, _c_i32p, _c_i8p, _c_f64p, _c_f64p, _c_i32p,
+        ctypes.c_int]
+    lib.sv_oracle_verify_probs.restype = ctypes.c_int
+    lib.sv_oracle_verify_probs.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _c_i32p, _c_i32p,
+        _c_i8p, _c_f64p, _c_f64p, _c_i32p, ctypes.c_int]
+    lib.sv_oracle_row_dists.restype = ctypes.c_double
+    lib.sv_oracle_row_dists.argtypes = [
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_double, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+        ctypes.c_int32, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p]
+    return lib
+
+
+_loaded: dict[str, "Oracle"] = {}
+
+
+@dataclass
+class OracleResult:
+    out_tokens: np.ndarray     # int32 [B, K+1], -1 padded
+    num_emitted: np.ndarray    # int32 [B], 0 for an invalid sequence
+    accept_flags: np.ndarray   # int8  [B, K]: 1 accepted, 0 rejected, -1 not reached
+    accept_prob: np.ndarray    # fp64  [B, K]: min(1, p(x)/q(x)) for every draft
+    residual_mass: np.ndarray  # fp64  [B]: sum max(0, p-q) at the rejection, 0 on bonus
+    status: np.ndarray         # int32 [B]: ORC_* bits
+
+
+class Oracle:
+    """ctypes handle on one compiled oracle library."""
+
+    def __init__(self, path: str):
+        self.path = path
+        self.lib = _bind(ctypes.CDLL(path))
+
+    @staticmethod
+    def _outputs(B: int, K: int):
+        return (np.empty((B, K + 1), np.int32), np.empty(B, np.int32),
+                np.empty((B, K), np.int8), np.empty((B, K), np.float64),
+                np.empty(B, np.float64), np.empty(B, np.int32))
+
+    @staticmethod
+    def _ptr(a, ct):
+        return a.ctypes.data_as(ct)
+
+    def verify(self, logits: np.ndarray, q: np.ndarray | None,
+               tokens: np.ndarray, u: np.ndarray, T: float,
+               nthreads: int = 1) -> OracleResult:
+        """logits: [B,K+1,V] uint16 (bf16 bits) or float32; q: [B,K,V]
+        float32 or None (one-hot drafts); tokens [B,K] int32; u [B,K+1] float32."""
+        logits = np.ascontiguousarray(logits)
+        if logits.dtype == np.uint16:
+            dtype = 0
+        elif logits.dtype == np.float32:
+            dtype = 1
+        else:
+            raise TypeError("logits must be uint16 (bf16 bits) or float32")
+        B, K1, V = logits.shape
+        K = K1 - 1
+        tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, K)
+        u = np.ascontiguousarray(u, dtype=np.float32).reshape(B, K + 1)
+        if q is not None:
+            q = np.ascontiguousarray(q, dtype=np.float32).reshape(B, K, V)
+        outs = self._outputs(B, K)
+        rc = self.lib.sv_oracle_verify(
+            logits.ctypes.data, dtype, None if q is None else q.ctypes.data,
+            tokens.ctypes.data, u.ctypes.data, float(T), B, K, V,
+            self._ptr(outs[0], _c_i32p), self._ptr(outs[1], _c_i32p),
+            self._ptr(outs[2], _c_i8p), self._ptr(outs[3], _c_f64p),
+            self._ptr(outs[4], _c_f64p), self._ptr(outs[5], _c_i32p),
+            int(nthreads))
+        if rc != 0:
+            raise RuntimeError("sv_oracle_verify failed")
+        return OracleResult(*outs)
+
+    def verify_probs(self, p: np.ndarray, q: np.ndarray | None,
+                     tokens: np.ndarray, u: np.ndarray,
+                     nthreads: int = 1) -> OracleResult:
+        """p: [B,K+1,V] fp64 probabilities; q: [B,K,V] fp64 or None;
+        tokens [B,K]; u [B,K+1] fp64."""
+        p = np.ascontiguousarray(p, dtype=np.float64)
+        B, K1, V = p.shape
+        K = K1 - 1
+        tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, K)
+        u = np.ascontiguousarray(u, dtype=np.float64).reshape(B, K + 1)
+        if q is not None:
+            q = np.ascontiguousarray(q, dtype=np.float64).reshape(B, K, V)
+        outs = self._outputs(B, K)
+        rc = self.lib.sv_oracle_verify_probs(
+            p.ctypes.data, None if q is None else q.ctypes.data,
+            tokens.ctypes.data, u.ctypes.data, B, K, V,
+            self._ptr(outs[0], _c_i32p), self._ptr(outs[1], _c_i32p),
+            self._ptr(outs[2], _c_i8p), self._ptr(outs[3], _c_f64p),
+            self._ptr(outs[4], _c_f64p), self._ptr(outs[5], _c_i32p),
+            int(nthreads))
+        if rc != 0:
+            raise RuntimeError("sv_oracle_verify_probs failed")
+        return OracleResult(*outs)
+
+    def row_dists(self, logits: np.ndarray, q: np.ndarray | None,
+                  tokens: np.ndarray, T: float, b: int, j: int,
+                  rejected: bool):
+        """(p, w, cdf, Z) of row j of sequence b: the softmax, the normalised
+        distribution the final token is drawn from (residual if `rejected`,
+        else p), its running sum in id order, and the unnormalised mass."""
+        logits = np.ascontiguousarray(logits)
+        dtype = 0 if logits.dtype == np.uint16 else 1
+        B, K1, V = logits.shape
+        K = K1 - 1
+        tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, K)
+        if q is not None:
+            q = np.ascontiguousarray(q, dtype=np.float32).reshape(B, K, V)
+        p = np.empty(V, np.float64)
+        w = np.empty(V, np.float64)
+        cdf = np.empty(V, np.float64)
+        Z = self.lib.sv_oracle_row_dists(
+            logits.ctypes.data, dtype, None if q is None else q.ctypes.data,
+            tokens.ctypes.data, float(T), int(b), K, V, int(j),
+            1 if rejected else 0, p.ctypes.data, w.ctypes.data,
+            cdf.ctypes.data)
+        if Z < 0:
+            raise ValueError("invalid row")
+        return p, w, cdf, Z
+
+
+def load(path: str | None = None) -> Oracle:
+    """The oracle library at `path` (default: build and load sv_oracle.c)."""
+    path = path or build()
+    if path not in _loaded:
+        _loaded[path] = Oracle(path)
+    return _loaded[path]

@@ -1,0 +1,494 @@
+/*
+ * sv_oracle.c -- plain fp64 CPU oracle for the speculative-sampling
+ * verification step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the bench's
+ * CPU-baseline leg load this library.  It shares no code, header, table or
+ * constant with the CUDA library; the two are compared on the same seeded
+ * inputs.  It is deliberately slow and literal: every sum runs sequentially
+ * in token-id order, nothing is blocked, fused or reordered.
+ *
+ * What it computes, and where each step is defined:
+ *
+ *  (1) p_j = softmax(z_j / T) for every one of the K+1 target rows.
+ *      "推测解码采样验证优化策略 —— 深度调研报告", part 1 section 4
+ *      (实现逻辑, verify(): softmax of target_logits / temperature), and
+ *      "推测解码：草稿、验证与实际加速", section 接受与拒绝怎样保住分布
+ *      (p already carries the temperature; q arrives already processed).
+ *  (2) Row j verifies draft x_{j+1}; row K is only used for the extra token.
+ *      "推测解码：草稿、验证与实际加速", section 候选已知，验证才能并行
+ *      (the equation listing p_1 .. p_4 and the offset between logits and
+ *      candidates).
+ *  (3) Accept draft x with probability a(x) = min(1, p(x)/q(x)), tested
+ *      left to right as  u_k < a(x_k).
+ *      Same page, section 接受与拒绝怎样保住分布 (equation for a(x)) and
+ *      section 算完三个 token 的全部概率 (the replay accepts when the draw is
+ *      strictly below the threshold).
+ *  (4) At the first rejection, emit one token drawn from
+ *      r(x) = max(0, p(x) - q(x)) / sum_y max(0, p(y) - q(y)); later drafts are
+ *      discarded.  If every draft is accepted, emit one extra token from
+ *      p_{K+1}.  Same page, sections 接受与拒绝怎样保住分布 (equation for r(x))
+ *      and 候选已知，验证才能并行; "投机采样", section 机制：起草-验证-接受
+ *      (n in [1, gamma+1]).
+ *  (5) Drawing from a distribution w with a uniform u: walk the token ids in
+ *      ascending order and return the first id whose cumulative mass exceeds
+ *      u * sum(w).  "推测解码：草稿、验证与实际加速", section
+ *      算完三个 token 的全部概率 (the sampler of the replay, which uses the
+ *      final draw for the correction or the extra token).
+ *  (6) A deterministic draft (n-gram / prompt lookup) is the case
+ *      q = delta_x: then a(x) = min(1, p(x)) and r is p with x removed.
+ *      Follows from (3)-(4) with q one-hot ("推测解码采样验证优化策略", part 1
+ *      section 1 on prompt lookup; "投机采样", 变体谱系 table, N-gram row).
+ *
+ * Readings taken where the pages are silent or disagree (also listed in the
+ * design notes):
+ *  - the accept test is  u < a  (one page writes <=, the replay uses <);
+ *  - the correction / extra token always uses the final uniform u[K];
+ *  - if rounding leaves no id with t < C(i), the last id of positive mass is
+ *    returned;
+ *  - if the residual mass is not positive after a rejection (impossible in
+ *    exact arithmetic) the token is drawn from p and a status bit is set;
+ *  - a sequence with an invalid input (u outside [0,1), token outside [0,V),
+ *    q(x) <= 0 or non-finite, a logit row with NaN/+inf or no finite entry)
+ *    emits nothing: num_emitted = 0, tokens and flags -1, probabilities 0.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Per-sequence status bits reported by the oracle. */
+enum {
+    ORC_BAD_U = 1,
+    ORC_BAD_TOKEN = 2,
+    ORC_BAD_Q = 4,
+    ORC_BAD_ROW = 8,
+    ORC_DEGENERATE_RESIDUAL = 16
+};
+
+/* ---------------------------------------------------------------- helpers */
+
+static double bf16_bits_to_double(uint16_t h)
+{
+    uint32_t bits = (uint32_t)h << 16; /* bf16 is the top half of an fp32 */
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+static double logit_at(const void *logits, int dtype, int64_t idx)
+{
+    if (dtype == 0)
+        return bf16_bits_to_double(((const uint16_t *)logits)[idx]);
+    return (double)((const float *)logits)[idx];
+}
+
+/* Step (1): p = softmax(z / T) over one row.  Returns 0 if the row has a
+ * NaN or +inf entry or no finite entry (then p is left undefined). */
+static int softmax_row(const void *logits, int dtype, int64_t row_off,
+                       int32_t V, double T, double *p)
+{
+    double m = -INFINITY;
+    for (int32_t i = 0; i < V; ++i) {
+        double z = logit_at(logits, dtype, row_off + i);
+        if (isnan(z) || (isinf(z) && z > 0))
+            return 0;
+        double zt = z / T;
+        if (zt > m)
+            m = zt;
+    }
+    if (!isfinite(m))
+        return 0;
+    double s = 0.0;
+    for (int32_t i = 0; i < V; ++i) {
+        double zt = logit_at(logits, dtype, row_off + i) / T;
+        p[i] = exp(zt - m); /* exp(-inf) = 0 for masked entries */
+        s += p[i];
+    }
+    for (int32_t i = 0; i < V; ++i)
+        p[i] /= s;
+    return 1;
+}
+
+/* Step (5): first id (ascending) with t < C(i), t = u * sum(w).  If rounding
+ * leaves none, the last id with positive mass.  *Z_out receives sum(w). */
+static int32_t inverse_cdf(const double *w, int32_t V, double u, double *Z_out)
+{
+    double Z = 0.0;
+    for (int32_t i = 0; i < V; ++i)
+        Z += w[i];
+    *Z_out = Z;
+    double t = u * Z;
+    double C = 0.0;
+    for (int32_t i = 0; i < V; ++i) {
+        C += w[i];
+        if (t < C)
+            return i;
+    }
+    for (int32_t i = V - 1; i >= 0; --i)
+        if (w[i] > 0.0)
+            return i;
+    return 0;
+}
+
+/* The distribution the final token is drawn from at survivor row j.
+ * rejected: r = max(0, p - q) (q one-hot on x when Q is NULL);
+ * bonus:    r = p. */
+static void survivor_weights(const double *p, const double *q, int onehot,
+                             int32_t x, int rejected, int32_t V, double *w)
+{
+    for (int32_t i = 0; i < V; ++i) {
+        if (!rejected) {
+            w[i] = p[i];
+        } else {
+            double qi = onehot ? (i == x ? 1.0 : 0.0) : q[i];
+            double d = p[i] - qi;
+            w[i] = d > 0.0 ? d : 0.0;
+        }
+    }
+}
+
+/* ------------------------------------------------- one sequence, probs in */
+
+typedef struct {
+    int32_t *out_tokens;   /* [K+1] */
+    int32_t *num_emitted;  /* [1]   */
+    int8_t *accept_flags;  /* [K]   */
+    double *accept_prob;   /* [K]   */
+    double *residual_mass; /* [1]   */
+    int32_t *status;       /* [1]   */
+} seq_out_t;
+
+/* P: K+1 rows of p (fp64); Q: K rows of q or NULL (one-hot drafts);
+ * rows_ok: validity of each of the K+1 rows (NULL = all valid). */
+static void verify_sequence(const double *P, const double *Q,
+                            const int32_t *tok, const double *u,
+                            const int *rows_ok, int32_t K, int32_t V,
+                            double *w_scratch, seq_out_t o)
+{
+    int32_t st = 0;
+    for (int32_t k = 0; k <= K; ++k)
+        if (!(u[k] >= 0.0 && u[k] < 1.0))
+            st |= ORC_BAD_U;
+    for (int32_t k = 0; k < K; ++k) {
+        if (tok[k] < 0 || tok[k] >= V) {
+            st |= ORC_BAD_TOKEN;
+        } else if (Q) {
+            double qx = Q[(int64_t)k * V + tok[k]];
+            if (!(qx > 0.0) || !isfinite(qx))
+                st |= ORC_BAD_Q;
+        }
+    }
+    if (rows_ok)
+        for (int32_t j = 0; j <= K; ++j)
+            if (!rows_ok[j])
+                st |= ORC_BAD_ROW;
+
+    for (int32_t k = 0; k <= K; ++k)
+        o.out_tokens[k] = -1;
+    for (int32_t k = 0; k < K; ++k) {
+        o.accept_flags[k] = -1;
+        o.accept_prob[k] = 0.0;
+    }
+    *o.residual_mass = 0.0;
+    *o.num_emitted = 0;
+    if (st) {
+        *o.status = st;
+        return;
+    }
+
+    /* accept probability of every draft (also of those never reached) */
+    for (int32_t k = 0; k < K; ++k) {
+        double px = P[(int64_t)k * V + tok[k]];
+        double qx = Q ? Q[(int64_t)k * V + tok[k]] : 1.0;
+        double a = px / qx;
+        o.accept_prob[k] = a < 1.0 ? a : 1.0;
+    }
+
+    /* steps (3)-(4): left to right, stop at the first rejection */
+    int32_t jstar = K;
+    for (int32_t k = 0; k < K; ++k) {
+        if (u[k] < o.accept_prob[k]) {
+            o.out_tokens[k] = tok[k];
+            o.accept_flags[k] = 1;
+        } else {
+            o.accept_flags[k] = 0;
+            jstar = k;
+            break;
+        }
+    }
+
+    int rejected = jstar < K;
+    const double *prow = P + (int64_t)jstar * V;
+    survivor_weights(prow, rejected && Q ? Q + (int64_t)jstar * V : NULL,
+                     rejected && !Q, rejected ? tok[jstar] : -1, rejected, V,
+                     w_scratch);
+    double Z;
+    int32_t y = inverse_cdf(w_scratch, V, u[K], &Z);
+    if (rejected && !(Z > 0.0)) {
+        st |= ORC_DEGENERATE_RESIDUAL;
+        double Zp;
+        y = inverse_cdf(prow, V, u[K], &Zp);
+    }
+    o.out_tokens[jstar] = y;
+    *o.residual_mass = rejected ? Z : 0.0;
+    *o.num_emitted = jstar + 1;
+    *o.status = st;
+}
+
+/* --------------------------------------------------------- thread fan-out */
+
+typedef struct {
+    /* common inputs */
+    const void *logits;
+    int dtype;
+    const float *qf;
+    const double *pd, *qd, *ud;
+    const int32_t *tokens;
+    const float *uf;
+    double T;
+    int64_t B;
+    int32_t K, V;
+    /* outputs */
+    int32_t *out_tokens, *num_emitted, *status;
+    int8_t *accept_flags;
+    double *accept_prob, *residual_mass;
+    /* work split */
+    int64_t b0, b1;
+    int from_logits;
+    int failed;
+} job_t;
+
+static seq_out_t outputs_of(const job_t *J, int64_t b)
+{
+    seq_out_t o;
+    o.out_tokens = J->out_tokens + b * (J->K + 1);
+    o.num_emitted = J->num_emitted + b;
+    o.accept_flags = J->accept_flags + b * J->K;
+    o.accept_prob = J->accept_prob + b * J->K;
+    o.residual_mass = J->residual_mass + b;
+    o.status = J->status + b;
+    return o;
+}
+
+static void *run_job(void *arg)
+{
+    job_t *J = (job_t *)arg;
+    int32_t K = J->K, V = J->V;
+    double *P = NULL, *Q = NULL, *w = NULL, *u = NULL;
+    int *ok = NULL;
+    w = (double *)malloc(sizeof(double) * (size_t)V);
+    u = (double *)malloc(sizeof(double) * (size_t)(K + 1));
+    ok = (int *)malloc(sizeof(int) * (size_t)(K + 1));
+    if (J->from_logits) {
+        P = (double *)malloc(sizeof(double) * (size_t)(K + 1) * (size_t)V);
+        if (J->qf && K > 0)
+            Q = (double *)malloc(sizeof(double) * (size_t)K * (size_t)V);
+    }
+    if (!w || !u || !ok || (J->from_logits && !P) ||
+        (J->from_logits && J->qf && K > 0 && !Q)) {
+        J->failed = 1;
+        goto done;
+    }
+    for (int64_t b = J->b0; b < J->b1; ++b) {
+        const int32_t *tok = J->tokens + b * K;
+        if (J->from_logits) {
+            for (int32_t j = 0; j <= K; ++j)
+                ok[j] = softmax_row(J->logits, J->dtype,
+                                    (b * (K + 1) + j) * (int64_t)V, V, J->T,
+                                    P + (int64_t)j * V);
+            if (Q)
+                for (int64_t e = 0; e < (int64_t)K * V; ++e)
+                    Q[e] = (double)J->qf[b * K * (int64_t)V + e];
+            for (int32_t k = 0; k <= K; ++k)
+                u[k] = (double)J->uf[b * (K + 1) + k];
+            verify_sequence(P, J->qf ? Q : NULL, tok, u, ok, K, V, w,
+                            outputs_of(J, b));
+        } else {
+            const double *Pb = J->pd + b * (K + 1) * (int64_t)V;
+            const double *Qb = J->qd ? J->qd + b * K * (int64_t)V : NULL;
+            verify_sequence(Pb, Qb, tok, J->ud + b * (K + 1), NULL, K, V, w,
+                            outputs_of(J, b));
+        }
+    }
+done:
+    free(P);
+    free(Q);
+    free(w);
+    free(u);
+    free(ok);
+    return NULL;
+}
+
+static int fan_out(job_t proto, int nthreads)
+{
+    if (nthreads < 1)
+        nthreads = 1;
+    if ((int64_t)nthreads > proto.B)
+        nthreads = (int)(proto.B > 0 ? proto.B : 1);
+    job_t *jobs = (job_t *)calloc((size_t)nthreads, sizeof(job_t));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !th) {
+        free(jobs);
+        free(th);
+        return -1;
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = proto;
+        jobs[t].b0 = proto.B * t / nthreads;
+        jobs[t].b1 = proto.B * (t + 1) / nthreads;
+    }
+    for (int t = 1; t < nthreads; ++t)
+        if (pthread_create(&th[t], NULL, run_job, &jobs[t]) != 0)
+            jobs[t].failed = 2; /* run it inline below instead */
+    run_job(&jobs[0]);
+    int rc = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (jobs[t].failed == 2) {
+            jobs[t].failed = 0;
+            run_job(&jobs[t]);
+        } else {
+            pthread_join(th[t], NULL);
+        }
+    }
+    for (int t = 0; t < nthreads; ++t)
+        if (jobs[t].failed)
+            rc = -1;
+    free(jobs);
+    free(th);
+    return rc;
+}
+
+/* ------------------------------------------------------------ entry points */
+
+/* Verification from target logits.
+ * logits: [B, K+1, V], dtype 0 = bf16 bit patterns (uint16), 1 = fp32.
+ * q: [B, K, V] fp32, or NULL for one-hot drafts.  tokens: [B, K] int32.
+ * u: [B, K+1] fp32, u[:, K] is the final draw.  T > 0.
+ * Outputs (host): out_tokens [B, K+1], num_emitted [B], accept_flags [B, K],
+ * accept_prob [B, K] fp64, residual_mass [B] fp64, status [B].
+ * Returns 0, or -1 on bad arguments / allocation failure. */
+int sv_oracle_verify(const void *logits, int dtype, const float *q,
+                     const int32_t *tokens, const float *u, double T,
+                     int64_t B, int32_t K, int32_t V, int32_t *out_tokens,
+                     int32_t *num_emitted, int8_t *accept_flags,
+                     double *accept_prob, double *residual_mass,
+                     int32_t *status, int nthreads)
+{
+    if (!logits || !tokens || !u || !out_tokens || !num_emitted ||
+        !accept_flags || !accept_prob || !residual_mass || !status)
+        return -1;
+    if (B < 0 || K < 0 || V < 1 || !(T > 0.0) || !isfinite(T) ||
+        (dtype != 0 && dtype != 1))
+        return -1;
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.logits = logits;
+    J.dtype = dtype;
+    J.qf = q;
+    J.tokens = tokens;
+    J.uf = u;
+    J.T = T;
+    J.B = B;
+    J.K = K;
+    J.V = V;
+    J.out_tokens = out_tokens;
+    J.num_emitted = num_emitted;
+    J.accept_flags = accept_flags;
+    J.accept_prob = accept_prob;
+    J.residual_mass = residual_mass;
+    J.status = status;
+    J.from_logits = 1;
+    if (B == 0)
+        return 0;
+    return fan_out(J, nthreads);
+}
+
+/* Verification from probabilities given directly (fp64): p [B, K+1, V],
+ * q [B, K, V] or NULL (one-hot), u [B, K+1] fp64.  Same outputs. */
+int sv_oracle_verify_probs(const double *p, const double *q,
+                           const int32_t *tokens, const double *u, int64_t B,
+                           int32_t K, int32_t V, int32_t *out_tokens,
+                           int32_t *num_emitted, int8_t *accept_flags,
+                           double *accept_prob, double *residual_mass,
+                           int32_t *status, int nthreads)
+{
+    if (!p || !tokens || !u || !out_tokens || !num_emitted || !accept_flags ||
+        !accept_prob || !residual_mass || !status)
+        return -1;
+    if (B < 0 || K < 0 || V < 1)
+        return -1;
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.pd = p;
+    J.qd = q;
+    J.ud = u;
+    J.tokens = tokens;
+    J.B = B;
+    J.K = K;
+    J.V = V;
+    J.out_tokens = out_tokens;
+    J.num_emitted = num_emitted;
+    J.accept_flags = accept_flags;
+    J.accept_prob = accept_prob;
+    J.residual_mass = residual_mass;
+    J.status = status;
+    J.from_logits = 0;
+    if (B == 0)
+        return 0;
+    return fan_out(J, nthreads);
+}
+
+/* Diagnostics for one sequence b of a logits input: the softmax of row j
+ * (p_out, V values) and the normalised distribution the final token would be
+ * drawn from at row j (w_out, V values): the residual when `rejected` is 1,
+ * p itself otherwise, each divided by its own sum; cdf_out (V values) is the
+ * running sum of w_out taken in id order.  Any output pointer may be NULL.
+ * Returns the unnormalised mass sum(w), or -1 if the row is invalid. */
+double sv_oracle_row_dists(const void *logits, int dtype, const float *q,
+                           const int32_t *tokens, double T, int64_t b,
+                           int32_t K, int32_t V, int32_t j, int rejected,
+                           double *p_out, double *w_out, double *cdf_out)
+{
+    if (!logits || !tokens || V < 1 || K < 0 || j < 0 || j > K ||
+        (rejected && j >= K) || !(T > 0.0))
+        return -1.0;
+    double *p = (double *)malloc(sizeof(double) * (size_t)V);
+    double *w = (double *)malloc(sizeof(double) * (size_t)V);
+    double *qr = NULL;
+    double Z = -1.0;
+    if (!p || !w)
+        goto out;
+    if (!softmax_row(logits, dtype, (b * (K + 1) + j) * (int64_t)V, V, T, p))
+        goto out;
+    if (rejected && q) {
+        qr = (double *)malloc(sizeof(double) * (size_t)V);
+        if (!qr)
+            goto out;
+        for (int32_t i = 0; i < V; ++i)
+            qr[i] = (double)q[(b * K + j) * (int64_t)V + i];
+    }
+    int32_t x = rejected ? tokens[b * K + j] : -1;
+    survivor_weights(p, qr, rejected && !q, x, rejected, V, w);
+    Z = 0.0;
+    for (int32_t i = 0; i < V; ++i)
+        Z += w[i];
+    {
+        double C = 0.0;
+        for (int32_t i = 0; i < V; ++i) {
+            C += w[i];
+            if (p_out)
+                p_out[i] = p[i];
+            if (w_out)
+                w_out[i] = Z > 0.0 ? w[i] / Z : 0.0;
+            if (cdf_out)
+                cdf_out[i] = Z > 0.0 ? C / Z : 0.0;
+        }
+    }
+out:
+    free(p);
+    free(w);
+    free(qr);
+    return Z;
+}

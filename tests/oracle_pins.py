@@ -1,0 +1,521 @@
+"""Pins that tie the fp64 oracle to what the pages and the mathematics fix.
+
+Each ``pin_*`` takes an oracle handle and raises AssertionError when the
+oracle disagrees with a value printed on the pages, a closed form, an
+invariant, a textbook special case, or exact brute force.  The same pins run
+against the real oracle (tests/test_oracle_pins.py) and against deliberately
+broken copies of it (tests/test_oracle_mutants.py), which must each fail at
+least one pin.
+
+Sources:
+  [NOTE]  "推测解码：草稿、验证与实际加速" -- sections 候选已知，验证才能并行,
+          接受与拒绝怎样保住分布, 算完三个 token 的全部概率 (worked example),
+          好草稿也要算得便宜 (E[N] and its printed values).
+  [KB]    "投机采样" -- sections 机制：起草-验证-接受, 收益账,
+          深入推导 (pointwise identity), 参考答案 (E[n] for alpha=0.8, gamma=3).
+  [SURVEY-REPORT] "推测解码采样验证优化策略 —— 深度调研报告", part 1 section 4
+          (softmax of logits / temperature before verification).
+"""
+from __future__ import annotations
+
+import os
+from fractions import Fraction as F
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ----------------------------------------------------------------- helpers
+
+def read_golden(name: str) -> dict[str, list[str]]:
+    out = {}
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as fh:
+        for line in fh:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, val = line.split("=", 1)
+            out[key.strip()] = val.split()
+    return out
+
+
+def probs_call(orc, p_rows, q_rows, tokens, u, B=1):
+    """Single-sequence call of the probabilities entry (p rows K+1, q rows K)."""
+    p = np.asarray(p_rows, np.float64)[None].repeat(B, 0)
+    q = None if q_rows is None else np.asarray(q_rows, np.float64)[None].repeat(B, 0)
+    t = np.asarray(tokens, np.int32)[None].repeat(B, 0)
+    uu = np.asarray(u, np.float64)[None].repeat(B, 0)
+    return orc.verify_probs(p, q, t, uu)
+
+
+def _softmax64(z):
+    z = np.asarray(z, np.float64)
+    m = z[np.isfinite(z)].max()
+    e = np.exp(z - m)
+    return e / e.sum()
+
+
+def _categorical_by_library(w, u):
+    """Textbook inverse-CDF draw: smallest i with u*sum(w) < cumsum(w)[i]."""
+    c = np.cumsum(np.asarray(w, np.float64))
+    return int(np.searchsorted(c, u * c[-1], side="right"))
+
+
+# -------------------------------------------------- the pages' worked example
+
+def pin_worked_example(orc):
+    """[NOTE] 算完三个 token 的全部概率: p=(.5,.3,.2), q=(.6,.1,.3), drafts A,C,B,
+    draws .7,.9,.2 and final draw .2 emit [A, B]; A passes at 0.833, C fails
+    at 0.667, the rest is discarded."""
+    g = read_golden("worked_example.txt")
+    ids = {name: i for i, name in enumerate(g["tokens"])}
+    p = [float(F(x)) for x in g["p"]]
+    q = [float(F(x)) for x in g["q"]]
+    draft = [ids[x] for x in g["draft"]]
+    u = [float(F(x)) for x in g["draws"]] + [float(F(g["final_draw"][0]))]
+    K = len(draft)
+    r = probs_call(orc, [p] * (K + 1), [q] * K, draft, u)
+    emit = [ids[x] for x in g["emit"]]
+    assert r.status[0] == 0
+    assert r.num_emitted[0] == len(emit), r.num_emitted
+    assert list(r.out_tokens[0, :len(emit)]) == emit, r.out_tokens
+    assert (r.out_tokens[0, len(emit):] == -1).all()
+    # A accepted, C rejected, B never reached (discarded)
+    assert list(r.accept_flags[0]) == [1, 0, -1], r.accept_flags
+    assert abs(r.accept_prob[0, 0] - float(g["threshold_A"][0])) < 5e-4
+    assert abs(r.accept_prob[0, 1] - float(g["threshold_C"][0])) < 5e-4
+    # residual mass at the rejection = 1 - acceptance
+    assert abs(r.residual_mass[0] - (1 - float(F(g["acceptance"][0])))) < 1e-12
+
+
+def pin_worked_example_probabilities(orc):
+    """[NOTE] 算完三个 token 的全部概率: per-token acceptance (5/6, 1, 2/3),
+    accepted mass (.5,.1,.2), total acceptance .8."""
+    g = read_golden("worked_example.txt")
+    p = [float(F(x)) for x in g["p"]]
+    q = [float(F(x)) for x in g["q"]]
+    V = len(p)
+    r = probs_call(orc, [p] * (V + 1), [q] * V, list(range(V)), [0.0] * (V + 1))
+    want = [float(F(x)) for x in g["accept_prob_per_token"]]
+    assert np.allclose(r.accept_prob[0], want, atol=1e-15, rtol=0), r.accept_prob
+    mass = r.accept_prob[0] * np.asarray(q)
+    assert np.allclose(mass, [float(F(x)) for x in g["accepted_mass_per_token"]],
+                       atol=1e-15, rtol=0)
+    assert abs(mass.sum() - float(F(g["acceptance"][0]))) < 1e-15
+
+
+def pin_worked_example_residual(orc):
+    """[NOTE] 算完三个 token 的全部概率: the residual is (0, 1, 0) and
+    accepted mass + (1-acceptance)*residual rebuilds p.  Checked through the
+    logits path: logits = ln p at T = 1."""
+    g = read_golden("worked_example.txt")
+    p = np.array([float(F(x)) for x in g["p"]])
+    q = np.array([float(F(x)) for x in g["q"]], np.float32)
+    V = 3
+    logits = np.log(p).astype(np.float32)[None, None].repeat(V + 1, 1)
+    qq = q[None, None].repeat(V, 1)
+    tok = np.arange(V, dtype=np.int32)[None]
+    pr, w, cdf, Z = orc.row_dists(logits, qq, tok, 1.0, 0, 0, True)
+    assert np.allclose(w, [float(F(x)) for x in g["residual"]], atol=1e-6)
+    assert abs(Z - (1 - float(F(g["acceptance"][0])))) < 1e-6
+    res = orc.verify(logits, qq, tok, np.zeros((1, V + 1), np.float32), 1.0)
+    rebuilt = res.accept_prob[0] * q + Z * w
+    assert np.allclose(rebuilt, [float(F(x)) for x in g["reconstructed"]],
+                       atol=1e-6)
+
+
+# ------------------------------------------------------------- special cases
+
+def pin_p_equals_q(orc):
+    """[NOTE] 接受与拒绝怎样保住分布: if p = q every draft is accepted and the
+    correction branch is never entered; the extra token comes from p_{K+1}."""
+    rng = np.random.default_rng(11)
+    V, K, B = 9, 5, 200
+    p = rng.dirichlet(np.ones(V), size=(B, K + 1))
+    q = p[:, :K].copy()
+    tok = np.stack([[rng.choice(V, p=q[b, k]) for k in range(K)] for b in range(B)])
+    u = rng.random((B, K + 1))
+    r = orc.verify_probs(p, q, tok, u)
+    assert (r.num_emitted == K + 1).all()
+    assert (r.accept_flags == 1).all()
+    assert (r.accept_prob == 1.0).all()
+    assert (r.residual_mass == 0.0).all()
+    assert (r.out_tokens[:, :K] == tok).all()
+    for b in range(B):
+        assert r.out_tokens[b, K] == _categorical_by_library(p[b, K], u[b, K])
+
+
+def pin_k0_is_categorical(orc):
+    """K = 0 leaves only the extra token: a textbook inverse-CDF draw from
+    softmax(z / T) ([SURVEY-REPORT] part 1 section 4 for the softmax)."""
+    rng = np.random.default_rng(12)
+    from scipy.special import softmax
+    for T in (0.5, 1.0, 1.7):
+        z = rng.normal(0, 2, size=(300, 1, 37)).astype(np.float32)
+        u = rng.random((300, 1)).astype(np.float32)
+        r = orc.verify(z, None, np.zeros((300, 0), np.int32), u, T)
+        assert (r.num_emitted == 1).all()
+        for b in range(300):
+            pb = softmax(z[b, 0].astype(np.float64) / T)
+            assert r.out_tokens[b, 0] == _categorical_by_library(pb, float(u[b, 0]))
+
+
+def pin_temperature_direction(orc):
+    """softmax(z / T): z = (0, ln 3) at T = 1/2 gives p = (1/10, 9/10)."""
+    z = np.array([[[0.0, np.log(3.0)], [0.0, np.log(3.0)]]], np.float32)
+    tok = np.array([[1]], np.int32)
+    r = orc.verify(z, None, tok, np.array([[0.0, 0.0]], np.float32), 0.5)
+    # one-hot draft on token 1: acceptance probability is p(1)
+    assert abs(r.accept_prob[0, 0] - 0.9) < 1e-6, r.accept_prob
+
+
+def pin_bf16_decoding(orc):
+    """bf16 bit patterns decode as the top half of an fp32: 0x3F80 = 1,
+    0x0000 = 0, 0xFF80 = -inf, 0xC000 = -2."""
+    bits = np.array([0x3F80, 0x0000, 0xFF80, 0xC000], np.uint16)
+    logits = bits[None, None].repeat(2, 1)
+    pr, w, cdf, Z = orc.row_dists(logits, None, np.array([[0]], np.int32), 1.0,
+                                  0, 1, False)
+    e = np.array([np.e, 1.0, 0.0, np.exp(-2.0)])
+    assert np.allclose(pr, e / e.sum(), rtol=1e-14, atol=0)
+
+
+def pin_onehot_draft(orc):
+    """q = delta_x: a(x) = p(x); the residual is p with x removed and
+    renormalised (deterministic drafts, [KB] 变体谱系 N-gram row)."""
+    rng = np.random.default_rng(13)
+    V, K = 11, 3
+    z = rng.normal(0, 1.5, size=(1, K + 1, V)).astype(np.float32)
+    tok = rng.integers(0, V, size=(1, K), dtype=np.int32)
+    from scipy.special import softmax
+    u = np.zeros((1, K + 1), np.float32)
+    r = orc.verify(z, None, tok, u, 1.0)
+    for k in range(K):
+        pk = softmax(z[0, k].astype(np.float64))
+        assert abs(r.accept_prob[0, k] - pk[tok[0, k]]) < 1e-14
+        _, w, _, Z = orc.row_dists(z, None, tok, 1.0, 0, k, True)
+        want = pk.copy()
+        want[tok[0, k]] = 0.0
+        assert abs(Z - (1 - pk[tok[0, k]])) < 1e-12
+        assert np.allclose(w, want / want.sum(), rtol=1e-12, atol=1e-15)
+
+
+def pin_vocab_of_one(orc):
+    """V = 1: p = q = 1, every draft accepted, K+1 tokens, all id 0."""
+    B, K = 5, 4
+    z = np.zeros((B, K + 1, 1), np.float32)
+    q = np.ones((B, K, 1), np.float32)
+    u = np.random.default_rng(14).random((B, K + 1)).astype(np.float32)
+    r = orc.verify(z, q, np.zeros((B, K), np.int32), u, 1.0)
+    assert (r.num_emitted == K + 1).all() and (r.out_tokens == 0).all()
+
+
+def pin_strict_accept(orc):
+    """Reading of [NOTE] 算完三个 token 的全部概率 (the replay accepts iff the
+    draw is strictly below the threshold): u = a rejects, u just below accepts."""
+    p = [0.25, 0.75]
+    q = [0.5, 0.5]
+    r = probs_call(orc, [p, p], [q], [0], [0.5, 0.3])
+    assert r.accept_flags[0, 0] == 0 and r.num_emitted[0] == 1
+    r = probs_call(orc, [p, p], [q], [0], [np.nextafter(0.5, 0), 0.3])
+    assert r.accept_flags[0, 0] == 1 and r.num_emitted[0] == 2
+
+
+def pin_zero_mass_never_drawn(orc):
+    """A token of zero mass is never drawn, even by u = 0 (strict t < C(i))."""
+    p = [0.0, 0.0, 1.0, 0.0]
+    r = probs_call(orc, [p], None, [], [0.0])
+    assert r.out_tokens[0, 0] == 2
+    # residual of zero mass on ids 0, 1: draw at u = 0 lands on id 2
+    p = [0.3, 0.2, 0.5]
+    q = [0.4, 0.5, 0.1]
+    r = probs_call(orc, [p, p], [q], [1], [0.99, 0.0])
+    assert r.accept_flags[0, 0] == 0 and r.out_tokens[0, 0] == 2
+
+
+def pin_final_draw_for_correction(orc):
+    """Reading of [NOTE] 算完三个 token 的全部概率: the correction is drawn with
+    the final draw u[K], not with the draw that rejected."""
+    p = [0.5, 0.5, 0.0]
+    q = [0.0, 0.0, 1.0]
+    # draft 2 has p = 0: rejected; residual = (0.5, 0.5, 0)
+    r = probs_call(orc, [p, p, p], [q, q], [2, 2], [0.9, 0.9, 0.2])
+    assert r.out_tokens[0, 0] == 0
+    r = probs_call(orc, [p, p, p], [q, q], [2, 2], [0.2, 0.2, 0.9])
+    assert r.out_tokens[0, 0] == 1
+
+
+def pin_first_rejection_discards_rest(orc):
+    """[NOTE] 候选已知，验证才能并行: after the first rejection the later drafts
+    and their verdicts are void, even ones that would pass."""
+    p = [0.1, 0.6, 0.3]
+    q = [0.6, 0.1, 0.3]
+    # draft 0 fails (a = 1/6 < .5), drafts 1 and 2 would pass (a = 1)
+    r = probs_call(orc, [p] * 4, [q] * 3, [0, 1, 2], [0.5, 0.0, 0.0, 0.5])
+    assert r.num_emitted[0] == 1
+    assert list(r.accept_flags[0]) == [0, -1, -1]
+    assert list(r.out_tokens[0, 1:]) == [-1, -1, -1]
+    assert np.allclose(r.accept_prob[0], [1 / 6, 1, 1])
+
+
+def pin_bonus_uses_last_row(orc):
+    """[NOTE] 候选已知，验证才能并行: with every draft accepted the extra token
+    comes from p_{K+1}, the row after the last draft."""
+    K = 2
+    rows = [[1 / 3, 1 / 3, 1 / 3]] * K + [[0.0, 0.0, 1.0]]
+    r = probs_call(orc, rows, [[1 / 3] * 3] * K, [0, 1], [0.1, 0.1, 0.5])
+    assert r.num_emitted[0] == K + 1 and r.out_tokens[0, K] == 2
+
+
+def pin_batch_consistency(orc):
+    """Sequences are independent: a batch gives what each sequence gives alone."""
+    rng = np.random.default_rng(15)
+    B, K, V = 7, 3, 13
+    z = rng.normal(0, 2, size=(B, K + 1, V)).astype(np.float32)
+    q = rng.dirichlet(np.ones(V), size=(B, K)).astype(np.float32)
+    tok = rng.integers(0, V, size=(B, K), dtype=np.int32)
+    u = rng.random((B, K + 1)).astype(np.float32)
+    whole = orc.verify(z, q, tok, u, 0.9, nthreads=3)
+    for b in range(B):
+        one = orc.verify(z[b:b + 1], q[b:b + 1], tok[b:b + 1], u[b:b + 1], 0.9)
+        assert (one.out_tokens[0] == whole.out_tokens[b]).all()
+        assert one.num_emitted[0] == whole.num_emitted[b]
+        assert (one.accept_prob[0] == whole.accept_prob[b]).all()
+
+
+def pin_invalid_inputs(orc):
+    """Preconditions of [NOTE] 算完三个 token 的全部概率 (q(x) > 0, 0 <= u < 1)
+    and of a well-formed softmax row; a violating sequence emits nothing."""
+    V, K = 4, 2
+    z = np.zeros((1, K + 1, V), np.float32)
+    q = np.full((1, K, V), 0.25, np.float32)
+    tok = np.array([[1, 2]], np.int32)
+    u = np.full((1, K + 1), 0.5, np.float32)
+    import oracle as O
+
+    def run(z=z, q=q, tok=tok, u=u):
+        return orc.verify(z, q, tok, u, 1.0)
+
+    cases = []
+    u1 = u.copy(); u1[0, 2] = 1.0; cases.append((run(u=u1), O.ORC_BAD_U))
+    u2 = u.copy(); u2[0, 0] = np.nan; cases.append((run(u=u2), O.ORC_BAD_U))
+    t1 = tok.copy(); t1[0, 1] = V; cases.append((run(tok=t1), O.ORC_BAD_TOKEN))
+    t2 = tok.copy(); t2[0, 0] = -1; cases.append((run(tok=t2), O.ORC_BAD_TOKEN))
+    q1 = q.copy(); q1[0, 0, 1] = 0.0; cases.append((run(q=q1), O.ORC_BAD_Q))
+    z1 = z.copy(); z1[0, 1, :] = -np.inf; cases.append((run(z=z1), O.ORC_BAD_ROW))
+    z2 = z.copy(); z2[0, 2, 3] = np.nan; cases.append((run(z=z2), O.ORC_BAD_ROW))
+    z3 = z.copy(); z3[0, 0, 0] = np.inf; cases.append((run(z=z3), O.ORC_BAD_ROW))
+    for r, bit in cases:
+        assert r.status[0] & bit, (r.status, bit)
+        assert r.num_emitted[0] == 0
+        assert (r.out_tokens == -1).all() and (r.accept_flags == -1).all()
+    ok = run(u=np.full((1, K + 1), -0.0, np.float32))
+    assert ok.status[0] == 0 and ok.num_emitted[0] >= 1
+
+
+# ------------------------------------------------------------- invariants
+
+def pin_pointwise_identity(orc):
+    """[KB] 深入推导: q*min(1,p/q) + (1 - sum_y q(y)min(1,p(y)/q(y))) * r = p,
+    pointwise, on the oracle's own fp64 vectors."""
+    rng = np.random.default_rng(16)
+    for V in (3, 8, 50):
+        for trial in range(5):
+            z = rng.normal(0, 2, size=V)
+            zq = z + rng.normal(0, 1.0, size=V)
+            q = np.exp(zq - zq.max())
+            q = (q / q.sum()).astype(np.float32)
+            q = np.maximum(q, np.float32(1e-30))
+            logits = z.astype(np.float32)[None, None].repeat(V + 1, 1)
+            qq = q[None, None].repeat(V, 1)
+            tok = np.arange(V, dtype=np.int32)[None]
+            res = orc.verify(logits, qq, tok, np.zeros((1, V + 1), np.float32), 1.0)
+            a = res.accept_prob[0]
+            p, r, _, Z = orc.row_dists(logits, qq, tok, 1.0, 0, 0, True)
+            q64 = q.astype(np.float64)
+            beta = float(np.sum(q64 * a))
+            assert abs(Z - (1 - beta)) < 1e-12
+            assert np.max(np.abs(q64 * a + (1 - beta) * r - p)) < 1e-12
+
+
+def _sample_rows(rng, dist, n):
+    """Draw n ids from each of the rows of `dist` (test-local sampler)."""
+    c = np.cumsum(dist, axis=-1)
+    c[..., -1] = 1.0
+    return np.stack([np.searchsorted(c[j], rng.random(n), side="right")
+                     for j in range(dist.shape[0])], axis=1).astype(np.int32)
+
+
+def emitted_position_counts(orc, p, q, n_rounds, seed, chunk=200_000):
+    """Run n_rounds i.i.d. rounds (drafts ~ q, or one-hot fixed drafts when q
+    is None) and count, at every position j, the token emitted there among
+    rounds that reach j."""
+    rng = np.random.default_rng(seed)
+    K1, V = p.shape
+    K = K1 - 1
+    counts = np.zeros((K1, V), np.int64)
+    total_emitted = 0
+    sq_emitted = 0
+    done = 0
+    while done < n_rounds:
+        n = min(chunk, n_rounds - done)
+        if q is None:
+            tok = np.tile(rng.integers(0, V, size=K, dtype=np.int32), (n, 1))
+        else:
+            tok = _sample_rows(rng, q, n)
+        u = rng.random((n, K1))
+        r = orc.verify_probs(np.broadcast_to(p, (n, K1, V)),
+                             None if q is None else np.broadcast_to(q, (n, K, V)),
+                             tok, u)
+        assert (r.status == 0).all()
+        for j in range(K1):
+            reached = r.num_emitted > j
+            counts[j] += np.bincount(r.out_tokens[reached, j], minlength=V)
+        total_emitted += int(r.num_emitted.sum())
+        sq_emitted += int((r.num_emitted.astype(np.int64) ** 2).sum())
+        done += n
+    return counts, total_emitted, sq_emitted
+
+
+def pin_output_distribution(orc):
+    """[KB] 深入推导 / [NOTE] 接受与拒绝怎样保住分布: the token emitted at each
+    position, given that the round reaches it, is distributed as p_j.
+    10^6 seeded rounds, V = 3 and V = 8, chi-square at alpha = 0.001."""
+    from scipy.stats import chisquare
+    rng = np.random.default_rng(17)
+    for V, K, onehot in ((3, 3, False), (8, 4, False), (8, 3, True)):
+        p = rng.dirichlet(np.ones(V) * 0.8, size=K + 1)
+        q = None if onehot else rng.dirichlet(np.ones(V) * 0.8, size=K)
+        counts, _, _ = emitted_position_counts(orc, p, q, 1_000_000,
+                                               seed=V * 100 + K)
+        for j in range(K + 1):
+            n = counts[j].sum()
+            exp = p[j] * n
+            keep = exp > 0
+            assert counts[j][~keep].sum() == 0
+            stat, pval = chisquare(counts[j][keep], exp[keep])
+            assert pval > 1e-3, (V, K, onehot, j, pval)
+
+
+def expected_tokens_closed_form(alpha: float, gamma: int) -> float:
+    """E[N] = 1 + alpha + ... + alpha^gamma = (1 - alpha^(gamma+1)) / (1 - alpha)."""
+    return (1 - alpha ** (gamma + 1)) / (1 - alpha)
+
+
+def pin_expected_tokens(orc):
+    """[NOTE] 好草稿也要算得便宜 prints 3.3616 (alpha .8) and 4.0951 (alpha .9)
+    for gamma = 4; [KB] 参考答案 gives about 2.95 for alpha .8, gamma 3.
+    The oracle's mean tokens per round over 10^6 rounds with i.i.d.
+    acceptance alpha (sum_x min(p, q) = alpha at every position) must match
+    within 5 standard errors."""
+    assert round(expected_tokens_closed_form(0.8, 4), 4) == 3.3616
+    assert round(expected_tokens_closed_form(0.9, 4), 4) == 4.0951
+    assert round(expected_tokens_closed_form(0.8, 3), 2) == 2.95
+    rng = np.random.default_rng(18)
+    for alpha, gamma in ((0.8, 4), (0.9, 4), (0.8, 3)):
+        V = 8
+        base = rng.dirichlet(np.ones(V - 1))
+        p1 = np.append(base, 0.0)                # p(y) = 0 on the last id
+        q1 = alpha * p1
+        q1[-1] = 1 - alpha                        # sum min(p, q) = alpha
+        p = np.tile(p1, (gamma + 1, 1))
+        q = np.tile(q1, (gamma, 1))
+        n = 1_000_000
+        _, tot, sq = emitted_position_counts(orc, p, q, n, seed=int(alpha * 10) + gamma)
+        mean = tot / n
+        var = sq / n - mean ** 2
+        se = np.sqrt(var / n)
+        want = expected_tokens_closed_form(alpha, gamma)
+        assert abs(mean - want) < 5 * se, (alpha, gamma, mean, want, se)
+
+
+# ----------------------------------------------------------- brute force
+
+def _exact_round(p_rows, q_rows, draft, u):
+    """The round's outcome in exact rational arithmetic, stepping through the
+    rule of [NOTE] 接受与拒绝怎样保住分布 one draft at a time."""
+    K = len(draft)
+    out = []
+    for k in range(K):
+        x = draft[k]
+        a = min(F(1), p_rows[k][x] / q_rows[k][x])
+        if u[k] < a:
+            out.append(x)
+            continue
+        w = [max(F(0), pi - qi) for pi, qi in zip(p_rows[k], q_rows[k])]
+        break
+    else:
+        w = list(p_rows[K])
+    t = u[K] * sum(w)
+    acc = F(0)
+    for i, wi in enumerate(w):
+        acc += wi
+        if t < acc:
+            out.append(i)
+            return out
+    raise AssertionError("no token drawn")
+
+
+def pin_bruteforce_tiny(orc):
+    """V = 3, K <= 3, rational p and q: on a grid of draws (odd multiples of
+    1/128, never equal to a threshold) the oracle's outcome equals the exact
+    rational outcome at every grid point."""
+    rng = np.random.default_rng(19)
+    grid = [F(2 * i + 1, 128) for i in range(0, 64, 5)]
+    for K in (0, 1, 2, 3):
+        for trial in range(3):
+            def rand_dist():
+                c = rng.integers(1, 7, size=3)
+                c[rng.integers(0, 3)] = 0 if rng.random() < 0.3 else c[0]
+                c = [int(x) for x in c]
+                if sum(c) == 0:
+                    c = [1, 1, 1]
+                return [F(x, sum(c)) for x in c]
+            p_rows = [rand_dist() for _ in range(K + 1)]
+            q_rows = []
+            draft = []
+            for _ in range(K):
+                qd = rand_dist()
+                q_rows.append(qd)
+                draft.append(int(rng.choice([i for i in range(3) if qd[i] > 0])))
+            pts = list(np.ndindex(*([len(grid)] * (K + 1))))
+            if len(pts) > 3000:
+                pts = [pts[i] for i in rng.choice(len(pts), 3000, replace=False)]
+            us = [[grid[i] for i in pt] for pt in pts]
+            n = len(us)
+            P = np.array([[float(v) for v in row] for row in p_rows])
+            Q = None if K == 0 else np.array([[float(v) for v in row] for row in q_rows])
+            r = orc.verify_probs(np.broadcast_to(P, (n, K + 1, 3)),
+                                 None if Q is None else np.broadcast_to(Q, (n, K, 3)),
+                                 np.tile(np.array(draft, np.int32), (n, 1)).reshape(n, K),
+                                 np.array([[float(x) for x in uu] for uu in us]))
+            for b in range(n):
+                want = _exact_round(p_rows, q_rows, draft, us[b])
+                got = list(r.out_tokens[b, :r.num_emitted[b]])
+                assert got == want, (K, p_rows, q_rows, draft, us[b], got, want)
+
+
+ALL_PINS = [
+    # cheap first: mutants should fail fast
+    pin_worked_example,
+    pin_worked_example_probabilities,
+    pin_worked_example_residual,
+    pin_strict_accept,
+    pin_zero_mass_never_drawn,
+    pin_final_draw_for_correction,
+    pin_first_rejection_discards_rest,
+    pin_bonus_uses_last_row,
+    pin_temperature_direction,
+    pin_bf16_decoding,
+    pin_vocab_of_one,
+    pin_onehot_draft,
+    pin_invalid_inputs,
+    pin_p_equals_q,
+    pin_k0_is_categorical,
+    pin_batch_consistency,
+    pin_pointwise_identity,
+    pin_bruteforce_tiny,
+    pin_output_distribution,
+    pin_expected_tokens,
+]

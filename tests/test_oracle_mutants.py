@@ -1,0 +1,55 @@
+"""Plant plausible mistakes in a copy of the oracle (on the CPU) and check
+that the pins catch each one.  The committed oracle is never modified."""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "sv_oracle.c")
+
+# (name, text in sv_oracle.c, replacement, expected number of occurrences)
+MUTANTS = [
+    ("accept_le", "if (u[k] < o.accept_prob[k])", "if (u[k] <= o.accept_prob[k])", 1),
+    ("residual_no_clamp", "w[i] = d > 0.0 ? d : 0.0;", "w[i] = d;", 1),
+    ("ratio_inverted", "double a = px / qx;", "double a = qx / px;", 1),
+    ("accept_no_min", "o.accept_prob[k] = a < 1.0 ? a : 1.0;", "o.accept_prob[k] = a;", 1),
+    ("temperature_times", "/ T;", "* T;", 2),
+    ("cdf_le", "if (t < C)", "if (t <= C)", 1),
+    ("correction_uses_rejecting_draw", "inverse_cdf(w_scratch, V, u[K], &Z)",
+     "inverse_cdf(w_scratch, V, u[jstar], &Z)", 1),
+    ("bonus_row_off_by_one", "const double *prow = P + (int64_t)jstar * V;",
+     "const double *prow = P + (int64_t)(jstar > 0 ? jstar - 1 : 0) * V;", 1),
+    ("onehot_keeps_x", "double qi = onehot ? (i == x ? 1.0 : 0.0) : q[i];",
+     "double qi = onehot ? 0.0 : q[i];", 1),
+    ("row_stride_K", "(b * (K + 1) + j) * (int64_t)V, V, J->T,",
+     "(b * K + j) * (int64_t)V, V, J->T,", 1),
+    ("no_stop_at_rejection", "jstar = k;\n            break;", "jstar = k;", 1),
+    ("unnormalised_p", "p[i] /= s;", "p[i] /= 1.0;", 1),
+    ("bf16_shift", "(uint32_t)h << 16", "(uint32_t)h << 15", 1),
+    ("residual_q_next_row",
+     "rejected && Q ? Q + (int64_t)jstar * V : NULL",
+     "rejected && Q ? Q + (int64_t)(jstar + 1 < K ? jstar + 1 : jstar) * V : NULL", 1),
+    ("u_upper_inclusive", "u[k] < 1.0)", "u[k] <= 1.0)", 1),
+    ("p_of_draft_from_next_row", "double px = P[(int64_t)k * V + tok[k]];",
+     "double px = P[(int64_t)(k + 1) * V + tok[k]];", 1),
+]
+
+
+@pytest.mark.parametrize("name,old,new,count", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(tmp_path, name, old, new, count):
+    src = open(SRC, encoding="utf-8").read()
+    assert src.count(old) == count, f"mutation site for {name} not found"
+    mutant_src = tmp_path / f"mut_{name}.c"
+    mutant_src.write_text(src.replace(old, new), encoding="utf-8")
+    lib = oracle.compile_oracle(str(mutant_src), str(tmp_path / f"lib_{name}.so"))
+    mut = oracle.load(lib)
+    caught = None
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(mut)
+        except Exception as exc:  # AssertionError or a refused call
+            caught = (pin.__name__, type(exc).__name__)
+            break
+    assert caught is not None, f"no pin caught mutant {name}"
