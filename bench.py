@@ -1,0 +1,431 @@
+#!/usr/bin/env python3
+"""Benchmark of the speculative-sampling verification step on GB300.
+
+One step = one spec_verify call over a whole batch (row pass + final draw)
+with inputs resident in HBM.  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, timed on the host
+
+Multi-GPU (torchrun): every rank verifies its own batch of B sequences (its
+shard of a global batch); there is no collective on the data path, so the
+scaling is weak; the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified seqs/s and achieved HBM GB/s (% of GB300 peak) for spec_verify"
+DEFAULT_WORKLOAD = "b256_k8_v151936_bf16"
+NOMINAL_HBM_GBS = 8000.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------- byte accounting
+
+def algorithmic_bytes(w, num_emitted: np.ndarray) -> dict:
+    """Bytes each kernel must move for this batch (the algorithmic count):
+    rows kernel: every logit once, the q(x) gathers as 32-byte sectors, the
+    tokens, uniforms and its outputs; draw kernel: the surviving logit row
+    once more and, after a rejection with dense q, that q row, plus outputs."""
+    B, K, V = w.B if num_emitted is None else len(num_emitted), w.K, w.V
+    es = 2 if w.dtype == "bf16" else 4
+    rows = B * (K + 1) * V * es
+    rows += B * K * (4 + (0 if w.onehot else 32) + 4 + 1)   # tokens, q(x), a, flag
+    rows += B * (K + 1) * 4 * 2 + B * 4                        # u, out_tokens, num_emitted
+    rejected = int(np.sum(num_emitted <= K))
+    surv = B * V * es + (0 if w.onehot else rejected * V * 4) + B * (4 + 4 + 4)
+    return {"rows": rows, "survivors": surv, "total": rows + surv, "rejected": rejected}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_sampling_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per rows-kernel launch from the committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
+            d = json.load(fh)
+        e = d.get(workload)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return e.get("rows_kernel_dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle samples while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons, watts = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                watts.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        busy = [s for s in sm] or [None]
+        return {"sm_mhz": statistics.median(busy) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(watts) if watts else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import synth
+    import speculative_decoding_sampling_gb300 as sv
+    from speculative_decoding_sampling_gb300 import _native as N
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = synth.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(B=args.batch)
+    B, K, V = w.B, w.K, w.V
+
+    # this rank's shard of the global batch: sequences [rank*B, (rank+1)*B)
+    inp = synth.generate(w, b0=rank * B, nb=B)
+    host = {"logits": torch.from_numpy(inp.logits.view(np.int16) if w.dtype == "bf16" else inp.logits),
+            "q": None if inp.q is None else torch.from_numpy(inp.q),
+            "tokens": torch.from_numpy(inp.tokens), "u": torch.from_numpy(inp.u)}
+    d_logits = host["logits"].to(dev)
+    if w.dtype == "bf16":
+        d_logits = d_logits.view(torch.bfloat16)
+    d_q = None if host["q"] is None else host["q"].to(dev)
+    d_tok = host["tokens"].to(dev)
+    d_u = host["u"].to(dev)
+    out = {"out_tokens": torch.empty((B, K + 1), dtype=torch.int32, device=dev),
+           "num_emitted": torch.empty((B,), dtype=torch.int32, device=dev),
+           "accept_flags": torch.empty((B, K), dtype=torch.int8, device=dev),
+           "accept_prob": torch.empty((B, K), dtype=torch.float32, device=dev),
+           "residual_mass": torch.empty((B,), dtype=torch.float32, device=dev)}
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    need = sv.sv_workspace_bytes(B, K, V)
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    lib = N.lib()
+    dt = N.SV_BF16 if w.dtype == "bf16" else N.SV_FP32
+
+    def args_for(logits, q, tok, u, o):
+        return (logits.data_ptr(), dt, None if q is None else q.data_ptr(), tok.data_ptr(),
+                u.data_ptr(), ctypes.c_float(w.T), B, K, V, o["out_tokens"].data_ptr(),
+                o["num_emitted"].data_ptr(), o["accept_flags"].data_ptr(),
+                o["accept_prob"].data_ptr(), o["residual_mass"].data_ptr(), status.data_ptr(),
+                ws.data_ptr(), need, stream.cuda_stream)
+
+    cargs = args_for(d_logits, d_q, d_tok, d_u, out)
+
+    def step_stages(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        rc = lib.sv_verify_rows(*cargs)
+        if evs is not None:
+            evs[1].record(stream)
+        rc |= lib.sv_sample_survivors(*cargs)
+        if evs is not None:
+            evs[2].record(stream)
+        if rc:
+            raise RuntimeError(sv.sv_status_string(rc))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # warm-up (also the parity reference outputs of this batch)
+    for _ in range(max(args.warmup, 3)):
+        step_stages()
+    barrier()
+
+    # ---- timed region: K steps, per-kernel events inside it
+    clocks = ClockSampler(local)
+    clocks.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step_stages(evs[i])
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    rows_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    surv_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    ms_step = ms_total / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    num_emitted = out["num_emitted"].cpu().numpy()
+    st = int(status.item())
+    tokens_per_step = int(num_emitted.sum())
+    nbytes = algorithmic_bytes(w, num_emitted)
+    peak, peak_kind = peaks()
+    rows_avg = sum(rows_ms) / len(rows_ms)
+    surv_avg = sum(surv_ms) / len(surv_ms)
+    rows_gbs = nbytes["rows"] / (rows_avg * 1e-3) / 1e9
+    step_gbs = nbytes["total"] / (ms_step * 1e-3) / 1e9
+
+    # ---- end to end through the public call with pinned host buffers
+    e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 10))
+    pin = {k: (v.pin_memory() if (v is not None and e2e_steps) else v) for k, v in host.items()}
+    h_out = {"out_tokens": torch.empty((B, K + 1), dtype=torch.int32).pin_memory(),
+             "num_emitted": torch.empty((B,), dtype=torch.int32).pin_memory()}
+    h2d = sum(v.numel() * v.element_size() for v in pin.values() if v is not None)
+    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
+    e_logits = torch.empty_like(host["logits"], device=dev) if e2e_steps else None
+    e_q = None if (d_q is None or not e2e_steps) else torch.empty_like(d_q)
+    e_tok = torch.empty_like(d_tok)
+    e_u = torch.empty_like(d_u)
+
+    def e2e_step():
+        e_logits.copy_(pin["logits"], non_blocking=True)
+        if e_q is not None:
+            e_q.copy_(pin["q"], non_blocking=True)
+        e_tok.copy_(pin["tokens"], non_blocking=True)
+        e_u.copy_(pin["u"], non_blocking=True)
+        lg = e_logits.view(torch.bfloat16) if w.dtype == "bf16" else e_logits
+        res = sv.spec_verify(lg, e_q, e_tok, e_u, w.T, out=out, workspace=ws, status=status)
+        h_out["out_tokens"].copy_(res.out_tokens, non_blocking=True)
+        h_out["num_emitted"].copy_(res.num_emitted, non_blocking=True)
+
+    e2e_ms = float("nan")
+    if e2e_steps:
+        e2e_step()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    result = None
+    if rank == 0:
+        seqs = B * world
+        cpu = None
+        parity_note = None
+        if not args.no_cpu_baseline:
+            cpu, parity_note = cpu_baseline_and_check(w, inp, out, args.cpu_seconds)
+        result = {
+            "metric": METRIC,
+            "value": seqs / (ms_step * 1e-3),
+            "unit": "seqs/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms_step,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic (seeded Philox4x32-10 generator; shapes and value "
+                    "distributions of the workload; no model weights or datasets)",
+            "config": {"workload": w.name, "B_per_gpu": B, "K": K, "V": V,
+                       "logits_dtype": w.dtype, "draft": "one-hot ids" if w.onehot else "dense q fp32",
+                       "temperature": w.T, "top_p": w.top_p or None,
+                       "l2": "inputs larger than L2 (%.0f MB > 129 MB), no flush" %
+                             ((B * (K + 1) * V * (2 if w.dtype == 'bf16' else 4)) / 1e6),
+                       "parallelism": f"replicas x{world} (shard over sequences)"},
+            "tokens_per_s": tokens_per_step * world / (ms_step * 1e-3),
+            "hbm_gbs_step": step_gbs,
+            "hbm_frac_of_8tbs_step": step_gbs / NOMINAL_HBM_GBS,
+            "kernels_ms": {"rows": rows_avg, "survivors": surv_avg},
+            "algorithmic_bytes": nbytes,
+            "roofline": {"bound": "hbm", "kernel": "rows_kernel",
+                         "achieved": rows_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": rows_gbs / peak, "peak_source": peak_kind,
+                         "traffic": recorded_traffic(w.name)},
+            "e2e": {"value": seqs / (e2e_ms * 1e-3), "unit": "seqs/s",
+                    "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk,
+            "status_bits": st,
+            "cpu_baseline": cpu,
+            "parity": parity_note,
+        }
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+def cpu_baseline_and_check(w, inp, out, seconds):
+    """Time the oracle as it stands on this host's cores over the whole batch
+    (repeated until `seconds` elapse) and check the GPU outputs against it."""
+    import oracle
+    from oracle import parity
+    orc = oracle.load()
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    passes = 0
+    ref = None
+    while True:
+        ref = orc.verify(inp.logits, inp.q, inp.tokens, inp.u, inp.T, nthreads=cores)
+        passes += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    cand = {k: out[k].cpu().numpy() for k in out}
+    rep = parity.compare(orc, inp.logits, inp.q, inp.tokens, inp.u, inp.T, cand, oracle_res=ref)
+    cpu = {"value": passes * inp.B / el, "unit": "seqs/s", "cores": cores, "kind": "oracle",
+           "sample": f"all {inp.B} sequences of the workload, {passes} passes, {el:.1f} s wall"}
+    return cpu, {"ok": rep.ok(), "summary": rep.summary()}
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    """The fp64 CPU oracle, timed as it stands on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return None
+    import oracle
+    import synth
+    w = synth.WORKLOADS[args.workload]
+    orc = oracle.load()
+    cores = os.cpu_count() or 1
+    # calibrate, then size each step's sample so the whole run stays ~60 s
+    calib = synth.generate(w, nb=min(w.B, cores))
+    t0 = time.perf_counter()
+    orc.verify(calib.logits, calib.q, calib.tokens, calib.u, calib.T, nthreads=cores)
+    rate = calib.B / max(time.perf_counter() - t0, 1e-6)
+    n_steps = args.steps + args.warmup
+    per_step = max(1, min(w.B, int(rate * 60.0 / max(n_steps, 1))))
+    inp = synth.generate(w, nb=per_step)
+    for _ in range(args.warmup):
+        orc.verify(inp.logits, inp.q, inp.tokens, inp.u, inp.T, nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.verify(inp.logits, inp.q, inp.tokens, inp.u, inp.T, nthreads=cores)
+    el = time.perf_counter() - t0
+    ms = el * 1e3 / args.steps
+    value = per_step / (el / args.steps)
+    sample = (f"first {per_step} of the {w.B} sequences of the workload per step, "
+              f"fp64 oracle, {cores} threads")
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "seqs/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B_per_gpu": w.B, "K": w.K, "V": w.V,
+                   "logits_dtype": w.dtype, "draft": "one-hot ids" if w.onehot else "dense q fp32"},
+        "cpu_baseline": {"value": value, "unit": "seqs/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "seqs/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--batch", type=int, default=0, help="override B (profiling runs)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    res = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

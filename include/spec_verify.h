@@ -1,0 +1,154 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 speculative-sampling verification
+ * library (libspecverify.so, sm_103a).
+ *
+ * The operation (one call verifies a whole batch of B sequences):
+ *
+ *   for every sequence b and target row j = 0..K:
+ *       p_j = softmax(z_{b,j} / T)
+ *     ("推测解码采样验证优化策略 —— 深度调研报告", part 1 section 4, verify():
+ *      the softmax of target logits / temperature; "推测解码：草稿、验证与实际加速",
+ *      section 接受与拒绝怎样保住分布: p already carries the temperature and q is
+ *      passed exactly as the draft used it)
+ *   row j verifies draft x_{j+1} (0-based: row k verifies draft k); row K only
+ *   serves the extra token ("推测解码：草稿、验证与实际加速", section
+ *   候选已知，验证才能并行, the equation listing p_1 .. p_4);
+ *   drafts are tested left to right, draft k accepted iff
+ *       u[b,k] < a_k,  a_k = min(1, p_k(x_k) / q_k(x_k))
+ *     (same page, section 接受与拒绝怎样保住分布, equation for a(x));
+ *   at the first rejection j*, one token is drawn from
+ *       r = max(0, p_{j*} - q_{j*}) / sum(max(0, p_{j*} - q_{j*}))
+ *     and later drafts are discarded; if all K drafts pass, one extra token is
+ *     drawn from p_K (same page, equation for r(x); "投机采样", section
+ *     机制：起草-验证-接受: each round emits n in [1, K+1] tokens);
+ *   the draw uses the final uniform u[b,K]: the token is the smallest id i
+ *     with u[b,K] * sum(w) < w_0 + ... + w_i ("推测解码：草稿、验证与实际加速",
+ *     section 算完三个 token 的全部概率, the replay's sampler and final draw).
+ *   A deterministic draft (n-gram, prompt lookup) is q = one-hot on x: pass
+ *   draft_probs = NULL; then a_k = min(1, p_k(x_k)) and r is p without x.
+ *
+ * Conventions for every entry point below:
+ *   - All tensor pointers are DEVICE pointers, row-major and contiguous, owned
+ *     by the caller.  The library allocates nothing and keeps no state beyond
+ *     the caller's workspace; calls on distinct workspaces are independent.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  A return of SV_OK means the work was enqueued.
+ *   - Host-side checks run before anything is launched and return SV_EINVAL
+ *     (null pointer, K < 0, B < 0, V < 1, temperature not finite or <= 0,
+ *     misaligned pointer, workspace too small) or SV_EUNSUPPORTED (V above
+ *     SV_MAX_V, or a batch too large for one launch).  B == 0 is a no-op.
+ *     Launch failures return SV_ECUDA.  Nothing traps on the device.
+ *   - Bad DATA is reported on the device: the sequence's outputs are set to
+ *     "nothing emitted" (num_emitted 0, tokens and flags -1, probabilities 0)
+ *     and SV_BAD_* bits are OR-ed into *status_dev (when not NULL).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SV_OK = 0,
+    SV_EINVAL = 1,
+    SV_ECUDA = 2,
+    SV_EUNSUPPORTED = 3
+} sv_status_t;
+
+typedef enum { SV_BF16 = 0, SV_FP32 = 1 } sv_dtype_t;
+
+/* Device status bits OR-ed into *status_dev. */
+#define SV_BAD_U 1               /* a uniform outside [0, 1) or NaN          */
+#define SV_BAD_TOKEN 2           /* a draft token outside [0, V)             */
+#define SV_BAD_Q 4               /* q_k(x_k) <= 0 or not finite (dense q)    */
+#define SV_BAD_ROW 8             /* a logit row with NaN / +inf / no finite  */
+#define SV_DEGENERATE_RESIDUAL 16 /* residual mass 0 after a rejection: the  */
+                                  /* token was drawn from p instead          */
+
+/* Largest vocabulary supported. */
+#define SV_MAX_V (1 << 24)
+
+/* Bytes of workspace spec_verify needs for (B, K, V).  The workspace must be
+ * zero-filled before its first use.  A completed spec_verify (or the two
+ * stages below, in order) returns every byte it used to zero, so the same
+ * workspace can serve later calls of any shape that fits in it without being
+ * cleared.  Two calls that may run at the same time need distinct
+ * workspaces. */
+size_t sv_workspace_bytes(int64_t B, int32_t K, int32_t V);
+
+/* Verify a batch.
+ *   target_logits  [B, K+1, V] bf16 or fp32 (logits_dtype); row j of sequence
+ *                  b at offset (b*(K+1) + j) * V.  -inf entries are allowed
+ *                  (masked tokens).  2-byte (bf16) / 4-byte (fp32) aligned.
+ *   draft_probs    [B, K, V] fp32, the draft's processed distribution q, or
+ *                  NULL for one-hot drafts.  4-byte aligned.
+ *   draft_tokens   [B, K] int32 (may be NULL when K == 0).
+ *   uniforms       [B, K+1] fp32 in [0, 1); u[b,k] tests draft k, u[b,K] is
+ *                  the final draw used for the correction or extra token.
+ *   temperature    T > 0, applied to the target logits only.
+ * Outputs:
+ *   out_tokens     [B, K+1] int32: accepted drafts, then the drawn token, then
+ *                  -1 padding.
+ *   num_emitted    [B] int32 in [1, K+1] (0 for a sequence with bad data).
+ *   accept_flags   [B, K] int8: 1 accepted, 0 the first rejection, -1 not
+ *                  reached.  May be NULL.
+ *   accept_prob    [B, K] fp32: a_k for every draft (also those not reached).
+ *                  May be NULL.
+ *   residual_mass  [B] fp32: sum(max(0, p_{j*} - q_{j*})) at the rejection,
+ *                  0 when the extra token was drawn.  May be NULL.
+ *   status_dev     one device int32; SV_BAD_* bits are OR-ed in.  May be NULL.
+ *   workspace      device scratch of at least sv_workspace_bytes(B, K, V)
+ *                  bytes, 256-byte aligned (see sv_workspace_bytes).
+ */
+sv_status_t spec_verify(const void *target_logits, sv_dtype_t logits_dtype,
+                        const float *draft_probs, const int32_t *draft_tokens,
+                        const float *uniforms, float temperature, int64_t B,
+                        int32_t K, int32_t V, int32_t *out_tokens,
+                        int32_t *num_emitted, int8_t *accept_flags,
+                        float *accept_prob, float *residual_mass,
+                        int32_t *status_dev, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/* The two stages of spec_verify, for callers that time or schedule them
+ * separately.  Same arguments and meaning as spec_verify.
+ *
+ * sv_verify_rows: the row pass over all B*(K+1) rows (max and softmax
+ * normaliser of every row, the accept test of every draft), then per sequence
+ * the first rejection; writes accept_flags, accept_prob, num_emitted, the
+ * accepted prefix of out_tokens and its -1 padding, and leaves in the
+ * workspace which row each sequence draws its final token from.
+ *
+ * sv_sample_survivors: per sequence, the draw of the final token from the
+ * residual (after a rejection) or from p_K (all accepted); writes
+ * out_tokens[b, num_emitted-1] and residual_mass.  Must follow
+ * sv_verify_rows on the same stream with the same workspace and inputs. */
+sv_status_t sv_verify_rows(const void *target_logits, sv_dtype_t logits_dtype,
+                           const float *draft_probs,
+                           const int32_t *draft_tokens, const float *uniforms,
+                           float temperature, int64_t B, int32_t K, int32_t V,
+                           int32_t *out_tokens, int32_t *num_emitted,
+                           int8_t *accept_flags, float *accept_prob,
+                           float *residual_mass, int32_t *status_dev,
+                           void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+sv_status_t sv_sample_survivors(
+    const void *target_logits, sv_dtype_t logits_dtype,
+    const float *draft_probs, const int32_t *draft_tokens,
+    const float *uniforms, float temperature, int64_t B, int32_t K, int32_t V,
+    int32_t *out_tokens, int32_t *num_emitted, int8_t *accept_flags,
+    float *accept_prob, float *residual_mass, int32_t *status_dev,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char *sv_status_string(sv_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,51 @@
+"""ctypes view of libspecverify.so (the C ABI declared in include/spec_verify.h)."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB
+
+SV_OK, SV_EINVAL, SV_ECUDA, SV_EUNSUPPORTED = 0, 1, 2, 3
+SV_BF16, SV_FP32 = 0, 1
+SV_BAD_U, SV_BAD_TOKEN, SV_BAD_Q, SV_BAD_ROW, SV_DEGENERATE_RESIDUAL = 1, 2, 4, 8, 16
+SV_MAX_V = 1 << 24
+
+# every function the header declares, in declaration order
+EXPORTS = ["sv_workspace_bytes", "spec_verify", "sv_verify_rows",
+           "sv_sample_survivors", "sv_status_string"]
+
+_VERIFY_ARGTYPES = [
+    ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+    ctypes.c_void_p, ctypes.c_float, ctypes.c_int64, ctypes.c_int32,
+    ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+    ctypes.c_size_t, ctypes.c_void_p]
+
+_lib = None
+
+
+class NativeLibraryMissing(RuntimeError):
+    pass
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library.  Raises if it has not been built: there is no
+    fallback implementation."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise NativeLibraryMissing(
+                f"{LIB} is missing; build it with "
+                "`python -m speculative_decoding_sampling_gb300.build`")
+        L = ctypes.CDLL(LIB)
+        L.sv_workspace_bytes.restype = ctypes.c_size_t
+        L.sv_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]
+        for name in ("spec_verify", "sv_verify_rows", "sv_sample_survivors"):
+            fn = getattr(L, name)
+            fn.restype = ctypes.c_int
+            fn.argtypes = _VERIFY_ARGTYPES
+        L.sv_status_string.restype = ctypes.c_char_p
+        L.sv_status_string.argtypes = [ctypes.c_int]
+        _lib = L
+    return _lib

@@ -1,0 +1,190 @@
+"""PyTorch binding of the C ABI: argument marshalling only.
+
+Every step of the verification runs in the CUDA kernels of
+libspecverify.so; this module checks shapes and dtypes, allocates outputs
+and the workspace through PyTorch, and passes raw device pointers and the
+current CUDA stream.  The function names are those of the C ABI.
+"""
+from __future__ import annotations
+
+import threading
+from dataclasses import dataclass
+
+import torch
+
+from . import _native as N
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, code: int):
+        self.code = code
+        super().__init__(sv_status_string(code))
+
+
+def sv_status_string(code: int) -> str:
+    return N.lib().sv_status_string(int(code)).decode()
+
+
+def sv_workspace_bytes(B: int, K: int, V: int) -> int:
+    return int(N.lib().sv_workspace_bytes(int(B), int(K), int(V)))
+
+
+_ws_lock = threading.Lock()
+_ws_cache: dict[int, torch.Tensor] = {}
+
+
+def default_workspace(device: torch.device, nbytes: int) -> torch.Tensor:
+    """A zero-filled workspace of at least `nbytes` on `device`, shared by the
+    calls that do not pass their own.  The kernels leave it zero-filled, so
+    calls ordered on one stream may reuse it; calls that may overlap (other
+    streams) must pass distinct workspaces."""
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    with _ws_lock:
+        ws = _ws_cache.get(idx)
+        if ws is None or ws.numel() < nbytes:
+            ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=f"cuda:{idx}")
+            _ws_cache[idx] = ws
+        return ws
+
+
+@dataclass
+class SpecVerifyResult:
+    out_tokens: torch.Tensor            # int32 [B, K+1], -1 padded
+    num_emitted: torch.Tensor           # int32 [B]
+    accept_flags: torch.Tensor          # int8  [B, K]
+    accept_prob: torch.Tensor | None    # fp32  [B, K]
+    residual_mass: torch.Tensor | None  # fp32  [B]
+    status: torch.Tensor | None         # int32 [1], OR of SV_BAD_* bits
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _check(t: torch.Tensor, name: str, dtype, shape, device):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.device != device:
+        raise ValueError(f"{name}: expected device {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+def _call(fn_name: str, target_logits, draft_probs, draft_tokens, uniforms,
+          temperature, out_tokens, num_emitted, accept_flags, accept_prob,
+          residual_mass, status, workspace, stream):
+    if not target_logits.is_cuda:
+        raise ValueError("target_logits must be a CUDA tensor")
+    dev = target_logits.device
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be [B, K+1, V]")
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    if K < 0:
+        raise ValueError("target_logits needs K+1 >= 1 rows per sequence")
+    if target_logits.dtype == torch.bfloat16:
+        dt = N.SV_BF16
+    elif target_logits.dtype == torch.float32:
+        dt = N.SV_FP32
+    else:
+        raise TypeError("target_logits must be bfloat16 or float32")
+    if not target_logits.is_contiguous():
+        raise ValueError("target_logits must be contiguous")
+    if draft_probs is not None:
+        _check(draft_probs, "draft_probs", torch.float32, (B, K, V), dev)
+    if draft_tokens is None:
+        if K > 0:
+            raise ValueError("draft_tokens required when K > 0")
+    else:
+        _check(draft_tokens, "draft_tokens", torch.int32, (B, K), dev)
+    _check(uniforms, "uniforms", torch.float32, (B, K + 1), dev)
+    for name, t, dtype, shape in (("out_tokens", out_tokens, torch.int32, (B, K + 1)),
+                                  ("num_emitted", num_emitted, torch.int32, (B,)),
+                                  ("accept_flags", accept_flags, torch.int8, (B, K)),
+                                  ("accept_prob", accept_prob, torch.float32, (B, K)),
+                                  ("residual_mass", residual_mass, torch.float32, (B,)),
+                                  ("status", status, torch.int32, (1,))):
+        if t is not None:
+            _check(t, name, dtype, shape, dev)
+    need = sv_workspace_bytes(B, K, V)
+    if need == 0 and B > 0:
+        raise SpecVerifyError(N.SV_EUNSUPPORTED)
+    if workspace is None:
+        workspace = default_workspace(dev, need)
+    elif workspace.device != dev or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must hold {need} bytes on {dev}")
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    rc = getattr(N.lib(), fn_name)(
+        target_logits.data_ptr(), dt, _ptr(draft_probs), _ptr(draft_tokens),
+        uniforms.data_ptr(), float(temperature), B, K, V, _ptr(out_tokens),
+        _ptr(num_emitted), _ptr(accept_flags), _ptr(accept_prob),
+        _ptr(residual_mass), _ptr(status), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), stream.cuda_stream)
+    if rc != N.SV_OK:
+        raise SpecVerifyError(rc)
+
+
+def _outputs(target_logits, want_probs, out):
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    dev = target_logits.device
+    o = dict(out or {})
+    o.setdefault("out_tokens", torch.empty((B, K + 1), dtype=torch.int32, device=dev))
+    o.setdefault("num_emitted", torch.empty((B,), dtype=torch.int32, device=dev))
+    o.setdefault("accept_flags", torch.empty((B, K), dtype=torch.int8, device=dev))
+    if want_probs:
+        o.setdefault("accept_prob", torch.empty((B, K), dtype=torch.float32, device=dev))
+        o.setdefault("residual_mass", torch.empty((B,), dtype=torch.float32, device=dev))
+    o.setdefault("accept_prob", None)
+    o.setdefault("residual_mass", None)
+    o.setdefault("status", None)
+    return o
+
+
+def spec_verify(target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
+                draft_tokens: torch.Tensor | None, uniforms: torch.Tensor,
+                temperature: float, *, want_probs: bool = True,
+                out: dict | None = None, status: torch.Tensor | None = None,
+                workspace: torch.Tensor | None = None,
+                stream: torch.cuda.Stream | None = None) -> SpecVerifyResult:
+    """Verify a batch of drafts against target logits on the GPU.
+
+    target_logits [B, K+1, V] bf16/fp32; draft_probs [B, K, V] fp32 or None
+    (one-hot drafts); draft_tokens [B, K] int32; uniforms [B, K+1] fp32 in
+    [0, 1) with uniforms[:, K] the final draw; temperature > 0.
+    `out` may supply preallocated output tensors by name; `status` an int32
+    [1] device tensor that receives SV_BAD_* bits.  Runs asynchronously on
+    `stream` (default: the current stream)."""
+    o = _outputs(target_logits, want_probs, out)
+    if status is not None:
+        o["status"] = status
+    _call("spec_verify", target_logits, draft_probs, draft_tokens, uniforms,
+          temperature, o["out_tokens"], o["num_emitted"], o["accept_flags"],
+          o["accept_prob"], o["residual_mass"], o["status"], workspace, stream)
+    return SpecVerifyResult(o["out_tokens"], o["num_emitted"], o["accept_flags"],
+                            o["accept_prob"], o["residual_mass"], o["status"])
+
+
+def sv_verify_rows(target_logits, draft_probs, draft_tokens, uniforms,
+                   temperature, *, out: dict, workspace: torch.Tensor,
+                   stream=None) -> None:
+    """First stage of spec_verify (see the C header); `out` as returned in
+    the fields of a SpecVerifyResult."""
+    _call("sv_verify_rows", target_logits, draft_probs, draft_tokens, uniforms,
+          temperature, out["out_tokens"], out["num_emitted"],
+          out.get("accept_flags"), out.get("accept_prob"),
+          out.get("residual_mass"), out.get("status"), workspace, stream)
+
+
+def sv_sample_survivors(target_logits, draft_probs, draft_tokens, uniforms,
+                        temperature, *, out: dict, workspace: torch.Tensor,
+                        stream=None) -> None:
+    """Second stage of spec_verify; must follow sv_verify_rows on the same
+    stream, workspace and inputs."""
+    _call("sv_sample_survivors", target_logits, draft_probs, draft_tokens,
+          uniforms, temperature, out["out_tokens"], out["num_emitted"],
+          out.get("accept_flags"), out.get("accept_prob"),
+          out.get("residual_mass"), out.get("status"), workspace, stream)

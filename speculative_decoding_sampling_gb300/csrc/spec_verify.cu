@@ -1,0 +1,248 @@
+// spec_verify.cu -- C ABI of the verification library: argument checks,
+// workspace layout, and the two launches (row pass, survivor draw) on the
+// caller's stream.  The operation itself is documented in spec_verify.h.
+#include "spec_verify.h"
+
+#include <cmath>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "sv_device.cuh"
+#include "sv_rows.cuh"
+#include "sv_survivor.cuh"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+int ceil_log2_u64(uint64_t v)
+{
+    int n = 0;
+    while ((uint64_t{1} << n) < v)
+        ++n;
+    return n;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// How the work of one call is cut, a function of (B, K, V) only.
+struct Plan {
+    int64_t R;      // rows B*(K+1)
+    int32_t S1;     // chunks per row in the row pass
+    int32_t CL;     // CTAs per survivor cluster
+    int32_t fix;    // fractional bits of the fixed-point masses
+    size_t off_part, off_row_cnt, off_row_m, off_seq_m, off_acc, off_seq_cnt, off_seq_bad, off_jstar, bytes;
+};
+
+bool make_plan(int64_t B, int32_t K, int32_t V, Plan &p)
+{
+    if (B < 0 || K < 0 || V < 1 || V > SV_MAX_V)
+        return false;
+    if (B > 0 && static_cast<int64_t>(K) + 1 > INT64_MAX / B)
+        return false;
+    p.R = B * (static_cast<int64_t>(K) + 1);
+    if (p.R > 0 && V > INT64_MAX / p.R)
+        return false;
+    // ~32K elements per chunk; more chunks when there are few rows, so that
+    // a small batch still spreads over the GPU; at least 4K elements each
+    int64_t s1 = ceil_div(V, 32768);
+    if (p.R > 0) {
+        const int64_t spread = ceil_div(1216, p.R);
+        const int64_t finest = ceil_div(V, 4096);
+        const int64_t want = spread < finest ? spread : finest;
+        if (want > s1)
+            s1 = want;
+    }
+    if (s1 > 64)
+        s1 = 64;
+    if (s1 < 1)
+        s1 = 1;
+    p.S1 = static_cast<int32_t>(s1);
+    int64_t cl = ceil_div(V, 16384);
+    p.CL = static_cast<int32_t>(cl < 1 ? 1 : (cl > sv::kMaxCluster ? sv::kMaxCluster : cl));
+    const int fb = 62 - ceil_log2_u64(static_cast<uint64_t>(V) + 1);
+    p.fix = fb < 40 ? fb : 40;
+    size_t off = 0;
+    p.off_part = off;    off = align_up(off + static_cast<size_t>(p.R) * p.S1 * sizeof(float2));
+    p.off_row_cnt = off; off = align_up(off + static_cast<size_t>(p.R) * sizeof(uint32_t));
+    p.off_row_m = off;   off = align_up(off + static_cast<size_t>(p.R) * sizeof(float));
+    p.off_seq_m = off;   off = align_up(off + static_cast<size_t>(B) * sizeof(float));
+    p.off_acc = off;     off = align_up(off + static_cast<size_t>(B) * K * sizeof(uint8_t));
+    p.off_seq_cnt = off; off = align_up(off + static_cast<size_t>(B) * sizeof(uint32_t));
+    p.off_seq_bad = off; off = align_up(off + static_cast<size_t>(B) * sizeof(int32_t));
+    p.off_jstar = off;   off = align_up(off + static_cast<size_t>(B) * sizeof(int32_t));
+    p.bytes = off;
+    return true;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+enum Stage { kRows = 1, kSurvivors = 2, kBoth = 3 };
+
+template <typename LT, bool DENSE>
+cudaError_t launch(const sv::Params &P, const Plan &plan, int stages, cudaStream_t stream)
+{
+    if (stages & kRows) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(plan.R * plan.S1));
+        cfg.blockDim = dim3(sv::kRowThreads);
+        cfg.stream = stream;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, sv::rows_kernel<LT, DENSE>, P);
+        if (e != cudaSuccess)
+            return e;
+    }
+    if (stages & kSurvivors) {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(plan.CL);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(P.B * plan.CL));
+        cfg.blockDim = dim3(sv::kSurvThreads);
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, sv::survivor_kernel<LT, DENSE>, P);
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
+}
+
+sv_status_t run(int stages, const void *logits, sv_dtype_t dtype, const float *q, const int32_t *tokens,
+                const float *u, float T, int64_t B, int32_t K, int32_t V, int32_t *out_tokens,
+                int32_t *num_emitted, int8_t *accept_flags, float *accept_prob, float *residual_mass,
+                int32_t *status_dev, void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (B < 0 || K < 0 || V < 1)
+        return SV_EINVAL;
+    if (V > SV_MAX_V)
+        return SV_EUNSUPPORTED;
+    if (dtype != SV_BF16 && dtype != SV_FP32)
+        return SV_EINVAL;
+    if (!std::isfinite(T) || !(T > 0.0f))
+        return SV_EINVAL;
+    const double c64 = 1.4426950408889634074 / static_cast<double>(T);
+    const float c = static_cast<float>(c64);
+    if (!std::isfinite(c) || !(c > 0.0f))
+        return SV_EINVAL;
+    if (!logits || !u || !out_tokens || !num_emitted || (K > 0 && !tokens) || !workspace)
+        return SV_EINVAL;
+    const size_t esize = dtype == SV_BF16 ? 2 : 4;
+    if (!aligned(logits, esize) || (q && !aligned(q, 4)) || (tokens && !aligned(tokens, 4)) ||
+        !aligned(u, 4) || !aligned(out_tokens, 4) || !aligned(num_emitted, 4) ||
+        (accept_prob && !aligned(accept_prob, 4)) || (residual_mass && !aligned(residual_mass, 4)) ||
+        (status_dev && !aligned(status_dev, 4)) || !aligned(workspace, kAlign))
+        return SV_EINVAL;
+    Plan plan;
+    if (!make_plan(B, K, V, plan))
+        return SV_EUNSUPPORTED;
+    if (workspace_bytes < plan.bytes)
+        return SV_EINVAL;
+    if (B == 0)
+        return SV_OK;
+    if (plan.R * plan.S1 > INT32_MAX || B * plan.CL > INT32_MAX)
+        return SV_EUNSUPPORTED;
+
+    char *ws = static_cast<char *>(workspace);
+    sv::Params P;
+    P.logits = logits;
+    P.q = K > 0 ? q : nullptr;
+    P.tokens = tokens;
+    P.u = u;
+    P.c = c;
+    P.B = B;
+    P.K = K;
+    P.V = V;
+    P.out_tokens = out_tokens;
+    P.num_emitted = num_emitted;
+    P.accept_flags = accept_flags;
+    P.accept_prob = accept_prob;
+    P.residual_mass = residual_mass;
+    P.status = status_dev;
+    P.row_part = reinterpret_cast<float2 *>(ws + plan.off_part);
+    P.row_cnt = reinterpret_cast<uint32_t *>(ws + plan.off_row_cnt);
+    P.row_m = reinterpret_cast<float *>(ws + plan.off_row_m);
+    P.seq_m = reinterpret_cast<float *>(ws + plan.off_seq_m);
+    P.acc = reinterpret_cast<uint8_t *>(ws + plan.off_acc);
+    P.seq_cnt = reinterpret_cast<uint32_t *>(ws + plan.off_seq_cnt);
+    P.seq_bad = reinterpret_cast<int32_t *>(ws + plan.off_seq_bad);
+    P.seq_jstar = reinterpret_cast<int32_t *>(ws + plan.off_jstar);
+    P.S1 = plan.S1;
+    P.CL = plan.CL;
+    P.fix_bits = plan.fix;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    const bool dense = P.q != nullptr;
+    if (dtype == SV_BF16)
+        e = dense ? launch<uint16_t, true>(P, plan, stages, s) : launch<uint16_t, false>(P, plan, stages, s);
+    else
+        e = dense ? launch<float, true>(P, plan, stages, s) : launch<float, false>(P, plan, stages, s);
+    return e == cudaSuccess ? SV_OK : SV_ECUDA;
+}
+
+} // namespace
+
+extern "C" {
+
+size_t sv_workspace_bytes(int64_t B, int32_t K, int32_t V)
+{
+    Plan p;
+    if (!make_plan(B, K, V, p))
+        return 0;
+    return p.bytes;
+}
+
+sv_status_t spec_verify(const void *target_logits, sv_dtype_t logits_dtype, const float *draft_probs,
+                        const int32_t *draft_tokens, const float *uniforms, float temperature, int64_t B,
+                        int32_t K, int32_t V, int32_t *out_tokens, int32_t *num_emitted, int8_t *accept_flags,
+                        float *accept_prob, float *residual_mass, int32_t *status_dev, void *workspace,
+                        size_t workspace_bytes, void *stream)
+{
+    return run(kBoth, target_logits, logits_dtype, draft_probs, draft_tokens, uniforms, temperature, B, K, V,
+               out_tokens, num_emitted, accept_flags, accept_prob, residual_mass, status_dev, workspace,
+               workspace_bytes, stream);
+}
+
+sv_status_t sv_verify_rows(const void *target_logits, sv_dtype_t logits_dtype, const float *draft_probs,
+                           const int32_t *draft_tokens, const float *uniforms, float temperature, int64_t B,
+                           int32_t K, int32_t V, int32_t *out_tokens, int32_t *num_emitted, int8_t *accept_flags,
+                           float *accept_prob, float *residual_mass, int32_t *status_dev, void *workspace,
+                           size_t workspace_bytes, void *stream)
+{
+    return run(kRows, target_logits, logits_dtype, draft_probs, draft_tokens, uniforms, temperature, B, K, V,
+               out_tokens, num_emitted, accept_flags, accept_prob, residual_mass, status_dev, workspace,
+               workspace_bytes, stream);
+}
+
+sv_status_t sv_sample_survivors(const void *target_logits, sv_dtype_t logits_dtype, const float *draft_probs,
+                                const int32_t *draft_tokens, const float *uniforms, float temperature, int64_t B,
+                                int32_t K, int32_t V, int32_t *out_tokens, int32_t *num_emitted,
+                                int8_t *accept_flags, float *accept_prob, float *residual_mass,
+                                int32_t *status_dev, void *workspace, size_t workspace_bytes, void *stream)
+{
+    return run(kSurvivors, target_logits, logits_dtype, draft_probs, draft_tokens, uniforms, temperature, B, K,
+               V, out_tokens, num_emitted, accept_flags, accept_prob, residual_mass, status_dev, workspace,
+               workspace_bytes, stream);
+}
+
+const char *sv_status_string(sv_status_t status)
+{
+    switch (status) {
+    case SV_OK:
+        return "SV_OK: work enqueued";
+    case SV_EINVAL:
+        return "SV_EINVAL: invalid argument (null or misaligned pointer, bad size, temperature or workspace)";
+    case SV_ECUDA:
+        return "SV_ECUDA: a CUDA launch failed";
+    case SV_EUNSUPPORTED:
+        return "SV_EUNSUPPORTED: size beyond what one call supports";
+    }
+    return "unknown sv_status_t";
+}
+
+} // extern "C"

@@ -1,0 +1,176 @@
+"""Seeded synthetic inputs for the speculative-sampling verification step.
+
+The generator (``synth.c``, Philox4x32-10, multithreaded) writes the same
+host bytes that both the CUDA library and the oracle consume; it contains
+none of the verification arithmetic.  Workloads follow the shapes and value
+distributions of the five configurations the verification step is measured
+on (see ``WORKLOADS``); the pages' own evaluation data (ShareGPT, GSM8K,
+MBPP on DeepSeek-V4-Flash) is not available, and these distributions stand
+in for it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass, replace
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "synth.c")
+_LIB = os.path.join(_HERE, "_build", "libsynth.so")
+
+DEFAULT_SEED = 20261202
+
+
+class _Cfg(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int), ("K", ctypes.c_int32),
+                ("V", ctypes.c_int32), ("sigma", ctypes.c_double),
+                ("zipf_s", ctypes.c_double), ("T", ctypes.c_double),
+                ("draft_sigma", ctypes.c_double), ("Tq", ctypes.c_double),
+                ("top_p", ctypes.c_double), ("onehot_p", ctypes.c_double)]
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One input recipe.  dtype: "bf16" or "fp32"; Tq = 0 means one-hot
+    drafts (no q tensor)."""
+    name: str
+    B: int
+    K: int
+    V: int
+    dtype: str
+    sigma: float
+    zipf_s: float
+    T: float
+    draft_sigma: float
+    Tq: float
+    top_p: float = 0.0
+    onehot_p: float = 0.0
+
+    @property
+    def onehot(self) -> bool:
+        return self.Tq <= 0.0
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+WORKLOADS = {
+    # B=1, K=4, V=32000: fp32 logits N(0, 2^2); q = softmax(z + N(0, .5^2)); T=1
+    "b1_k4_v32000_fp32": Workload("b1_k4_v32000_fp32", 1, 4, 32000, "fp32",
+                                  2.0, 0.0, 1.0, 0.5, 1.0),
+    # B=8, K=4, V=32000: bf16 N(0, 3^2) + Zipf(1.1); q from z + N(0, 1); T=.8 on both
+    "b8_k4_v32000_bf16": Workload("b8_k4_v32000_bf16", 8, 4, 32000, "bf16",
+                                  3.0, 1.1, 0.8, 1.0, 0.8),
+    # B=64, K=5, V=128256: bf16 N(0, 3^2) + Zipf(1.1); q from z + N(0, .7^2);
+    # T=1; top-p 0.9 on both p and q
+    "b64_k5_v128256_bf16_topp": Workload("b64_k5_v128256_bf16_topp", 64, 5,
+                                         128256, "bf16", 3.0, 1.1, 1.0, 0.7,
+                                         1.0, top_p=0.9),
+    # B=256, K=8, V=151936: bf16 N(0, 4^2) + Zipf(1.2); q from z + N(0, 1.5^2); T=.7
+    "b256_k8_v151936_bf16": Workload("b256_k8_v151936_bf16", 256, 8, 151936,
+                                     "bf16", 4.0, 1.2, 0.7, 1.5, 0.7),
+    # B=128, K=8, V=128256: bf16 N(0, 3^2) + Zipf(1.1); T=.7; one-hot drafts:
+    # the target argmax with probability 0.6, else uniform over V
+    "b128_k8_v128256_bf16_onehot": Workload("b128_k8_v128256_bf16_onehot", 128,
+                                            8, 128256, "bf16", 3.0, 1.1, 0.7,
+                                            0.0, 0.0, onehot_p=0.6),
+}
+# the five configurations in their usual order
+CONFIGS = list(WORKLOADS.values())
+
+
+def compile_synth(out: str = _LIB) -> str:
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
+                    "-ffp-contract=off", "-pthread", "-o", out, _SRC, "-lm"],
+                   check=True)
+    return out
+
+
+def build() -> str:
+    if not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        compile_synth()
+    return _LIB
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(build())
+        L.synth_generate.restype = ctypes.c_int
+        L.synth_generate.argtypes = [ctypes.POINTER(_Cfg), ctypes.c_uint64,
+                                     ctypes.c_int64, ctypes.c_int64,
+                                     ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_int]
+        L.synth_philox4x32_10.restype = None
+        L.synth_philox4x32_10.argtypes = [ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_void_p]
+        L.synth_f32_to_bf16.restype = None
+        L.synth_f32_to_bf16.argtypes = [ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_int64]
+        _lib = L
+    return _lib
+
+
+@dataclass
+class Inputs:
+    """Host inputs of one call.  logits: uint16 bf16 bits or float32."""
+    workload: Workload
+    logits: np.ndarray        # [B, K+1, V]
+    q: np.ndarray | None      # [B, K, V] float32, None for one-hot drafts
+    tokens: np.ndarray        # [B, K] int32
+    u: np.ndarray             # [B, K+1] float32
+    T: float
+    b0: int = 0
+
+    @property
+    def B(self) -> int:
+        return self.logits.shape[0]
+
+
+def generate(w: Workload | str, seed: int = DEFAULT_SEED, b0: int = 0,
+             nb: int | None = None, nthreads: int | None = None) -> Inputs:
+    """Sequences [b0, b0+nb) of workload `w` for `seed` (default: all B)."""
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    nb = w.B - b0 if nb is None else nb
+    K, V = w.K, w.V
+    cfg = _Cfg(0 if w.dtype == "bf16" else 1, K, V, w.sigma, w.zipf_s, w.T,
+               w.draft_sigma, w.Tq, w.top_p, w.onehot_p)
+    logits = np.empty((nb, K + 1, V), np.uint16 if w.dtype == "bf16" else np.float32)
+    q = None if w.onehot else np.empty((nb, K, V), np.float32)
+    tokens = np.empty((nb, K), np.int32)
+    u = np.empty((nb, K + 1), np.float32)
+    nthreads = nthreads or os.cpu_count() or 1
+    rc = lib().synth_generate(ctypes.byref(cfg), seed, b0, nb, logits.ctypes.data,
+                              None if q is None else q.ctypes.data,
+                              tokens.ctypes.data, u.ctypes.data, int(nthreads))
+    if rc != 0:
+        raise RuntimeError("synth_generate failed")
+    return Inputs(w, logits, q, tokens, u, w.T, b0)
+
+
+def philox4x32_10(ctr, key) -> list[int]:
+    c = (ctypes.c_uint32 * 4)(*ctr)
+    k = (ctypes.c_uint32 * 2)(*key)
+    o = (ctypes.c_uint32 * 4)()
+    lib().synth_philox4x32_10(c, k, o)
+    return list(o)
+
+
+def f32_to_bf16(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, np.float32)
+    out = np.empty(x.shape, np.uint16)
+    lib().synth_f32_to_bf16(x.ctypes.data, out.ctypes.data, x.size)
+    return out
+
+
+def bf16_to_f32(h: np.ndarray) -> np.ndarray:
+    return (np.asarray(h, np.uint16).astype(np.uint32) << 16).view(np.float32)

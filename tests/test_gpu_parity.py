@@ -1,0 +1,181 @@
+"""GPU path (through the C ABI) against the fp64 oracle on seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import parity
+
+import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(orc, inp, cand, seqs=None):
+    rep = parity.compare(orc, inp.logits, inp.q, inp.tokens, inp.u, inp.T, cand, seqs=seqs)
+    assert rep.ok(), rep.summary()
+    return rep
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_config_full_size(orc, name):
+    """Each of the five configurations at full size, every sequence checked."""
+    inp = synth.generate(name)
+    cand = G.run_inputs(inp)
+    assert cand["status"] == 0
+    rep = _check(orc, inp, cand)
+    print(name, rep.summary())
+
+
+SHAPES = [(1, 1), (3, 0), (7, 1), (8, 4), (9, 2), (31, 16), (257, 8), (4097, 4),
+          (16385, 3), (40000, 5)]
+
+
+@pytest.mark.parametrize("V,K", SHAPES, ids=[f"V{v}_K{k}" for v, k in SHAPES])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("onehot", [False, True], ids=["dense", "onehot"])
+def test_shapes(orc, V, K, dtype, onehot):
+    """Ragged vocabularies (scalar heads and tails, several tiles, one to
+    eight cluster CTAs), K from 0 to 16, both dtypes and both draft modes."""
+    base = synth.WORKLOADS["b8_k4_v32000_bf16"]
+    w = base.with_(name="shape", B=24, K=K, V=V, dtype=dtype,
+                   Tq=0.0 if onehot else 0.8, onehot_p=0.5 if onehot else 0.0)
+    inp = synth.generate(w, seed=1000 + V + 17 * K)
+    cand = G.run_inputs(inp)
+    assert cand["status"] == 0
+    _check(orc, inp, cand)
+
+
+def test_topp_masked_rows_and_zero_mass_drafts(orc):
+    """-inf (masked) logits everywhere outside a nucleus, and drafts whose
+    target probability is exactly 0 (always rejected)."""
+    w = synth.WORKLOADS["b64_k5_v128256_bf16_topp"].with_(B=16, V=5000)
+    inp = synth.generate(w, seed=7)
+    masked = inp.logits == 0xFF80
+    assert masked.mean() > 0.5
+    # point some drafts at masked tokens: p(x) = 0, q(x) > 0
+    rng = np.random.default_rng(3)
+    for b in range(0, 16, 2):
+        k = rng.integers(0, w.K)
+        cand_ids = np.nonzero(masked[b, k] & (inp.q[b, k] > 0))[0]
+        if len(cand_ids):
+            inp.tokens[b, k] = cand_ids[0]
+        else:
+            x = np.nonzero(masked[b, k])[0][0]
+            inp.q[b, k, x] = 1e-3
+            inp.tokens[b, k] = x
+    cand = G.run_inputs(inp)
+    _check(orc, inp, cand)
+
+
+def test_extreme_uniforms(orc):
+    """u = 0 and u = the largest float below 1, for accept tests and the draw."""
+    w = synth.WORKLOADS["b8_k4_v32000_bf16"].with_(B=32, V=3000)
+    inp = synth.generate(w, seed=8)
+    top = np.nextafter(np.float32(1), np.float32(0))
+    inp.u[::2] = 0.0
+    inp.u[1::2] = top
+    cand = G.run_inputs(inp)
+    _check(orc, inp, cand)
+
+
+def test_p_equals_q_all_accepted(orc):
+    """q(x) = p(x) exactly: one finite logit per row and one-hot q give
+    p = q = 1 at the draft, so every draft is accepted."""
+    B, K, V = 16, 6, 777
+    rng = np.random.default_rng(9)
+    logits = np.full((B, K + 1, V), -np.inf, np.float32)
+    ids = rng.integers(0, V, size=(B, K + 1))
+    for b in range(B):
+        for j in range(K + 1):
+            logits[b, j, ids[b, j]] = 0.5
+    q = np.zeros((B, K, V), np.float32)
+    for b in range(B):
+        for k in range(K):
+            q[b, k, ids[b, k]] = 1.0
+    tok = ids[:, :K].astype(np.int32)
+    u = rng.random((B, K + 1)).astype(np.float32)
+    inp = synth.Inputs(None, logits, q, tok, u, 1.3)
+    cand = G.run_inputs(inp)
+    assert (cand["num_emitted"] == K + 1).all()
+    assert (cand["out_tokens"] == ids).all()
+    _check(orc, inp, cand)
+
+
+def test_bad_inputs_report_and_emit_nothing(orc):
+    """Bad data sets status bits, that sequence emits nothing, others are unaffected."""
+    import speculative_decoding_sampling_gb300 as sv
+    w = synth.WORKLOADS["b8_k4_v32000_bf16"].with_(B=8, V=1000)
+    inp = synth.generate(w, seed=10)
+    inp.u[1, 2] = 1.0                       # bad uniform
+    inp.tokens[2, 1] = 1000                 # token out of range
+    inp.q[3, 0, inp.tokens[3, 0]] = 0.0     # q(x) = 0
+    inp.logits[4, 3, :] = 0xFF80            # row all -inf
+    inp.logits[5, 0, 17] = 0x7FC0           # NaN logit
+    inp.u[6, 4] = np.nan                    # bad final draw
+    cand = G.run_inputs(inp)
+    want = sv.SV_BAD_U | sv.SV_BAD_TOKEN | sv.SV_BAD_Q | sv.SV_BAD_ROW
+    assert cand["status"] == want, cand["status"]
+    for b in range(1, 7):
+        assert cand["num_emitted"][b] == 0 and (cand["out_tokens"][b] == -1).all()
+    _check(orc, inp, cand)
+
+
+def test_deterministic_and_workspace_reuse(orc):
+    """One workspace reused across calls of different shapes gives the same
+    results as a fresh one: every call returns its counters to zero."""
+    import speculative_decoding_sampling_gb300 as sv
+    inp1 = synth.generate("b64_k5_v128256_bf16_topp", nb=12)
+    inp2 = synth.generate("b128_k8_v128256_bf16_onehot", nb=20)
+    d1, d2 = G.to_device(inp1), G.to_device(inp2)
+    need = max(sv.sv_workspace_bytes(12, 5, 128256), sv.sv_workspace_bytes(20, 8, 128256))
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda:0")
+    a = G.run(*d1, inp1.T, workspace=ws)
+    assert int(ws.count_nonzero().item()) == 0
+    b = G.run(*d2, inp2.T, workspace=ws)
+    assert int(ws.count_nonzero().item()) == 0
+    a2 = G.run(*d1, inp1.T, workspace=ws)
+    b2 = G.run(*d2, inp2.T, workspace=torch.zeros_like(ws))
+    for k in ("out_tokens", "num_emitted", "accept_flags", "accept_prob", "residual_mass"):
+        assert np.array_equal(a[k], a2[k]), k
+        assert np.array_equal(b[k], b2[k]), k
+    _check(orc, inp1, a)
+    _check(orc, inp2, b)
+
+
+def test_stages_equal_whole_call(orc):
+    import speculative_decoding_sampling_gb300 as sv
+    inp = synth.generate("b128_k8_v128256_bf16_onehot", nb=16)
+    logits, q, tok, u = G.to_device(inp)
+    whole = G.run(logits, q, tok, u, inp.T)
+    B, K = inp.tokens.shape
+    V = inp.logits.shape[2]
+    dev = logits.device
+    out = {"out_tokens": torch.empty((B, K + 1), dtype=torch.int32, device=dev),
+           "num_emitted": torch.empty((B,), dtype=torch.int32, device=dev),
+           "accept_flags": torch.empty((B, K), dtype=torch.int8, device=dev),
+           "accept_prob": torch.empty((B, K), dtype=torch.float32, device=dev),
+           "residual_mass": torch.empty((B,), dtype=torch.float32, device=dev)}
+    ws = torch.zeros(sv.sv_workspace_bytes(B, K, V), dtype=torch.uint8, device=dev)
+    sv.sv_verify_rows(logits, q, tok, u, inp.T, out=out, workspace=ws)
+    sv.sv_sample_survivors(logits, q, tok, u, inp.T, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    for k in out:
+        assert np.array_equal(out[k].cpu().numpy(), whole[k]), k
+
+
+def test_misaligned_base_pointers(orc):
+    """Tensors that start off a 16-byte boundary take the scalar paths."""
+    w = synth.WORKLOADS["b8_k4_v32000_bf16"].with_(B=6, V=2051)
+    inp = synth.generate(w, seed=12)
+    B, K1, V = inp.logits.shape
+    flat = torch.empty(B * K1 * V + 3, dtype=torch.bfloat16, device="cuda:0")
+    logits = flat[3:].view(B, K1, V)
+    logits.copy_(G.host_logits_tensor(inp.logits))
+    qflat = torch.empty(B * (K1 - 1) * V + 1, dtype=torch.float32, device="cuda:0")
+    q = qflat[1:].view(B, K1 - 1, V)
+    q.copy_(torch.from_numpy(inp.q))
+    tok = torch.from_numpy(inp.tokens).cuda()
+    u = torch.from_numpy(inp.u).cuda()
+    cand = G.run(logits, q, tok, u, inp.T)
+    _check(orc, inp, cand)
