@@ -1,0 +1,85 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_sampling_gb300 as sv
+from speculative_decoding_sampling_gb300 import _native as N
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f), encoding="utf-8").read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[a-z_][a-z0-9_]*\s*\**\s*([a-z_][a-z0-9_]*)\s*\(",
+                                text, flags=re.M)
+    return names
+
+
+def test_library_exports_every_declared_function():
+    lib = N.lib()
+    names = declared_functions()
+    assert "spec_verify" in names and "sv_workspace_bytes" in names
+    for name in names:
+        assert hasattr(lib, name), name
+    # the binding's list covers the header's original entry points
+    for name in N.EXPORTS:
+        assert name in names
+
+
+def test_status_strings():
+    for code in (N.SV_OK, N.SV_EINVAL, N.SV_ECUDA, N.SV_EUNSUPPORTED):
+        assert sv.sv_status_string(code).startswith("SV_")
+    assert "unknown" in sv.sv_status_string(99)
+
+
+def test_workspace_size_is_a_function_of_shape():
+    a = sv.sv_workspace_bytes(256, 8, 151936)
+    assert a > 0 and a % 256 == 0
+    assert a == sv.sv_workspace_bytes(256, 8, 151936)
+    assert sv.sv_workspace_bytes(0, 4, 100) >= 0
+    assert sv.sv_workspace_bytes(-1, 4, 100) == 0
+    assert sv.sv_workspace_bytes(1, 4, 0) == 0
+    assert sv.sv_workspace_bytes(1, 4, N.SV_MAX_V + 1) == 0
+
+
+def _call(**kw):
+    """spec_verify with plausible (fake, never dereferenced) device pointers."""
+    fake = 1 << 40
+    args = dict(logits=fake, dtype=N.SV_BF16, q=fake, tok=fake, u=fake, T=1.0, B=4, K=3,
+                V=1000, out=fake, n=fake, flags=None, prob=None, mass=None, status=None,
+                ws=fake, ws_bytes=1 << 20, stream=None)
+    args.update(kw)
+    return N.lib().spec_verify(args["logits"], args["dtype"], args["q"], args["tok"],
+                               args["u"], ctypes.c_float(args["T"]), args["B"], args["K"],
+                               args["V"], args["out"], args["n"], args["flags"],
+                               args["prob"], args["mass"], args["status"], args["ws"],
+                               args["ws_bytes"], args["stream"])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(logits=None), dict(u=None), dict(out=None), dict(n=None), dict(ws=None),
+    dict(tok=None), dict(T=0.0), dict(T=-1.0), dict(T=float("nan")), dict(T=float("inf")),
+    dict(T=1e-45), dict(B=-1), dict(K=-1), dict(V=0), dict(dtype=7),
+    dict(logits=(1 << 40) + 1), dict(ws=(1 << 40) + 16), dict(u=(1 << 40) + 2),
+    dict(ws_bytes=16),
+], ids=lambda d: ",".join(f"{k}" for k in d))
+def test_host_checks_reject_without_launching(kw):
+    # every case returns before any CUDA call, so no GPU is needed
+    assert _call(**kw) == N.SV_EINVAL
+
+
+def test_unsupported_sizes():
+    assert _call(V=N.SV_MAX_V + 1) == N.SV_EUNSUPPORTED
+
+
+def test_empty_batch_is_a_noop():
+    assert _call(B=0, ws_bytes=0) == N.SV_OK
