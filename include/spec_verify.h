@@ -144,6 +144,39 @@ sv_status_t sv_sample_survivors(
     float *accept_prob, float *residual_mass, int32_t *status_dev,
     void *workspace, size_t workspace_bytes, void *stream);
 
+/* Allocation-free variant of spec_verify.  The pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory,
+ * for example a server whose device memory is reserved up front by its own
+ * pool and that forbids cudaMalloc on the request path, or a plugin interface
+ * that hands a plugin its input and output buffers but no allocator.
+ *
+ * Same arguments and results as spec_verify, without the workspace: the
+ * scratch is a fixed array of SV_NOALLOC_SCRATCH_BYTES in the library's
+ * device image, present on every GPU that loads the library until the
+ * process exits.  The caller still passes all inputs and outputs.
+ *   - Returns SV_EUNSUPPORTED when sv_workspace_bytes(B, K, V) exceeds
+ *     SV_NOALLOC_SCRATCH_BYTES (1 MiB holds, e.g., B = 256, K = 8 at any V).
+ *   - Calls no cudaMalloc / cudaFree and no allocating library routine.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the one array: each call clears the
+ *     bytes it uses (an asynchronous memset on `stream`) and then launches.
+ *     Calls whose work may overlap on the GPU (different streams or host
+ *     threads without ordering between them) race on the array and give
+ *     undefined results; order them on one stream. */
+#define SV_NOALLOC_SCRATCH_BYTES (1u << 20)
+sv_status_t spec_verify_noalloc(const void *target_logits,
+                                sv_dtype_t logits_dtype,
+                                const float *draft_probs,
+                                const int32_t *draft_tokens,
+                                const float *uniforms, float temperature,
+                                int64_t B, int32_t K, int32_t V,
+                                int32_t *out_tokens, int32_t *num_emitted,
+                                int8_t *accept_flags, float *accept_prob,
+                                float *residual_mass, int32_t *status_dev,
+                                void *stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char *sv_status_string(sv_status_t status);
 

@@ -246,3 +246,76 @@ const char *sv_status_string(sv_status_t status)
 }
 
 } // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.  Some callers cannot hand the library a
+// workspace: a server whose device memory is reserved up front by its own
+// pool and that forbids cudaMalloc on the request path, or a plugin interface
+// that passes a plugin its input and output buffers but no allocator.  For
+// them, spec_verify_noalloc runs the same two kernels with their scratch in a
+// fixed-size array that lives in the library's device image.  The array is
+// shared by every call on a device and keeps the last call's contents, so
+// each call clears the bytes it needs before launching; calls that overlap on
+// the GPU (two streams, two host threads) race on it.
+#include <mutex>
+
+namespace {
+constexpr size_t kNoallocScratchBytes = SV_NOALLOC_SCRATCH_BYTES;
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kNoallocMaxDevices] = {};
+} // namespace
+
+// Every GPU that loads this library holds this array until the process exits.
+static __device__ __align__(256) unsigned char g_sv_noalloc_scratch[kNoallocScratchBytes];
+
+namespace {
+// The device address of the scratch array on the current device.  The host
+// symbol is only a stand-in for the array, so the address is looked up once
+// per device (with that device current) and cached.
+sv_status_t noalloc_scratch(void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return SV_ECUDA;
+    if (dev < 0 || dev >= kNoallocMaxDevices)
+        return SV_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_sv_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return SV_ECUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return SV_OK;
+}
+} // namespace
+
+extern "C" sv_status_t spec_verify_noalloc(const void *target_logits, sv_dtype_t logits_dtype,
+                                           const float *draft_probs, const int32_t *draft_tokens,
+                                           const float *uniforms, float temperature, int64_t B, int32_t K,
+                                           int32_t V, int32_t *out_tokens, int32_t *num_emitted,
+                                           int8_t *accept_flags, float *accept_prob, float *residual_mass,
+                                           int32_t *status_dev, void *stream)
+{
+    Plan plan;
+    if (make_plan(B, K, V, plan) && plan.bytes > kNoallocScratchBytes)
+        return SV_EUNSUPPORTED; // this batch needs more scratch than the array holds
+    void *scratch = nullptr;
+    sv_status_t st = noalloc_scratch(&scratch);
+    if (st != SV_OK)
+        return st;
+    // host checks only (stage mask 0 launches nothing)
+    st = run(0, target_logits, logits_dtype, draft_probs, draft_tokens, uniforms, temperature, B, K, V,
+             out_tokens, num_emitted, accept_flags, accept_prob, residual_mass, status_dev, scratch,
+             kNoallocScratchBytes, stream);
+    if (st != SV_OK || B == 0)
+        return st;
+    // the kernels expect zeroed scratch; a previous call may not have finished cleanly
+    if (cudaMemsetAsync(scratch, 0, plan.bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SV_ECUDA;
+    return run(kBoth, target_logits, logits_dtype, draft_probs, draft_tokens, uniforms, temperature, B, K, V,
+               out_tokens, num_emitted, accept_flags, accept_prob, residual_mass, status_dev, scratch,
+               kNoallocScratchBytes, stream);
+}

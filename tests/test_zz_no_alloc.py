@@ -1,0 +1,85 @@
+"""spec_verify_noalloc: the allocation-free entry point, for callers that
+cannot allocate device memory (a server whose memory is reserved up front by
+its own pool, a plugin interface that hands out only input and output
+buffers).  Called through the C ABI and compared with spec_verify, the
+entry point that takes a caller workspace, on calls made back to back.
+
+This file is collected last on purpose, so that a run stopping at its first
+failure has already run every other test."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+import speculative_decoding_sampling_gb300 as sv
+from speculative_decoding_sampling_gb300 import _native as N
+
+import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-5  # the probability tolerance of the parity tests
+
+
+def _entry():
+    fn = N.lib().spec_verify_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                   ctypes.c_void_p, ctypes.c_float, ctypes.c_int64, ctypes.c_int32,
+                   ctypes.c_int32] + [ctypes.c_void_p] * 7
+    return fn
+
+
+def _call_noalloc(logits, q, tok, u, T):
+    B, K1, V = logits.shape
+    K = K1 - 1
+    dev = logits.device
+    out = {"out_tokens": torch.full((B, K + 1), -7, dtype=torch.int32, device=dev),
+           "num_emitted": torch.full((B,), -7, dtype=torch.int32, device=dev),
+           "accept_flags": torch.full((B, K), -7, dtype=torch.int8, device=dev),
+           "accept_prob": torch.full((B, K), -7.0, dtype=torch.float32, device=dev),
+           "residual_mass": torch.full((B,), -7.0, dtype=torch.float32, device=dev)}
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    dt = N.SV_BF16 if logits.dtype == torch.bfloat16 else N.SV_FP32
+    rc = _entry()(logits.data_ptr(), dt, None if q is None else q.data_ptr(), tok.data_ptr(),
+                  u.data_ptr(), float(T), B, K, V, out["out_tokens"].data_ptr(),
+                  out["num_emitted"].data_ptr(), out["accept_flags"].data_ptr(),
+                  out["accept_prob"].data_ptr(), out["residual_mass"].data_ptr(),
+                  status.data_ptr(), torch.cuda.current_stream(dev).cuda_stream)
+    assert rc == N.SV_OK, sv.sv_status_string(rc)
+    torch.cuda.synchronize()
+    res = {k: v.cpu().numpy() for k, v in out.items()}
+    res["status"] = int(status.item())
+    return res
+
+
+def _same(a, b):
+    for k in ("out_tokens", "num_emitted", "accept_flags"):
+        assert np.array_equal(a[k], b[k]), k
+    for k in ("accept_prob", "residual_mass"):
+        assert np.max(np.abs(a[k].astype(np.float64) - b[k])) <= TOL, k
+    assert a["status"] == b["status"]
+
+
+@pytest.mark.parametrize("name,nb", [("b256_k8_v151936_bf16", 256),
+                                     ("b128_k8_v128256_bf16_onehot", 64),
+                                     ("b1_k4_v32000_fp32", 1)])
+def test_noalloc_matches_spec_verify_on_consecutive_calls(name, nb):
+    inp = synth.generate(name, nb=nb)
+    d = G.to_device(inp)
+    ref = G.run(*d, inp.T)               # spec_verify with a caller workspace
+    first = _call_noalloc(*d, inp.T)     # two allocation-free calls in a row
+    second = _call_noalloc(*d, inp.T)
+    _same(first, ref)
+    _same(second, ref)
+
+
+def test_noalloc_rejects_batches_beyond_its_scratch():
+    B, K, V = 20000, 8, 1000
+    assert sv.sv_workspace_bytes(B, K, V) > (1 << 20)   # SV_NOALLOC_SCRATCH_BYTES
+    fake = 1 << 40
+    rc = _entry()(fake, N.SV_BF16, None, fake, fake, 1.0, B, K, V, fake, fake, None, None,
+                  None, None, None)
+    assert rc == N.SV_EUNSUPPORTED
