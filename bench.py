@@ -71,14 +71,14 @@ def kernel_source_hash() -> str:
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per rows-kernel launch from the committed ncu summary, if it
+    """DRAM bytes per verify_kernel launch from the committed ncu summary, if it
     was taken on the current kernel source; else None."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
             d = json.load(fh)
         e = d.get(workload)
         if e and e.get("source_hash") == kernel_source_hash():
-            return e.get("rows_kernel_dram_bytes_per_launch")
+            return e.get("verify_kernel_dram_bytes_per_launch")
     except Exception:
         pass
     return None
@@ -193,15 +193,13 @@ def run_gpu(args):
 
     cargs = args_for(d_logits, d_q, d_tok, d_u, out)
 
-    def step_stages(evs=None):
+    def step(evs=None):
+        # one call = one launch of the persistent verification kernel
         if evs is not None:
             evs[0].record(stream)
-        rc = lib.sv_verify_rows(*cargs)
+        rc = lib.spec_verify(*cargs)
         if evs is not None:
             evs[1].record(stream)
-        rc |= lib.sv_sample_survivors(*cargs)
-        if evs is not None:
-            evs[2].record(stream)
         if rc:
             raise RuntimeError(sv.sv_status_string(rc))
 
@@ -212,25 +210,24 @@ def run_gpu(args):
 
     # warm-up (also the parity reference outputs of this batch)
     for _ in range(max(args.warmup, 3)):
-        step_stages()
+        step()
     barrier()
 
     # ---- timed region: K steps, per-kernel events inside it
     clocks = ClockSampler(local)
     clocks.start()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     barrier()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
-        step_stages(evs[i])
+        step(evs[i])
     t_end.record(stream)
     barrier()
     clk = clocks.stop()
     ms_total = t_start.elapsed_time(t_end)
-    rows_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    surv_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    kern_ms = [e[0].elapsed_time(e[1]) for e in evs]
     ms_step = ms_total / args.steps
     if world > 1:
         t = torch.tensor([ms_step], device=dev)
@@ -242,9 +239,8 @@ def run_gpu(args):
     tokens_per_step = int(num_emitted.sum())
     nbytes = algorithmic_bytes(w, num_emitted)
     peak, peak_kind = peaks()
-    rows_avg = sum(rows_ms) / len(rows_ms)
-    surv_avg = sum(surv_ms) / len(surv_ms)
-    rows_gbs = nbytes["rows"] / (rows_avg * 1e-3) / 1e9
+    kern_avg = sum(kern_ms) / len(kern_ms)
+    kern_gbs = nbytes["total"] / (kern_avg * 1e-3) / 1e9
     step_gbs = nbytes["total"] / (ms_step * 1e-3) / 1e9
 
     # ---- end to end through the public call with pinned host buffers
@@ -317,16 +313,16 @@ def run_gpu(args):
             "tokens_per_s": tokens_per_step * world / (ms_step * 1e-3),
             "hbm_gbs_step": step_gbs,
             "hbm_frac_of_8tbs_step": step_gbs / NOMINAL_HBM_GBS,
-            "kernels_ms": {"rows": rows_avg, "survivors": surv_avg},
+            "kernels_ms": {"verify_kernel": kern_avg},
             "algorithmic_bytes": nbytes,
-            "roofline": {"bound": "hbm", "kernel": "rows_kernel",
-                         "achieved": rows_gbs, "peak": peak, "unit": "GB/s",
-                         "frac": rows_gbs / peak, "peak_source": peak_kind,
+            "roofline": {"bound": "hbm", "kernel": "verify_kernel",
+                         "achieved": kern_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": kern_gbs / peak, "peak_source": peak_kind,
                          "traffic": recorded_traffic(w.name)},
             "e2e": {"value": seqs / (e2e_ms * 1e-3), "unit": "seqs/s",
                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": args.steps,
             "clocks": clk,
             "status_bits": st,
             "cpu_baseline": cpu,

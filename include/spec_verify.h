@@ -68,9 +68,12 @@ typedef enum { SV_BF16 = 0, SV_FP32 = 1 } sv_dtype_t;
 #define SV_BAD_ROW 8             /* a logit row with NaN / +inf / no finite  */
 #define SV_DEGENERATE_RESIDUAL 16 /* residual mass 0 after a rejection: the  */
                                   /* token was drawn from p instead          */
+#define SV_INTERNAL_TIMEOUT 32   /* a bounded wait inside a kernel ran out  */
+                                  /* (never expected): outputs are undefined */
+                                  /* and the workspace must be re-zeroed     */
 
 /* Largest vocabulary supported. */
-#define SV_MAX_V (1 << 24)
+#define SV_MAX_V (1 << 21)
 
 /* Bytes of workspace spec_verify needs for (B, K, V).  The workspace must be
  * zero-filled before its first use.  A completed spec_verify (or the two
@@ -155,7 +158,7 @@ sv_status_t sv_sample_survivors(
  * device image, present on every GPU that loads the library until the
  * process exits.  The caller still passes all inputs and outputs.
  *   - Returns SV_EUNSUPPORTED when sv_workspace_bytes(B, K, V) exceeds
- *     SV_NOALLOC_SCRATCH_BYTES (1 MiB holds, e.g., B = 256, K = 8 at any V).
+ *     SV_NOALLOC_SCRATCH_BYTES (4 MiB holds, e.g., B = 256, K = 8 at V = 151936).
  *   - Calls no cudaMalloc / cudaFree and no allocating library routine.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
@@ -165,7 +168,7 @@ sv_status_t sv_sample_survivors(
  *     Calls whose work may overlap on the GPU (different streams or host
  *     threads without ordering between them) race on the array and give
  *     undefined results; order them on one stream. */
-#define SV_NOALLOC_SCRATCH_BYTES (1u << 20)
+#define SV_NOALLOC_SCRATCH_BYTES (4u << 20)
 sv_status_t spec_verify_noalloc(const void *target_logits,
                                 sv_dtype_t logits_dtype,
                                 const float *draft_probs,

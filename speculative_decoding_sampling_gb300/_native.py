@@ -9,7 +9,8 @@ from .build import LIB
 SV_OK, SV_EINVAL, SV_ECUDA, SV_EUNSUPPORTED = 0, 1, 2, 3
 SV_BF16, SV_FP32 = 0, 1
 SV_BAD_U, SV_BAD_TOKEN, SV_BAD_Q, SV_BAD_ROW, SV_DEGENERATE_RESIDUAL = 1, 2, 4, 8, 16
-SV_MAX_V = 1 << 24
+SV_INTERNAL_TIMEOUT = 32
+SV_MAX_V = 1 << 21
 
 # every function the header declares, in declaration order
 EXPORTS = ["sv_workspace_bytes", "spec_verify", "sv_verify_rows",

@@ -1,13 +1,13 @@
 // spec_verify.cu -- C ABI of the verification library: argument checks,
-// workspace layout, and the two launches (row pass, survivor draw) on the
+// workspace layout, and the two launches (row pass, final draws) on the
 // caller's stream.  The operation itself is documented in spec_verify.h.
 #include "spec_verify.h"
 
 #include <cmath>
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <mutex>
 
-#include "sv_device.cuh"
 #include "sv_rows.cuh"
 #include "sv_survivor.cuh"
 
@@ -27,13 +27,15 @@ int ceil_log2_u64(uint64_t v)
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// How the work of one call is cut, a function of (B, K, V) only.
+// How the work of one call is cut and where its scratch lives: a function of
+// (B, K, V) only.
 struct Plan {
-    int64_t R;      // rows B*(K+1)
-    int32_t S1;     // chunks per row in the row pass
-    int32_t CL;     // CTAs per survivor cluster
-    int32_t fix;    // fractional bits of the fixed-point masses
-    size_t off_part, off_row_cnt, off_row_m, off_seq_m, off_acc, off_seq_cnt, off_seq_bad, off_jstar, bytes;
+    int64_t R;    // rows B*(K+1)
+    int32_t S1;   // row items per row
+    int32_t NSL;  // survivor slices per sequence
+    int32_t fix;  // fractional bits of the fixed-point masses
+    size_t off_part, off_row_cnt, off_row_m, off_row_s, off_acc, off_seq_cnt, off_seq_bad, off_jstar, off_seq_m,
+        off_seq_s, off_surv_cnt, off_seqE, off_seqF, off_slice, off_rec_a, off_rec_q, off_ctr, bytes;
 };
 
 bool make_plan(int64_t B, int32_t K, int32_t V, Plan &p)
@@ -45,34 +47,40 @@ bool make_plan(int64_t B, int32_t K, int32_t V, Plan &p)
     p.R = B * (static_cast<int64_t>(K) + 1);
     if (p.R > 0 && V > INT64_MAX / p.R)
         return false;
-    // ~32K elements per chunk; more chunks when there are few rows, so that
-    // a small batch still spreads over the GPU; at least 4K elements each
-    int64_t s1 = ceil_div(V, 32768);
+    // ~SV_ROW_ITEM ids per row item; more items when there are few rows, so
+    // that a small batch still spreads over the GPU's warps; at least 1024
+    // ids each
+    int64_t s1 = ceil_div(V, sv::kRowItemElems);
     if (p.R > 0) {
-        const int64_t spread = ceil_div(1216, p.R);
-        const int64_t finest = ceil_div(V, 4096);
+        const int64_t spread = ceil_div(4096, p.R);
+        const int64_t finest = ceil_div(V, 1024);
         const int64_t want = spread < finest ? spread : finest;
         if (want > s1)
             s1 = want;
     }
-    if (s1 > 64)
-        s1 = 64;
-    if (s1 < 1)
-        s1 = 1;
-    p.S1 = static_cast<int32_t>(s1);
-    int64_t cl = ceil_div(V, 16384);
-    p.CL = static_cast<int32_t>(cl < 1 ? 1 : (cl > sv::kMaxCluster ? sv::kMaxCluster : cl));
+    p.S1 = static_cast<int32_t>(s1 < 1 ? 1 : (s1 > 256 ? 256 : s1));
+    p.NSL = static_cast<int32_t>(ceil_div(V, static_cast<int64_t>(sv::kSliceGroups) * sv::kGroup));
     const int fb = 62 - ceil_log2_u64(static_cast<uint64_t>(V) + 1);
     p.fix = fb < 40 ? fb : 40;
+    const size_t Bz = static_cast<size_t>(B), R = static_cast<size_t>(p.R);
     size_t off = 0;
-    p.off_part = off;    off = align_up(off + static_cast<size_t>(p.R) * p.S1 * sizeof(float2));
-    p.off_row_cnt = off; off = align_up(off + static_cast<size_t>(p.R) * sizeof(uint32_t));
-    p.off_row_m = off;   off = align_up(off + static_cast<size_t>(p.R) * sizeof(float));
-    p.off_seq_m = off;   off = align_up(off + static_cast<size_t>(B) * sizeof(float));
-    p.off_acc = off;     off = align_up(off + static_cast<size_t>(B) * K * sizeof(uint8_t));
-    p.off_seq_cnt = off; off = align_up(off + static_cast<size_t>(B) * sizeof(uint32_t));
-    p.off_seq_bad = off; off = align_up(off + static_cast<size_t>(B) * sizeof(int32_t));
-    p.off_jstar = off;   off = align_up(off + static_cast<size_t>(B) * sizeof(int32_t));
+    p.off_part = off;     off = align_up(off + R * p.S1 * sizeof(float2));
+    p.off_row_cnt = off;  off = align_up(off + R * sizeof(uint32_t));
+    p.off_row_m = off;    off = align_up(off + R * sizeof(float));
+    p.off_row_s = off;    off = align_up(off + R * sizeof(float));
+    p.off_acc = off;      off = align_up(off + Bz * K * sizeof(uint8_t));
+    p.off_seq_cnt = off;  off = align_up(off + Bz * sizeof(uint32_t));
+    p.off_seq_bad = off;  off = align_up(off + Bz * sizeof(int32_t));
+    p.off_jstar = off;    off = align_up(off + Bz * sizeof(int32_t));
+    p.off_seq_m = off;    off = align_up(off + Bz * sizeof(float));
+    p.off_seq_s = off;    off = align_up(off + Bz * sizeof(float));
+    p.off_surv_cnt = off; off = align_up(off + Bz * sizeof(uint32_t));
+    p.off_seqE = off;     off = align_up(off + Bz * sizeof(long long));
+    p.off_seqF = off;     off = align_up(off + Bz * sizeof(long long));
+    p.off_slice = off;    off = align_up(off + Bz * p.NSL * 2 * sizeof(long long));
+    p.off_rec_a = off;    off = align_up(off + Bz * p.NSL * sv::kSliceTiles * sizeof(long long));
+    p.off_rec_q = off;    off = align_up(off + Bz * p.NSL * sv::kSliceTiles * sizeof(float));
+    p.off_ctr = off;      off = align_up(off + 2 * sizeof(unsigned long long));
     p.bytes = off;
     return true;
 }
@@ -81,31 +89,89 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 enum Stage { kRows = 1, kSurvivors = 2, kBoth = 3 };
 
+constexpr int kMaxDevices = 64;
+constexpr int kDrawSmem = sv::kWarps * sv::kWarpSmem; // the draw warps' async-copy rings
+
+// Per device and kernel instantiation: how many CTAs of each kernel fit on
+// the device at once (the grids of the persistent kernels).
+struct Resident {
+    int rows, draw;
+};
+
 template <typename LT, bool DENSE>
-cudaError_t launch(const sv::Params &P, const Plan &plan, int stages, cudaStream_t stream)
+cudaError_t resident_ctas(Resident &out)
 {
+    static std::mutex mu;
+    static Resident cache[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev].rows == 0) {
+        int sms = 0, rows = 0, draw = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return e;
+        e = cudaFuncSetAttribute(sv::survivor_kernel<LT, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kDrawSmem);
+        if (e != cudaSuccess)
+            return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&rows, sv::rows_kernel<LT, DENSE>, sv::kRowCtaThreads, 0);
+        if (e != cudaSuccess)
+            return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&draw, sv::survivor_kernel<LT, DENSE>, sv::kThreads,
+                                                          kDrawSmem);
+        if (e != cudaSuccess)
+            return e;
+        sms = sms > 0 ? sms : 1;
+        cache[dev].rows = (rows > 0 ? rows : 1) * sms;
+        cache[dev].draw = (draw > 0 ? draw : 1) * sms;
+    }
+    out = cache[dev];
+    return cudaSuccess;
+}
+
+int64_t clamp_grid(int64_t want, int64_t cap) { return want < 1 ? 1 : (want > cap ? cap : want); }
+
+template <typename LT, bool DENSE>
+cudaError_t launch(sv::Params P, const Plan &plan, int stages, cudaStream_t stream)
+{
+    if (stages == 0)
+        return cudaSuccess;
+    Resident res;
+    cudaError_t e = resident_ctas<LT, DENSE>(res);
+    if (e != cudaSuccess)
+        return e;
+    P.RI = (static_cast<int64_t>(P.K) + 1) * plan.S1;
     if (stages & kRows) {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(plan.R * plan.S1));
-        cfg.blockDim = dim3(sv::kRowThreads);
+        cfg.gridDim = dim3(static_cast<unsigned>(clamp_grid(P.B * P.RI, res.rows)));
+        cfg.blockDim = dim3(sv::kRowCtaThreads);
         cfg.stream = stream;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, sv::rows_kernel<LT, DENSE>, P);
+        e = cudaLaunchKernelEx(&cfg, sv::rows_kernel<LT, DENSE>, P);
         if (e != cudaSuccess)
             return e;
     }
     if (stages & kSurvivors) {
+        const int64_t grid = clamp_grid(ceil_div(P.B * plan.NSL, sv::kWarps), res.draw);
+        P.n_warps = static_cast<uint64_t>(grid) * sv::kWarps;
+        // programmatic dependent launch: the draw's CTAs may be scheduled
+        // while the row pass drains; they wait in griddepcontrol.wait for
+        // its completion before reading anything it wrote
         cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(plan.CL);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(P.B * plan.CL));
-        cfg.blockDim = dim3(sv::kSurvThreads);
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(sv::kThreads);
+        cfg.dynamicSmemBytes = kDrawSmem;
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, sv::survivor_kernel<LT, DENSE>, P);
+        e = cudaLaunchKernelEx(&cfg, sv::survivor_kernel<LT, DENSE>, P);
         if (e != cudaSuccess)
             return e;
     }
@@ -144,8 +210,6 @@ sv_status_t run(int stages, const void *logits, sv_dtype_t dtype, const float *q
         return SV_EINVAL;
     if (B == 0)
         return SV_OK;
-    if (plan.R * plan.S1 > INT32_MAX || B * plan.CL > INT32_MAX)
-        return SV_EUNSUPPORTED;
 
     char *ws = static_cast<char *>(workspace);
     sv::Params P;
@@ -166,14 +230,25 @@ sv_status_t run(int stages, const void *logits, sv_dtype_t dtype, const float *q
     P.row_part = reinterpret_cast<float2 *>(ws + plan.off_part);
     P.row_cnt = reinterpret_cast<uint32_t *>(ws + plan.off_row_cnt);
     P.row_m = reinterpret_cast<float *>(ws + plan.off_row_m);
-    P.seq_m = reinterpret_cast<float *>(ws + plan.off_seq_m);
+    P.row_s = reinterpret_cast<float *>(ws + plan.off_row_s);
     P.acc = reinterpret_cast<uint8_t *>(ws + plan.off_acc);
     P.seq_cnt = reinterpret_cast<uint32_t *>(ws + plan.off_seq_cnt);
     P.seq_bad = reinterpret_cast<int32_t *>(ws + plan.off_seq_bad);
     P.seq_jstar = reinterpret_cast<int32_t *>(ws + plan.off_jstar);
+    P.seq_m = reinterpret_cast<float *>(ws + plan.off_seq_m);
+    P.seq_s = reinterpret_cast<float *>(ws + plan.off_seq_s);
+    P.surv_cnt = reinterpret_cast<uint32_t *>(ws + plan.off_surv_cnt);
+    P.seq_E = reinterpret_cast<long long *>(ws + plan.off_seqE);
+    P.seq_F = reinterpret_cast<long long *>(ws + plan.off_seqF);
+    P.slice_tot = reinterpret_cast<long long *>(ws + plan.off_slice);
+    P.rec_a = reinterpret_cast<long long *>(ws + plan.off_rec_a);
+    P.rec_q = reinterpret_cast<float *>(ws + plan.off_rec_q);
+    P.ctr = reinterpret_cast<unsigned long long *>(ws + plan.off_ctr);
     P.S1 = plan.S1;
-    P.CL = plan.CL;
+    P.NSL = plan.NSL;
     P.fix_bits = plan.fix;
+    P.RI = 0;
+    P.n_warps = 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;

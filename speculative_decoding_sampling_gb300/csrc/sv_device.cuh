@@ -1,8 +1,6 @@
-// sv_device.cuh -- device helpers shared by the two kernels of the
-// verification step: launch parameters, element decoding, the exact
-// fixed-point accumulation of probability masses, the exact product
-// floor(u * Z), warp reductions, and the cluster / distributed-shared-memory
-// primitives (inline PTX, sm_90+ cluster model, compiled for sm_103a).
+// sv_device.cuh -- device helpers of the verification kernel: launch
+// parameters, element decoding, the base-2 online softmax normaliser, exact
+// fixed-point masses, warp reductions and the acquire/release flag accesses.
 #pragma once
 
 #include <cstdint>
@@ -10,15 +8,36 @@
 
 namespace sv {
 
-constexpr int kRowThreads = 256;  // threads of a row-pass CTA
-constexpr int kSurvThreads = 256; // threads of a survivor CTA
-constexpr int kGroup = 8;         // contiguous elements per survivor thread
-constexpr int kMaxTiles = 1024;   // tiles of one survivor CTA (V <= 2^24)
-constexpr int kMaxCluster = 8;    // portable cluster size
+// Tuning knobs (defaults measured on GB300; each may be set with -D).
+#ifndef SV_ROW_ITEM
+#define SV_ROW_ITEM 32768 // ids of one row item (one CTA of the row pass)
+#endif
+#ifndef SV_ROW_MIN_CTAS
+#define SV_ROW_MIN_CTAS 4 // row pass: resident CTAs per SM the register budget is cut for
+#endif
+#ifndef SV_STAGES
+#define SV_STAGES 3       // final draw: per-warp async-copy ring depth
+#endif
+#ifndef SV_STAGE_BYTES
+#define SV_STAGE_BYTES 2048
+#endif
+#ifndef SV_MIN_CTAS
+#define SV_MIN_CTAS 4     // final draw: resident CTAs per SM the register budget is cut for
+#endif
 
-// Device status bits (the same values the public header documents).
-constexpr int32_t kBadU = 1, kBadToken = 2, kBadQ = 4, kBadRow = 8,
-                  kDegenerate = 16;
+constexpr int kThreads = 256;          // threads of a CTA
+constexpr int kWarps = kThreads / 32;
+constexpr int kRowItemElems = SV_ROW_ITEM;
+constexpr int kGroup = 8;              // consecutive ids a lane owns in the final draw
+constexpr int kSliceGroups = 256;      // groups of one survivor slice item (2048 ids)
+constexpr int kSliceTiles = kSliceGroups / 32; // warp tiles of a slice
+constexpr int kStages = SV_STAGES;     // per-warp async-copy ring depth
+constexpr int kStageBytes = SV_STAGE_BYTES; // one stage: 16-byte pieces, a multiple of 512 per warp
+constexpr int kWarpSmem = kStages * kStageBytes;
+static_assert(kStages >= 2 && kStageBytes % 512 == 0 && kStageBytes >= 2048, "ring shape");
+
+// Device status bits (the values the public header documents).
+constexpr int32_t kBadU = 1, kBadToken = 2, kBadQ = 4, kBadRow = 8, kDegenerate = 16;
 
 struct Params {
     const void *logits;
@@ -34,20 +53,30 @@ struct Params {
     float *accept_prob;
     float *residual_mass;
     int32_t *status;
-    // workspace views
-    float2 *row_part;  // [R * S1]  (max of z, sum of exp2 relative to it)
-    uint32_t *row_cnt; // [R]       arrival counters, left at zero
-    float *row_m;      // [R]       max of z over the row
-    float *seq_m;      // [B]       max of z over the row of the final draw
-    uint8_t *acc;      // [B * K]   1 = accepted
-    uint32_t *seq_cnt; // [B]       arrival counters, left at zero
-    int32_t *seq_bad;  // [B]       status bits of the sequence, left at zero
-    int32_t *seq_jstar;// [B]       row the final token is drawn from, -1 = bad
-    // Every workspace word is returned to zero by its last reader, so a call
-    // leaves the whole workspace zero-filled.
-    int32_t S1;        // chunks per row in the row pass
-    int32_t CL;        // cluster size of the survivor pass
-    int32_t fix_bits;  // fractional bits of the fixed-point masses
+    // workspace views; every word is returned to zero by its last reader, so
+    // a completed call leaves the whole workspace zero-filled
+    float2 *row_part;     // [R * S1]  (max of z, normaliser relative to it) per row item
+    uint32_t *row_cnt;    // [R]       row items done
+    float *row_m;         // [R]       max of z over the row
+    float *row_s;         // [R]       fp32 normaliser of the row (relative to fl(m*c))
+    uint8_t *acc;         // [B * K]   1 = accepted
+    uint32_t *seq_cnt;    // [B]       rows done
+    int32_t *seq_bad;     // [B]       status bits of the sequence
+    int32_t *seq_jstar;   // [B]       row the final token is drawn from, -1 = bad
+    float *seq_m;         // [B]       max of z of that row
+    float *seq_s;         // [B]       fp32 normaliser of that row
+    uint32_t *surv_cnt;   // [B]       survivor slices done
+    long long *seq_E;     // [B]       exact sum of pt over the surviving row (dense), 2^-fix_bits units
+    long long *seq_F;     // [B]       sum of pt (one-hot normaliser), 2^-fix_bits units
+    long long *slice_tot; // [B * NSL * 2] per slice: mass A, bits(double Qp)
+    long long *rec_a;     // [B * NSL * 8] per warp tile: mass A
+    float *rec_q;         // [B * NSL * 8] per warp tile: Qp
+    unsigned long long *ctr; // [2] next slice ticket, draw warps done
+    int32_t S1;           // row items per row
+    int32_t NSL;          // survivor slices per sequence
+    int32_t fix_bits;     // fractional bits of the fixed-point masses
+    int64_t RI;           // row items per sequence, (K+1) * S1
+    uint64_t n_warps;     // warps of the draw kernel's grid
 };
 
 // ------------------------------------------------------------ element loads
@@ -75,11 +104,66 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *p)
     return r;
 }
 
+__device__ __forceinline__ uint8_t ld_cg_u8(const uint8_t *p)
+{
+    uint16_t v;
+    asm volatile("ld.global.cg.u8 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
+    return static_cast<uint8_t>(v);
+}
+
+
+
+// ------------------------------------------------------- async copies
+//
+// Each warp owns a ring of kStages shared-memory stages.  A lane copies only
+// the 16-byte pieces it will read itself, so completion is tracked with the
+// lane's own copy groups (cp.async.wait_group) and no lane ever waits for
+// another.
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// wait until at most N of this lane's copy groups are still in flight
+template <int N> __device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds_v4(const void *p)
+{
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(smem_addr(p)));
+    return r;
+}
+
 // ------------------------------------------------------- softmax normaliser
 
+// 2^x on the special-function unit (flush-to-zero: results below 2^-126
+// are far below every mass this library resolves).
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // y-space offset of a running maximum M: fl(M * c), or 0 while nothing but
-// -inf has been seen (then every finite-free term is exp2(-inf) = 0 and a
-// NaN still propagates).
+// -inf has been seen (then every term is exp2(-inf) = 0 and a NaN still
+// propagates).
 __device__ __forceinline__ float mc_of(float M, float c)
 {
     return M == -INFINITY ? 0.0f : __fmul_rn(M, c);
@@ -88,23 +172,23 @@ __device__ __forceinline__ float mc_of(float M, float c)
 // One softmax term relative to the offset mc: exp2(z*c - mc).
 __device__ __forceinline__ float term(float z, float c, float mc)
 {
-    return exp2f(__fmaf_rn(z, c, -mc));
+    return ex2(__fmaf_rn(z, c, -mc));
 }
 
 // Merge two partial (max, sum) pairs of the online softmax normaliser.
 __device__ __forceinline__ void merge_ms(float &M, float &S, float M2, float S2, float c)
 {
-    float Mn = fmaxf(M, M2);
-    float mn = mc_of(Mn, c);
-    float f1 = (M == -INFINITY) ? 0.0f : exp2f(mc_of(M, c) - mn);
-    float f2 = (M2 == -INFINITY) ? 0.0f : exp2f(mc_of(M2, c) - mn);
+    const float Mn = fmaxf(M, M2);
+    const float mn = mc_of(Mn, c);
+    const float f1 = (M == -INFINITY) ? 0.0f : ex2(mc_of(M, c) - mn);
+    const float f2 = (M2 == -INFINITY) ? 0.0f : ex2(mc_of(M2, c) - mn);
     S = __fadd_rn(__fmul_rn(S, f1), __fmul_rn(S2, f2));
     M = Mn;
 }
 
 // --------------------------------------------------- exact fixed-point mass
 
-// A probability mass w in [0, 2] as an integer multiple of 2^-fix_bits.
+// A probability mass w (|w| < 2^22) as an integer multiple of 2^-fix_bits.
 // w * 2^fix_bits is exact in fp32 (a power-of-two scale); the conversion
 // rounds to nearest.  Sums of these integers are exact and independent of
 // the order of summation.
@@ -113,22 +197,77 @@ __device__ __forceinline__ long long to_fixed(float w, float scale)
     return __float2ll_rn(__fmul_rn(w, scale));
 }
 
-// floor(u * Z) exactly, for u in [0, 1) (fp32) and 0 <= Z < 2^63.
-__device__ __forceinline__ unsigned long long floor_mul(float u, unsigned long long Z)
+// --------------------------------------------------- packed fp32 pairs
+//
+// Two fp32 lanes in one 64-bit register pair; each operation rounds both
+// halves exactly as the scalar instruction would.
+
+__device__ __forceinline__ unsigned long long pack2(float a, float b)
 {
-    uint32_t bits = __float_as_uint(u);
-    uint32_t E = (bits >> 23) & 0xFFu;
-    unsigned long long mant = (bits & 0x7FFFFFu) | (E ? 0x800000u : 0u);
-    if (mant == 0ull || Z == 0ull)
-        return 0ull;
-    int shift = 150 - (E ? static_cast<int>(E) : 1); // u = mant * 2^-shift, shift >= 24
-    unsigned long long lo = mant * Z;
-    unsigned long long hi = __umul64hi(mant, Z);
-    if (shift >= 128)
-        return 0ull;
-    if (shift >= 64)
-        return hi >> (shift - 64);
-    return (hi << (64 - shift)) | (lo >> shift);
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ void unpack2(unsigned long long v, float &a, float &b)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c)
+{
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b)
+{
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b)
+{
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// a / b and a % b for 0 <= a, 0 < b < 2^31, in 32-bit arithmetic when a fits
+__device__ __forceinline__ int64_t divi(int64_t a, int64_t b)
+{
+    return a < 0x80000000ll ? static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b)) : a / b;
+}
+
+// ------------------------------------------------- programmatic launch
+
+// Let the next kernel in the stream start launching its CTAs.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the preceding kernel in the stream has completed and its
+// memory is visible (a hardware dependency, not a polling loop).
+__device__ __forceinline__ void pdl_wait_primary()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ------------------------------------------------------- named barriers
+
+// Arrive at named barrier `id` (expecting `count` threads) without waiting.
+__device__ __forceinline__ void bar_arrive(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Arrive at named barrier `id` and wait until `count` threads have arrived.
+__device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ------------------------------------------------------------ warp helpers
@@ -141,42 +280,31 @@ __device__ __forceinline__ long long warp_sum_ll(long long v)
     return v;
 }
 
-// inclusive scan over the warp
-__device__ __forceinline__ long long warp_incl_scan_ll(long long v, int lane)
+// butterfly: every lane computes the same additions, so all lanes agree
+__device__ __forceinline__ float warp_sum_f(float v)
 {
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        long long n = __shfl_up_sync(0xFFFFFFFFu, v, o);
-        if (lane >= o)
-            v += n;
-    }
+    for (int o = 16; o > 0; o >>= 1)
+        v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
     return v;
 }
 
-// ------------------------------------------------------- cluster primitives
-
-__device__ __forceinline__ uint32_t cluster_ctarank()
+__device__ __forceinline__ double warp_sum_d(double v)
 {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
 }
 
-__device__ __forceinline__ void cluster_sync_all()
+__device__ __forceinline__ double warp_incl_scan_d(double v, int lane)
 {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Read a 64-bit value from the shared memory of CTA `rank` of the cluster,
-// at the address that `local` has in this CTA.
-__device__ __forceinline__ long long ld_cluster_ll(const long long *local, uint32_t rank)
-{
-    uint32_t saddr = static_cast<uint32_t>(__cvta_generic_to_shared(local));
-    uint32_t raddr;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(saddr), "r"(rank));
-    long long v;
-    asm volatile("ld.shared::cluster.s64 %0, [%1];" : "=l"(v) : "r"(raddr) : "memory");
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double n = __shfl_up_sync(0xFFFFFFFFu, v, o);
+        if (lane >= o)
+            v += n;
+    }
     return v;
 }
 
