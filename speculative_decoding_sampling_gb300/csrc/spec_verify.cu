@@ -31,7 +31,7 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // (B, K, V) only.
 struct Plan {
     int64_t R;    // rows B*(K+1)
-    int32_t S1;   // row items per row
+    int32_t PM;   // row_part slots per row
     int32_t NSL;  // survivor slices per sequence
     int32_t fix;  // fractional bits of the fixed-point masses
     size_t off_part, off_row_cnt, off_row_m, off_row_s, off_acc, off_seq_cnt, off_seq_bad, off_jstar, off_seq_m,
@@ -47,24 +47,15 @@ bool make_plan(int64_t B, int32_t K, int32_t V, Plan &p)
     p.R = B * (static_cast<int64_t>(K) + 1);
     if (p.R > 0 && V > INT64_MAX / p.R)
         return false;
-    // ~SV_ROW_ITEM ids per row item; more items when there are few rows, so
-    // that a small batch still spreads over the GPU's warps; at least 1024
-    // ids each
-    int64_t s1 = ceil_div(V, sv::kRowItemElems);
-    if (p.R > 0) {
-        const int64_t spread = ceil_div(4096, p.R);
-        const int64_t finest = ceil_div(V, 1024);
-        const int64_t want = spread < finest ? spread : finest;
-        if (want > s1)
-            s1 = want;
-    }
-    p.S1 = static_cast<int32_t>(s1 < 1 ? 1 : (s1 > 256 ? 256 : s1));
+    // row_part slots per row: enough for any cut of the flat row array into
+    // at most kRowMaxCtas spans (the launch widens spans to keep to it)
+    p.PM = static_cast<int32_t>(p.R > 0 ? ceil_div(sv::kRowMaxCtas, p.R) + 3 : 4);
     p.NSL = static_cast<int32_t>(ceil_div(V, static_cast<int64_t>(sv::kSliceGroups) * sv::kGroup));
     const int fb = 62 - ceil_log2_u64(static_cast<uint64_t>(V) + 1);
     p.fix = fb < 40 ? fb : 40;
     const size_t Bz = static_cast<size_t>(B), R = static_cast<size_t>(p.R);
     size_t off = 0;
-    p.off_part = off;     off = align_up(off + R * p.S1 * sizeof(float2));
+    p.off_part = off;     off = align_up(off + R * p.PM * sizeof(float2));
     p.off_row_cnt = off;  off = align_up(off + R * sizeof(uint32_t));
     p.off_row_m = off;    off = align_up(off + R * sizeof(float));
     p.off_row_s = off;    off = align_up(off + R * sizeof(float));
@@ -145,10 +136,28 @@ cudaError_t launch(sv::Params P, const Plan &plan, int stages, cudaStream_t stre
     cudaError_t e = resident_ctas<LT, DENSE>(res);
     if (e != cudaSuccess)
         return e;
-    P.RI = (static_cast<int64_t>(P.K) + 1) * plan.S1;
+    // the flat view of the logits and its cut into one span per CTA
+    constexpr int64_t VW = 16 / sizeof(LT);
+    P.total = plan.R * P.V;
+    P.h = static_cast<int64_t>((16 - reinterpret_cast<uintptr_t>(P.logits) % 16) % 16) / static_cast<int64_t>(sizeof(LT));
+    if (P.h > P.total)
+        P.h = P.total;
+    P.nvec = (P.total - P.h) / VW;
+    P.NV = P.nvec + 2;
+    {
+        int64_t want = clamp_grid(ceil_div(P.NV, sv::kRowMinSpan), res.rows < sv::kRowMaxCtas ? res.rows : sv::kRowMaxCtas);
+        if (want < ceil_div(P.NV, sv::kRowMaxSpan))
+            want = ceil_div(P.NV, sv::kRowMaxSpan); // offsets inside a span stay in int
+        int64_t span = ceil_div(P.NV, want);
+        // a row touches at most `touch` vectors; spans of at least
+        // touch / (PM - 2) vectors put it in at most PM - 1 CTAs
+        const int64_t touch = ceil_div(P.V, VW) + 2;
+        const int64_t span_min = ceil_div(touch, plan.PM - 2);
+        P.span = span > span_min ? span : span_min;
+    }
     if (stages & kRows) {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(clamp_grid(P.B * P.RI, res.rows)));
+        cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(P.NV, P.span)));
         cfg.blockDim = dim3(sv::kRowCtaThreads);
         cfg.stream = stream;
         e = cudaLaunchKernelEx(&cfg, sv::rows_kernel<LT, DENSE>, P);
@@ -244,10 +253,10 @@ sv_status_t run(int stages, const void *logits, sv_dtype_t dtype, const float *q
     P.rec_a = reinterpret_cast<long long *>(ws + plan.off_rec_a);
     P.rec_q = reinterpret_cast<float *>(ws + plan.off_rec_q);
     P.ctr = reinterpret_cast<unsigned long long *>(ws + plan.off_ctr);
-    P.S1 = plan.S1;
+    P.PM = plan.PM;
     P.NSL = plan.NSL;
     P.fix_bits = plan.fix;
-    P.RI = 0;
+    P.total = P.h = P.nvec = P.NV = P.span = 0;
     P.n_warps = 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -9,8 +9,8 @@
 namespace sv {
 
 // Tuning knobs (defaults measured on GB300; each may be set with -D).
-#ifndef SV_ROW_ITEM
-#define SV_ROW_ITEM 32768 // ids of one row item (one CTA of the row pass)
+#ifndef SV_ROW_MIN_SPAN
+#define SV_ROW_MIN_SPAN 1024 // row pass: fewest 16-byte vectors a CTA streams
 #endif
 #ifndef SV_ROW_MIN_CTAS
 #define SV_ROW_MIN_CTAS 4 // row pass: resident CTAs per SM the register budget is cut for
@@ -27,7 +27,8 @@ namespace sv {
 
 constexpr int kThreads = 256;          // threads of a CTA
 constexpr int kWarps = kThreads / 32;
-constexpr int kRowItemElems = SV_ROW_ITEM;
+constexpr int kRowMinSpan = SV_ROW_MIN_SPAN;
+constexpr int kRowMaxCtas = 4096;      // row pass: most CTAs a call's span is cut for
 constexpr int kGroup = 8;              // consecutive ids a lane owns in the final draw
 constexpr int kSliceGroups = 256;      // groups of one survivor slice item (2048 ids)
 constexpr int kSliceTiles = kSliceGroups / 32; // warp tiles of a slice
@@ -55,8 +56,8 @@ struct Params {
     int32_t *status;
     // workspace views; every word is returned to zero by its last reader, so
     // a completed call leaves the whole workspace zero-filled
-    float2 *row_part;     // [R * S1]  (max of z, normaliser relative to it) per row item
-    uint32_t *row_cnt;    // [R]       row items done
+    float2 *row_part;     // [R * PM]  (max of z, normaliser relative to it) per CTA a row falls in
+    uint32_t *row_cnt;    // [R]       row parts done
     float *row_m;         // [R]       max of z over the row
     float *row_s;         // [R]       fp32 normaliser of the row (relative to fl(m*c))
     uint8_t *acc;         // [B * K]   1 = accepted
@@ -72,10 +73,14 @@ struct Params {
     long long *rec_a;     // [B * NSL * 8] per warp tile: mass A
     float *rec_q;         // [B * NSL * 8] per warp tile: Qp
     unsigned long long *ctr; // [2] next slice ticket, draw warps done
-    int32_t S1;           // row items per row
+    int64_t total;        // R * V elements of the logits
+    int64_t h;            // elements before the first 16-byte boundary (< 16 / element size)
+    int64_t nvec;         // whole 16-byte vectors from there on
+    int64_t NV;           // nvec + 2: the flat view's vectors, the two ragged ends included
+    int64_t span;         // vectors per row-pass CTA
+    int32_t PM;           // row_part slots per row
     int32_t NSL;          // survivor slices per sequence
     int32_t fix_bits;     // fractional bits of the fixed-point masses
-    int64_t RI;           // row items per sequence, (K+1) * S1
     uint64_t n_warps;     // warps of the draw kernel's grid
 };
 

@@ -1,12 +1,11 @@
 // sv_rows.cuh -- the row pass of the verification step.
 //
-// Every one of the B*(K+1) target rows is streamed once from HBM.  A row is
-// cut into S1 row items of about SV_ROW_ITEM ids; persistent CTAs take them
-// round-robin and stream them with 16-byte loads, the next step (possibly of
-// the next item) in flight while the current one is folded.  Each thread
+// Every one of the B*(K+1) target rows is streamed once from HBM.  The rows
+// are one flat array; each CTA streams one contiguous span of it with 16-byte
+// loads, the next step in flight while the current one is folded.  Each thread
 // keeps an online (max, normaliser) pair of softmax(z / T) in the base-2 form
 // sum_i exp2(z_i * c - fl(M * c)), c = log2(e) / T (one exp2 per element).
-// The CTA that finishes a row last merges the item partials and runs the
+// The CTA that finishes a row last merges the row's partials and runs the
 // accept test of the draft that row
 // verifies: a = min(1, p(x) / q(x)), accept iff u < a
 // ("推测解码：草稿、验证与实际加速", section 接受与拒绝怎样保住分布, equation for
@@ -17,6 +16,8 @@
 // detected with arrival counters; each is returned to zero by the CTA that
 // saw it complete.
 #pragma once
+
+#include <climits>
 
 #include "sv_device.cuh"
 
@@ -61,19 +62,18 @@ __device__ __forceinline__ float vec_max(const uint4 (&w)[U])
     }
 }
 
-// Fold U vectors into the running (M, S) of one lane; S holds four packed
-// pairs of partial sums (eight accumulators).
+// Fold U vectors into the running (M, S) of one lane; S holds two packed
+// pairs of partial sums (four accumulators).
 template <typename LT, int U>
-__device__ __forceinline__ void fold(const uint4 (&w)[U], float &M, unsigned long long (&S)[4], float c)
+__device__ __forceinline__ void fold(const uint4 (&w)[U], float &M, unsigned long long (&S)[2], float c)
 {
     const float gm = vec_max<LT, U>(w);
     if (gm > M) {
         // rescale what was summed against the old maximum
         const float f = (M == -INFINITY) ? 0.0f : ex2(mc_of(M, c) - mc_of(gm, c));
         const unsigned long long f2 = pack2(f, f);
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-            S[a] = mul2(S[a], f2);
+        S[0] = mul2(S[0], f2);
+        S[1] = mul2(S[1], f2);
         M = gm;
     }
     const float mc = mc_of(M, c);
@@ -86,14 +86,14 @@ __device__ __forceinline__ void fold(const uint4 (&w)[U], float &M, unsigned lon
             for (int h = 0; h < 4; ++h) {
                 float y0, y1;
                 unpack2(fma2(pack2(bf16_lo(v[h]), bf16_hi(v[h])), c2, nmc2), y0, y1);
-                S[h] = add2(S[h], pack2(ex2(y0), ex2(y1)));
+                S[h & 1] = add2(S[h & 1], pack2(ex2(y0), ex2(y1)));
             }
         } else {
 #pragma unroll
             for (int h = 0; h < 4; h += 2) {
                 float y0, y1;
                 unpack2(fma2(pack2(__uint_as_float(v[h]), __uint_as_float(v[h + 1])), c2, nmc2), y0, y1);
-                S[h + (k & 1)] = add2(S[h + (k & 1)], pack2(ex2(y0), ex2(y1)));
+                S[(h >> 1)] = add2(S[(h >> 1)], pack2(ex2(y0), ex2(y1)));
             }
         }
     }
@@ -189,18 +189,19 @@ __device__ __forceinline__ RowSide fetch_side(const Params &P, int64_t r)
     return s;
 }
 
-// The last warp of row r merges the item partials and tests the draft.
+// The last warp of row r merges the row's n_parts partials and tests the
+// draft.
 // `side` is valid in lane 0.
 template <typename LT, bool DENSE>
-__device__ __noinline__ void finish_row(const Params &P, int64_t r, int lane, const RowSide &side)
+__device__ __noinline__ void finish_row(const Params &P, int64_t r, int n_parts, int lane, const RowSide &side)
 {
     __threadfence();
     const float c = P.c;
     const int32_t K = P.K, V = P.V;
     float M = -INFINITY, S = 0.0f;
-    for (int32_t i = lane; i < P.S1; i += 32) {
-        const float2 pr = __ldcg(&P.row_part[r * P.S1 + i]);
-        P.row_part[r * P.S1 + i] = make_float2(0.0f, 0.0f);
+    for (int32_t i = lane; i < n_parts; i += 32) {
+        const float2 pr = __ldcg(&P.row_part[r * P.PM + i]);
+        P.row_part[r * P.PM + i] = make_float2(0.0f, 0.0f);
         merge_ms(M, S, pr.x, pr.y, c);
     }
     warp_merge_ms(M, S, c);
@@ -249,44 +250,78 @@ __device__ __noinline__ void finish_row(const Params &P, int64_t r, int lane, co
         finish_sequence<DENSE>(P, b, lane);
 }
 
-// Row item `it`: row r = it / S1, item ch = it % S1.  A row has a scalar head
-// (until 16-byte aligned), whole 16-byte vectors shared out over the S1
-// items, and a scalar tail.
-struct ItemSpan {
-    const uint4 *p;  // the item's first whole vector
-    int32_t nv;      // its whole vectors
-    int32_t nsteps;  // CTA steps covering them (at least one)
-};
-
+// The flat view of the logits.  The B*(K+1) rows of V ids are one array of
+// R*V elements.  From the first 16-byte boundary on it is cut into whole
+// 16-byte vectors 1..nvec; "vector" 0 stands for the h elements before that
+// boundary and vector nvec+1 for the ragged end.  CTA g owns the vectors
+// [g*span, (g+1)*span): one contiguous piece of HBM.  A vector is streamed
+// (read with one 16-byte load by a streaming warp) when it is whole and all
+// its ids lie in one row; the others -- the two ragged ends and, when
+// V * element size is not a multiple of 16 or the array is not 16-byte
+// aligned, the vectors that straddle a row boundary -- are read id by id by
+// the epilogue warp of the CTA that owns them, once for each row they touch.
+// Each row's partial (max, normaliser) pairs come from the CTAs its ids fall
+// in; CTA g writes its pair of row r into slot g - first_cta(r) of the row.
 template <typename LT>
-__device__ __forceinline__ const LT *row_ptr(const Params &P, int64_t r)
-{
-    return static_cast<const LT *>(P.logits) + r * static_cast<int64_t>(P.V);
-}
-
-template <typename LT>
-__device__ __forceinline__ int32_t row_head(const LT *row, int32_t V)
-{
-    const int32_t h = static_cast<int32_t>(((16u - (reinterpret_cast<uintptr_t>(row) & 15u)) & 15u) / sizeof(LT));
-    return h < V ? h : V;
-}
-
-template <typename LT, int STEP>
-__device__ __forceinline__ ItemSpan item_span(const Params &P, int64_t it)
+__device__ __forceinline__ int64_t vec_of_elem(const Params &P, int64_t e)
 {
     constexpr int VW = 16 / sizeof(LT);
-    const int64_t r = divi(it, P.S1);
-    const int32_t ch = static_cast<int32_t>(it - r * P.S1);
-    const LT *row = row_ptr<LT>(P, r);
-    const int32_t head = row_head(row, P.V);
-    const int32_t nvec = (P.V - head) / VW;
-    const int32_t v0 = static_cast<int32_t>(static_cast<int64_t>(nvec) * ch / P.S1);
-    const int32_t v1 = static_cast<int32_t>(static_cast<int64_t>(nvec) * (ch + 1) / P.S1);
-    ItemSpan s;
-    s.p = reinterpret_cast<const uint4 *>(row + head) + v0;
-    s.nv = v1 - v0;
-    s.nsteps = max(1, (s.nv + STEP - 1) / STEP);
-    return s;
+    return (e - P.h + VW) / VW; // e - h + VW > 0 since h < VW
+}
+
+template <typename LT>
+__device__ __forceinline__ bool streamed(const Params &P, int64_t vv)
+{
+    constexpr int VW = 16 / sizeof(LT);
+    const int64_t e0 = P.h + (vv - 1) * VW;
+    return vv >= 1 && vv <= P.nvec && e0 / P.V == (e0 + VW - 1) / P.V;
+}
+
+// The streamed vectors of row r inside vectors [vbeg, vend), as offsets
+// [b, e) relative to vbeg.
+template <typename LT>
+__device__ __forceinline__ void row_vectors(const Params &P, int64_t r, int64_t vbeg, int64_t vend, int &b, int &e)
+{
+    constexpr int VW = 16 / sizeof(LT);
+    const int64_t lo = r * P.V - P.h, hi = (r + 1) * P.V - P.h; // ids relative to vector 1's first id
+    // first vector starting at or after the row's first id; first vector
+    // ending after its last id (lo > -VW and hi > -VW, so the divisions of
+    // non-negative numbers below are floors)
+    const int64_t vs = (lo + VW - 1 + VW) / VW;
+    const int64_t ve = (hi + VW) / VW;
+    const int64_t vb = max(max(vs, int64_t{1}), vbeg);
+    const int64_t vx = min(min(ve, P.nvec + 1), vend);
+    b = static_cast<int>(vb - vbeg);
+    e = static_cast<int>(max(vx, vb) - vbeg);
+}
+
+// The epilogue lane's share of the ids of row r that CTA g reads one by
+// one: lanes 8.. take the vector holding the row's first id, lanes 16.. the
+// one holding its last id (when it is another vector), each only if that
+// vector is not streamed and belongs to CTA g.  A lane's pair is (z, 1), or
+// stays (-inf, 0) when it has none.
+template <typename LT>
+__device__ __forceinline__ void ragged_pair(const Params &P, int64_t g, int64_t r, int lane, float &M, float &S)
+{
+    constexpr int VW = 16 / sizeof(LT);
+    const int64_t vf = vec_of_elem<LT>(P, r * P.V);
+    const int64_t vl = vec_of_elem<LT>(P, r * P.V + P.V - 1);
+    int64_t vv = -1;
+    int i = 0;
+    if (lane >= 8 && lane < 8 + VW) {
+        vv = vf;
+        i = lane - 8;
+    } else if (lane >= 16 && lane < 16 + VW && vl != vf) {
+        vv = vl;
+        i = lane - 16;
+    }
+    if (vv < 0 || vv / P.span != g || streamed<LT>(P, vv))
+        return;
+    const int64_t e = P.h + (vv - 1) * VW + i;
+    if (e >= 0 && e < P.total && e / P.V == r) {
+        M = load_elem<LT>(static_cast<const LT *>(P.logits) + e);
+        S = 1.0f;
+    }
 }
 
 // Reduce the (max, normaliser) pairs of the 32 lanes through a common
@@ -302,140 +337,138 @@ __device__ __forceinline__ void warp_common_max(float &M, float &S, float c)
     M = Mw;
 }
 
-// The row pass.  Persistent CTAs take row items round-robin.  Warps 0..7
-// stream: a thread folds its vectors of the item in steps of U, the next step
-// (possibly of the next item) already requested while the current one is
-// folded; at the end of an item each streaming warp reduces its pairs and
-// hands them to warp 8 through a queue of kRowSlots shared-memory slots,
-// without waiting.  Warp 8 combines the CTA's pair, publishes it, and, when
-// its CTA finishes a row last, runs the accept test; so the fences and
-// atomics of an item never stall the stream.  Slot hand-off uses named
-// barriers: "full" (8 warps arrive, warp 8 waits) and "free" (warp 8
-// arrives, the 8 warps wait before reusing the slot kRowSlots items later).
+// The row pass.  Warps 0..7 stream the CTA's span: a thread folds U vectors
+// per step, the next step already requested while the current one is
+// folded.  A step inside one row takes the plain fold; a step that reaches a
+// row's end folds each row's elements separately, with the others masked to
+// -inf.  When a row's part of the span ends, each streaming warp reduces its
+// pairs and hands them to warp 8 through a queue of kRowSlots shared-memory
+// slots, without waiting.  Warp 8 adds the row's ragged elements, combines
+// the CTA's pair, publishes it, and, when its CTA completes a row last, runs
+// the accept test; so the fences and atomics of a row never stall the
+// stream.  Slot hand-off uses named barriers: "full" (8 warps arrive, warp 8
+// waits) and "free" (warp 8 arrives, the 8 warps wait before reusing the slot
+// kRowSlots rows later).
 constexpr int kRowSlots = 4;
 constexpr int kRowCtaThreads = kThreads + 32;
+constexpr int kRowU = 4;                   // vectors per thread per step
+constexpr int kRowStep = kThreads * kRowU; // vectors per CTA step
+constexpr int64_t kRowMaxSpan = int64_t{1} << 30; // keeps offsets inside a span in int
 
 template <typename LT, bool DENSE>
 __global__ void __launch_bounds__(kRowCtaThreads, SV_ROW_MIN_CTAS) rows_kernel(const Params P)
 {
     constexpr int VW = 16 / sizeof(LT);
-    constexpr int U = 4;                 // vectors per thread per step
-    constexpr int STEP = kThreads * U;   // vectors per CTA step
+    constexpr int U = kRowU;
+    constexpr int STEP = kRowStep;
     __shared__ float sM[kRowSlots][kWarps], sS[kRowSlots][kWarps];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float c = P.c;
-    const int64_t n_items = P.B * P.RI;
-    const int64_t G = gridDim.x;
-    if (static_cast<int64_t>(blockIdx.x) >= n_items)
-        return;
-    const int n_mine = static_cast<int>((n_items - 1 - blockIdx.x) / G) + 1; // items of this CTA
+    const int64_t V = P.V;
+    const int64_t g = blockIdx.x;
+    const int64_t vbeg = g * P.span;
+    const int64_t vend = min(P.NV, vbeg + P.span);
+    // the span's elements [E0, E1) and rows r0..r1
+    const int64_t E0 = max(int64_t{0}, P.h + (vbeg - 1) * VW);
+    const int64_t E1 = min(P.total, P.h + (vend - 1) * VW);
+    const int64_t r0 = E0 / V;
+    const int n_rows = E1 > E0 ? static_cast<int>((E1 - 1) / V - r0 + 1) : 0;
     auto bar_full = [](int q) { return 1u + static_cast<uint32_t>(q); };
     auto bar_free = [](int q) { return 1u + kRowSlots + static_cast<uint32_t>(q); };
 
     if (warp == kWarps) {
         // ---- epilogue warp
-        for (int k = 0; k < n_mine; ++k) {
-            const int64_t it = blockIdx.x + static_cast<int64_t>(k) * G;
-            const int64_t r = divi(it, P.S1);
+        for (int k = 0; k < n_rows; ++k) {
+            const int64_t r = r0 + k;
             RowSide side;
             if (lane == 0)
-                side = fetch_side<LT, DENSE>(P, r); // in flight while the item streams
+                side = fetch_side<LT, DENSE>(P, r); // in flight while the row streams
+            float M = -INFINITY, S = 0.0f;
+            ragged_pair<LT>(P, g, r, lane, M, S);
+            const int64_t first = vec_of_elem<LT>(P, r * V) / P.span;
+            const int n_parts = static_cast<int>(vec_of_elem<LT>(P, r * V + V - 1) / P.span - first + 1);
             const int q = k % kRowSlots;
             bar_sync(bar_full(q), kRowCtaThreads);
-            float M = lane < kWarps ? sM[q][lane] : -INFINITY;
-            float S = lane < kWarps ? sS[q][lane] : 0.0f;
-            if (k + kRowSlots < n_mine)
+            if (lane < kWarps) {
+                M = sM[q][lane];
+                S = sS[q][lane];
+            }
+            if (k + kRowSlots < n_rows)
                 bar_arrive(bar_free(q), kRowCtaThreads);
             warp_common_max(M, S, c);
             int last = 0;
             if (lane == 0) {
-                P.row_part[it] = make_float2(M, S);
+                P.row_part[r * P.PM + (g - first)] = make_float2(M, S);
                 __threadfence();
-                last = atomicAdd(&P.row_cnt[r], 1u) == static_cast<unsigned>(P.S1 - 1);
+                last = atomicAdd(&P.row_cnt[r], 1u) == static_cast<unsigned>(n_parts - 1);
             }
             last = __shfl_sync(0xFFFFFFFFu, last, 0);
             if (last)
-                finish_row<LT, DENSE>(P, r, lane, side);
+                finish_row<LT, DENSE>(P, r, n_parts, lane, side);
         }
         pdl_launch_dependents();
         return;
     }
 
-    // ---- streaming warps
-    const uint4 neg_inf = sizeof(LT) == 2 ? make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)
-                                          : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
-    auto load_step = [&](const ItemSpan &sp, int s, uint4 (&w)[U]) {
+    // ---- streaming warps: row r0 + k's streamed vectors of the span, in
+    // steps of STEP vectors; one flush per row
+    if (n_rows > 0) {
+        const uint4 neg_inf = sizeof(LT) == 2 ? make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)
+                                              : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+        const uint4 *base = reinterpret_cast<const uint4 *>(static_cast<const LT *>(P.logits) + P.h) + (vbeg - 1);
+        // the step at offset off of a row whose streamed vectors end at offset e
+        auto load_step = [&](int off, int e, uint4 (&w)[U]) {
 #pragma unroll
-        for (int k = 0; k < U; ++k) {
-            const int32_t e = s * STEP + tid + k * kThreads;
-            w[k] = e < sp.nv ? ld_stream_v4(sp.p + e) : neg_inf;
-        }
-    };
-    int k = 0;
-    int64_t it = blockIdx.x;
-    ItemSpan sp = item_span<LT, STEP>(P, it);
-    int s = 0;
-    uint4 cur[U], nxt[U];
-    load_step(sp, 0, cur);
-    float M = -INFINITY;
-    unsigned long long S[4] = {0ull, 0ull, 0ull, 0ull}; // packed (+0, +0) pairs
-    for (;;) {
-        // the next step, possibly of the next item, is requested first
-        ItemSpan spn = sp;
-        int64_t itn = it;
-        int sn = s + 1;
-        if (sn >= sp.nsteps) {
-            itn = it + G;
-            sn = 0;
-            if (itn < n_items)
-                spn = item_span<LT, STEP>(P, itn);
-        }
-        const bool more = itn < n_items;
-        if (more)
-            load_step(spn, sn, nxt);
-        fold<LT, U>(cur, M, S, c);
-
-        if (s + 1 >= sp.nsteps) {
-            // ---- end of item `it`: reduce and hand the pair to the epilogue warp
-            float a0, a1;
-            unpack2(add2(add2(S[0], S[1]), add2(S[2], S[3])), a0, a1);
-            float Ssum = __fadd_rn(a0, a1);
-            const int64_t r = divi(it, P.S1);
-            const int32_t ch = static_cast<int32_t>(it - r * P.S1);
-            if (ch == 0 || ch == P.S1 - 1) {
-                const LT *row = row_ptr<LT>(P, r);
-                const int32_t head = row_head(row, P.V);
-                const int32_t tail0 = head + (P.V - head) / VW * VW;
-                if (ch == 0)
-                    for (int32_t e = tid; e < head; e += kThreads)
-                        merge_ms(M, Ssum, load_elem<LT>(row + e), 1.0f, c);
-                if (ch == P.S1 - 1)
-                    for (int32_t e = tail0 + tid; e < P.V; e += kThreads)
-                        merge_ms(M, Ssum, load_elem<LT>(row + e), 1.0f, c);
+            for (int k = 0; k < U; ++k) {
+                const int i = off + k * kThreads + tid;
+                w[k] = i < e ? ld_stream_v4(base + i) : neg_inf;
             }
-            warp_common_max(M, Ssum, c);
-            const int q = k % kRowSlots;
-            if (k >= kRowSlots)
-                bar_sync(bar_free(q), kRowCtaThreads); // the epilogue has read the slot's last use
-            if (lane == 0) {
-                sM[q][warp] = M;
-                sS[q][warp] = Ssum;
+        };
+        const int64_t r_last = r0 + n_rows - 1;
+        int64_t row = r0;
+        int off, e;
+        row_vectors<LT>(P, row, vbeg, vend, off, e);
+        float M = -INFINITY;
+        unsigned long long S[2] = {0ull, 0ull}; // packed (+0, +0) pairs
+        uint4 cur[U], nxt[U];
+        load_step(off, e, cur);
+        for (int k = 0;;) {
+            // the next step, possibly of the next row, is requested first
+            int noff = off + STEP, ne = e;
+            const bool row_done = noff >= e;
+            if (row_done && row < r_last)
+                row_vectors<LT>(P, row + 1, vbeg, vend, noff, ne);
+            const bool more = !row_done || row < r_last;
+            if (more)
+                load_step(noff, ne, nxt);
+            fold<LT, U>(cur, M, S, c);
+            if (row_done) {
+                // hand the row's pairs to the epilogue warp
+                float a0, a1;
+                unpack2(add2(S[0], S[1]), a0, a1);
+                float Ssum = __fadd_rn(a0, a1);
+                warp_common_max(M, Ssum, c);
+                const int q = k % kRowSlots;
+                if (k >= kRowSlots)
+                    bar_sync(bar_free(q), kRowCtaThreads); // the epilogue has read the slot's last use
+                if (lane == 0) {
+                    sM[q][warp] = M;
+                    sS[q][warp] = Ssum;
+                }
+                bar_arrive(bar_full(q), kRowCtaThreads);
+                ++k;
+                ++row;
+                M = -INFINITY;
+                S[0] = S[1] = 0ull;
             }
-            bar_arrive(bar_full(q), kRowCtaThreads);
-            ++k;
-            M = -INFINITY;
+            if (!more)
+                break;
 #pragma unroll
-            for (int a = 0; a < 4; ++a)
-                S[a] = 0ull;
+            for (int j = 0; j < U; ++j)
+                cur[j] = nxt[j];
+            off = noff;
+            e = ne;
         }
-        if (!more)
-            break;
-#pragma unroll
-        for (int j = 0; j < U; ++j)
-            cur[j] = nxt[j];
-        sp = spn;
-        it = itn;
-        s = sn;
     }
     pdl_launch_dependents();
 }
