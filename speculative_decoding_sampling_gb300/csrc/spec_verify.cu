@@ -32,10 +32,10 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 struct Plan {
     int64_t R;    // rows B*(K+1)
     int32_t PM;   // row_part slots per row
-    int32_t NSL;  // survivor slices per sequence
+    int32_t CPS;  // final-draw chunks per sequence
     int32_t fix;  // fractional bits of the fixed-point masses
     size_t off_part, off_row_cnt, off_row_m, off_row_s, off_acc, off_seq_cnt, off_seq_bad, off_jstar, off_seq_m,
-        off_seq_s, off_surv_cnt, off_seqE, off_seqF, off_slice, off_rec_a, off_rec_q, off_ctr, bytes;
+        off_seq_s, off_surv_cnt, off_seqE, off_seqF, off_rec_a, off_rec_q, bytes;
 };
 
 bool make_plan(int64_t B, int32_t K, int32_t V, Plan &p)
@@ -50,7 +50,7 @@ bool make_plan(int64_t B, int32_t K, int32_t V, Plan &p)
     // row_part slots per row: enough for any cut of the flat row array into
     // at most kRowMaxCtas spans (the launch widens spans to keep to it)
     p.PM = static_cast<int32_t>(p.R > 0 ? ceil_div(sv::kRowMaxCtas, p.R) + 3 : 4);
-    p.NSL = static_cast<int32_t>(ceil_div(V, static_cast<int64_t>(sv::kSliceGroups) * sv::kGroup));
+    p.CPS = static_cast<int32_t>(ceil_div(V, static_cast<int64_t>(sv::kChunkGroups) * sv::kGroup));
     const int fb = 62 - ceil_log2_u64(static_cast<uint64_t>(V) + 1);
     p.fix = fb < 40 ? fb : 40;
     const size_t Bz = static_cast<size_t>(B), R = static_cast<size_t>(p.R);
@@ -68,10 +68,8 @@ bool make_plan(int64_t B, int32_t K, int32_t V, Plan &p)
     p.off_surv_cnt = off; off = align_up(off + Bz * sizeof(uint32_t));
     p.off_seqE = off;     off = align_up(off + Bz * sizeof(long long));
     p.off_seqF = off;     off = align_up(off + Bz * sizeof(long long));
-    p.off_slice = off;    off = align_up(off + Bz * p.NSL * 2 * sizeof(long long));
-    p.off_rec_a = off;    off = align_up(off + Bz * p.NSL * sv::kSliceTiles * sizeof(long long));
-    p.off_rec_q = off;    off = align_up(off + Bz * p.NSL * sv::kSliceTiles * sizeof(float));
-    p.off_ctr = off;      off = align_up(off + 2 * sizeof(unsigned long long));
+    p.off_rec_a = off;    off = align_up(off + Bz * p.CPS * sizeof(long long));
+    p.off_rec_q = off;    off = align_up(off + Bz * p.CPS * sizeof(float));
     p.bytes = off;
     return true;
 }
@@ -81,7 +79,6 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 enum Stage { kRows = 1, kSurvivors = 2, kBoth = 3 };
 
 constexpr int kMaxDevices = 64;
-constexpr int kDrawSmem = sv::kWarps * sv::kWarpSmem; // the draw warps' async-copy rings
 
 // Per device and kernel instantiation: how many CTAs of each kernel fit on
 // the device at once (the grids of the persistent kernels).
@@ -107,14 +104,14 @@ cudaError_t resident_ctas(Resident &out)
         if (e != cudaSuccess)
             return e;
         e = cudaFuncSetAttribute(sv::survivor_kernel<LT, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kDrawSmem);
+                                 sv::DrawShape<LT, DENSE>::kCtaBytes);
         if (e != cudaSuccess)
             return e;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&rows, sv::rows_kernel<LT, DENSE>, sv::kRowCtaThreads, 0);
         if (e != cudaSuccess)
             return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&draw, sv::survivor_kernel<LT, DENSE>, sv::kThreads,
-                                                          kDrawSmem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&draw, sv::survivor_kernel<LT, DENSE>,
+                                                          sv::kDrawWarps * 32, sv::DrawShape<LT, DENSE>::kCtaBytes);
         if (e != cudaSuccess)
             return e;
         sms = sms > 0 ? sms : 1;
@@ -165,8 +162,8 @@ cudaError_t launch(sv::Params P, const Plan &plan, int stages, cudaStream_t stre
             return e;
     }
     if (stages & kSurvivors) {
-        const int64_t grid = clamp_grid(ceil_div(P.B * plan.NSL, sv::kWarps), res.draw);
-        P.n_warps = static_cast<uint64_t>(grid) * sv::kWarps;
+        // at least one chunk per warp
+        const int64_t grid = clamp_grid(ceil_div(P.NC, sv::kDrawWarps), res.draw);
         // programmatic dependent launch: the draw's CTAs may be scheduled
         // while the row pass drains; they wait in griddepcontrol.wait for
         // its completion before reading anything it wrote
@@ -175,8 +172,8 @@ cudaError_t launch(sv::Params P, const Plan &plan, int stages, cudaStream_t stre
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(grid));
-        cfg.blockDim = dim3(sv::kThreads);
-        cfg.dynamicSmemBytes = kDrawSmem;
+        cfg.blockDim = dim3(sv::kDrawWarps * 32);
+        cfg.dynamicSmemBytes = sv::DrawShape<LT, DENSE>::kCtaBytes;
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
@@ -249,15 +246,14 @@ sv_status_t run(int stages, const void *logits, sv_dtype_t dtype, const float *q
     P.surv_cnt = reinterpret_cast<uint32_t *>(ws + plan.off_surv_cnt);
     P.seq_E = reinterpret_cast<long long *>(ws + plan.off_seqE);
     P.seq_F = reinterpret_cast<long long *>(ws + plan.off_seqF);
-    P.slice_tot = reinterpret_cast<long long *>(ws + plan.off_slice);
     P.rec_a = reinterpret_cast<long long *>(ws + plan.off_rec_a);
     P.rec_q = reinterpret_cast<float *>(ws + plan.off_rec_q);
-    P.ctr = reinterpret_cast<unsigned long long *>(ws + plan.off_ctr);
     P.PM = plan.PM;
-    P.NSL = plan.NSL;
+    P.CPS = plan.CPS;
+    P.NC = B * static_cast<int64_t>(plan.CPS);
+    P.ring_ok = (V % sv::kGroup) == 0 && aligned(logits, 16) && (P.q == nullptr || aligned(P.q, 16)) ? 1 : 0;
     P.fix_bits = plan.fix;
     P.total = P.h = P.nvec = P.NV = P.span = 0;
-    P.n_warps = 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;

@@ -12,17 +12,23 @@ namespace sv {
 #ifndef SV_ROW_MIN_SPAN
 #define SV_ROW_MIN_SPAN 1024 // row pass: fewest 16-byte vectors a CTA streams
 #endif
+#ifndef SV_ROW_WARPS
+#define SV_ROW_WARPS 8    // row pass: streaming warps of a CTA
+#endif
+#ifndef SV_ROW_U
+#define SV_ROW_U 4        // row pass: 16-byte vectors a thread loads per step
+#endif
 #ifndef SV_ROW_MIN_CTAS
 #define SV_ROW_MIN_CTAS 4 // row pass: resident CTAs per SM the register budget is cut for
 #endif
-#ifndef SV_STAGES
-#define SV_STAGES 3       // final draw: per-warp async-copy ring depth
+#ifndef SV_DRAW_STAGES
+#define SV_DRAW_STAGES 3  // final draw: chunks in a warp's async-copy ring
 #endif
-#ifndef SV_STAGE_BYTES
-#define SV_STAGE_BYTES 2048
+#ifndef SV_DRAW_WARPS
+#define SV_DRAW_WARPS 4   // final draw: warps of a CTA
 #endif
 #ifndef SV_MIN_CTAS
-#define SV_MIN_CTAS 4     // final draw: resident CTAs per SM the register budget is cut for
+#define SV_MIN_CTAS 3     // final draw: resident CTAs per SM the register budget is cut for
 #endif
 
 constexpr int kThreads = 256;          // threads of a CTA
@@ -30,12 +36,11 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kRowMinSpan = SV_ROW_MIN_SPAN;
 constexpr int kRowMaxCtas = 4096;      // row pass: most CTAs a call's span is cut for
 constexpr int kGroup = 8;              // consecutive ids a lane owns in the final draw
-constexpr int kSliceGroups = 256;      // groups of one survivor slice item (2048 ids)
-constexpr int kSliceTiles = kSliceGroups / 32; // warp tiles of a slice
-constexpr int kStages = SV_STAGES;     // per-warp async-copy ring depth
-constexpr int kStageBytes = SV_STAGE_BYTES; // one stage: 16-byte pieces, a multiple of 512 per warp
-constexpr int kWarpSmem = kStages * kStageBytes;
-static_assert(kStages >= 2 && kStageBytes % 512 == 0 && kStageBytes >= 2048, "ring shape");
+constexpr int kChunkTiles = 4;        // warp tiles (32 groups each) of a final-draw chunk
+constexpr int kChunkGroups = kChunkTiles * 32; // groups of a chunk (1024 ids)
+constexpr int kDrawStages = SV_DRAW_STAGES; // chunks in a draw warp's async-copy ring
+constexpr int kDrawWarps = SV_DRAW_WARPS;   // warps of a draw CTA
+static_assert(kDrawStages >= 2 && kDrawWarps >= 1 && kDrawWarps <= 32, "draw ring shape");
 
 // Device status bits (the values the public header documents).
 constexpr int32_t kBadU = 1, kBadToken = 2, kBadQ = 4, kBadRow = 8, kDegenerate = 16;
@@ -66,22 +71,21 @@ struct Params {
     int32_t *seq_jstar;   // [B]       row the final token is drawn from, -1 = bad
     float *seq_m;         // [B]       max of z of that row
     float *seq_s;         // [B]       fp32 normaliser of that row
-    uint32_t *surv_cnt;   // [B]       survivor slices done
+    uint32_t *surv_cnt;   // [B]       final-draw chunks done
     long long *seq_E;     // [B]       exact sum of pt over the surviving row (dense), 2^-fix_bits units
     long long *seq_F;     // [B]       sum of pt (one-hot normaliser), 2^-fix_bits units
-    long long *slice_tot; // [B * NSL * 2] per slice: mass A, bits(double Qp)
-    long long *rec_a;     // [B * NSL * 8] per warp tile: mass A
-    float *rec_q;         // [B * NSL * 8] per warp tile: Qp
-    unsigned long long *ctr; // [2] next slice ticket, draw warps done
+    long long *rec_a;     // [B * CPS] per chunk: mass A, 2^-fix_bits units
+    float *rec_q;         // [B * CPS] per chunk: Qp
     int64_t total;        // R * V elements of the logits
     int64_t h;            // elements before the first 16-byte boundary (< 16 / element size)
     int64_t nvec;         // whole 16-byte vectors from there on
     int64_t NV;           // nvec + 2: the flat view's vectors, the two ragged ends included
     int64_t span;         // vectors per row-pass CTA
     int32_t PM;           // row_part slots per row
-    int32_t NSL;          // survivor slices per sequence
+    int32_t CPS;          // final-draw chunks per sequence
+    int64_t NC;           // final-draw chunks of the call, B * CPS
+    int32_t ring_ok;      // rows of whole 16-byte aligned groups: the draw streams through its rings
     int32_t fix_bits;     // fractional bits of the fixed-point masses
-    uint64_t n_warps;     // warps of the draw kernel's grid
 };
 
 // ------------------------------------------------------------ element loads
@@ -120,7 +124,7 @@ __device__ __forceinline__ uint8_t ld_cg_u8(const uint8_t *p)
 
 // ------------------------------------------------------- async copies
 //
-// Each warp owns a ring of kStages shared-memory stages.  A lane copies only
+// Each draw warp owns a ring of kDrawStages shared-memory stages.  A lane copies only
 // the 16-byte pieces it will read itself, so completion is tracked with the
 // lane's own copy groups (cp.async.wait_group) and no lane ever waits for
 // another.
@@ -193,13 +197,46 @@ __device__ __forceinline__ void merge_ms(float &M, float &S, float M2, float S2,
 
 // --------------------------------------------------- exact fixed-point mass
 
-// A probability mass w (|w| < 2^22) as an integer multiple of 2^-fix_bits.
-// w * 2^fix_bits is exact in fp32 (a power-of-two scale); the conversion
-// rounds to nearest.  Sums of these integers are exact and independent of
-// the order of summation.
-__device__ __forceinline__ long long to_fixed(float w, float scale)
+// A finite fp32 value w as the nearest integer multiple of 2^-fb (halves
+// away from zero), for |w| * 2^fb < 2^62.  Sums of these integers are exact
+// and independent of the order of summation.  Integer ALU only: w = m * 2^(e-150)
+// with a 24-bit m, so w * 2^fb = m * 2^s, s = e - 150 + fb, is a shift of m
+// (rounded when s < 0).  The float-to-64-bit-integer conversion instruction
+// is avoided on purpose: it runs on the double-precision pipe, which is
+// narrow on this GPU.
+__device__ __forceinline__ long long to_fixed(float w, int fb)
 {
-    return __float2ll_rn(__fmul_rn(w, scale));
+    const uint32_t b = __float_as_uint(w);
+    const int e = static_cast<int>((b >> 23) & 0xFFu);
+    const uint32_t m = (b & 0x7FFFFFu) | 0x800000u;
+    const int s = e - 150 + fb;
+    long long r;
+    if (s >= 0)
+        r = static_cast<long long>(m) << (s < 38 ? s : 38);
+    else
+        r = -s < 32 ? static_cast<long long>((m + (1u << (-s - 1))) >> -s) : 0;
+    if (e == 0)
+        r = 0; // zero or subnormal: below 2^-126
+    return (b >> 31) ? -r : r;
+}
+
+// floor(u * Z) for u in [0, 1) and 0 <= Z < 2^62, exactly: u = mu * 2^-k with
+// a 24-bit mu and k >= 24, so u * Z = (mu * Z) / 2^k with a 96-bit product.
+__device__ __forceinline__ long long mul_floor(float u, long long Z)
+{
+    const uint32_t b = __float_as_uint(u);
+    const int e = static_cast<int>((b >> 23) & 0xFFu);
+    if (e == 0 || Z <= 0)
+        return 0; // u = 0 (or subnormal, below 2^-126: u * Z < 1)
+    const unsigned long long mu = (b & 0x7FFFFFu) | 0x800000u;
+    const int k = 150 - e; // u = mu * 2^-k, k >= 24 for u < 1
+    const unsigned long long z = static_cast<unsigned long long>(Z);
+    const unsigned long long lo = mu * z, hi = __umul64hi(mu, z);
+    if (k >= 128)
+        return 0;
+    if (k >= 64)
+        return static_cast<long long>(hi >> (k - 64));
+    return static_cast<long long>((lo >> k) | (hi << (64 - k)));
 }
 
 // --------------------------------------------------- packed fp32 pairs
@@ -294,19 +331,11 @@ __device__ __forceinline__ float warp_sum_f(float v)
     return v;
 }
 
-__device__ __forceinline__ double warp_sum_d(double v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    return v;
-}
-
-__device__ __forceinline__ double warp_incl_scan_d(double v, int lane)
+__device__ __forceinline__ long long warp_incl_scan_ll(long long v, int lane)
 {
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const double n = __shfl_up_sync(0xFFFFFFFFu, v, o);
+        const long long n = __shfl_up_sync(0xFFFFFFFFu, v, o);
         if (lane >= o)
             v += n;
     }

@@ -296,7 +296,7 @@ __device__ __forceinline__ void row_vectors(const Params &P, int64_t r, int64_t 
 }
 
 // The epilogue lane's share of the ids of row r that CTA g reads one by
-// one: lanes 8.. take the vector holding the row's first id, lanes 16.. the
+// one: lanes 16.. take the vector holding the row's first id, lanes 24.. the
 // one holding its last id (when it is another vector), each only if that
 // vector is not streamed and belongs to CTA g.  A lane's pair is (z, 1), or
 // stays (-inf, 0) when it has none.
@@ -308,12 +308,12 @@ __device__ __forceinline__ void ragged_pair(const Params &P, int64_t g, int64_t 
     const int64_t vl = vec_of_elem<LT>(P, r * P.V + P.V - 1);
     int64_t vv = -1;
     int i = 0;
-    if (lane >= 8 && lane < 8 + VW) {
+    if (lane >= 16 && lane < 16 + VW) {
         vv = vf;
-        i = lane - 8;
-    } else if (lane >= 16 && lane < 16 + VW && vl != vf) {
-        vv = vl;
         i = lane - 16;
+    } else if (lane >= 24 && lane < 24 + VW && vl != vf) {
+        vv = vl;
+        i = lane - 24;
     }
     if (vv < 0 || vv / P.span != g || streamed<LT>(P, vv))
         return;
@@ -337,22 +337,25 @@ __device__ __forceinline__ void warp_common_max(float &M, float &S, float c)
     M = Mw;
 }
 
-// The row pass.  Warps 0..7 stream the CTA's span: a thread folds U vectors
-// per step, the next step already requested while the current one is
-// folded.  A step inside one row takes the plain fold; a step that reaches a
-// row's end folds each row's elements separately, with the others masked to
-// -inf.  When a row's part of the span ends, each streaming warp reduces its
-// pairs and hands them to warp 8 through a queue of kRowSlots shared-memory
-// slots, without waiting.  Warp 8 adds the row's ragged elements, combines
-// the CTA's pair, publishes it, and, when its CTA completes a row last, runs
-// the accept test; so the fences and atomics of a row never stall the
-// stream.  Slot hand-off uses named barriers: "full" (8 warps arrive, warp 8
-// waits) and "free" (warp 8 arrives, the 8 warps wait before reusing the slot
-// kRowSlots rows later).
+// The row pass.  The kRowWarps streaming warps walk the CTA's span row by
+// row: a thread folds U vectors per step, the next step (possibly of the next
+// row) already requested while the current one is folded; a step never
+// crosses a row's end.  When a row's part of the span is done, each streaming
+// warp reduces its pairs and hands them to the epilogue warp (the last one)
+// through a queue of kRowSlots shared-memory slots, without waiting.  The
+// epilogue warp adds the row's ids it reads one by one, combines the CTA's
+// pair, publishes it, and, when its CTA completes a row last, runs the accept
+// test; so the fences and atomics of a row never stall the stream.  Slot
+// hand-off uses named barriers: "full" (streaming warps arrive, the epilogue
+// warp waits) and "free" (the epilogue warp arrives, the streaming warps wait
+// before reusing the slot kRowSlots rows later).
 constexpr int kRowSlots = 4;
-constexpr int kRowCtaThreads = kThreads + 32;
-constexpr int kRowU = 4;                   // vectors per thread per step
-constexpr int kRowStep = kThreads * kRowU; // vectors per CTA step
+constexpr int kRowWarps = SV_ROW_WARPS;            // streaming warps of a CTA
+constexpr int kRowThreads = kRowWarps * 32;
+constexpr int kRowCtaThreads = kRowThreads + 32;   // and the epilogue warp
+constexpr int kRowU = SV_ROW_U;                    // vectors per thread per step
+constexpr int kRowStep = kRowThreads * kRowU;      // vectors per CTA step
+static_assert(kRowWarps >= 1 && kRowWarps <= 16 && kRowU >= 1, "row CTA shape (lanes 16..31 of the epilogue warp read ragged ids)");
 constexpr int64_t kRowMaxSpan = int64_t{1} << 30; // keeps offsets inside a span in int
 
 template <typename LT, bool DENSE>
@@ -361,7 +364,7 @@ __global__ void __launch_bounds__(kRowCtaThreads, SV_ROW_MIN_CTAS) rows_kernel(c
     constexpr int VW = 16 / sizeof(LT);
     constexpr int U = kRowU;
     constexpr int STEP = kRowStep;
-    __shared__ float sM[kRowSlots][kWarps], sS[kRowSlots][kWarps];
+    __shared__ float sM[kRowSlots][kRowWarps], sS[kRowSlots][kRowWarps];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float c = P.c;
     const int64_t V = P.V;
@@ -376,7 +379,7 @@ __global__ void __launch_bounds__(kRowCtaThreads, SV_ROW_MIN_CTAS) rows_kernel(c
     auto bar_full = [](int q) { return 1u + static_cast<uint32_t>(q); };
     auto bar_free = [](int q) { return 1u + kRowSlots + static_cast<uint32_t>(q); };
 
-    if (warp == kWarps) {
+    if (warp == kRowWarps) {
         // ---- epilogue warp
         for (int k = 0; k < n_rows; ++k) {
             const int64_t r = r0 + k;
@@ -389,7 +392,7 @@ __global__ void __launch_bounds__(kRowCtaThreads, SV_ROW_MIN_CTAS) rows_kernel(c
             const int n_parts = static_cast<int>(vec_of_elem<LT>(P, r * V + V - 1) / P.span - first + 1);
             const int q = k % kRowSlots;
             bar_sync(bar_full(q), kRowCtaThreads);
-            if (lane < kWarps) {
+            if (lane < kRowWarps) {
                 M = sM[q][lane];
                 S = sS[q][lane];
             }
@@ -420,7 +423,7 @@ __global__ void __launch_bounds__(kRowCtaThreads, SV_ROW_MIN_CTAS) rows_kernel(c
         auto load_step = [&](int off, int e, uint4 (&w)[U]) {
 #pragma unroll
             for (int k = 0; k < U; ++k) {
-                const int i = off + k * kThreads + tid;
+                const int i = off + k * kRowThreads + tid;
                 w[k] = i < e ? ld_stream_v4(base + i) : neg_inf;
             }
         };
