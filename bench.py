@@ -1,8 +1,9 @@
 #!/usr/bin/env python3
 """Benchmark of the speculative-sampling verification step on GB300.
 
-One step = one spec_verify call over a whole batch (row pass + final draw)
-with inputs resident in HBM.  Prints ONE JSON line on rank 0.
+One step = one spec_verify call over a whole batch: two launches, the row
+pass (rows_kernel) and the final draws (survivor_kernel), with inputs
+resident in HBM.  Prints ONE JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle, timed on the host
@@ -46,18 +47,21 @@ def peaks():
 # ----------------------------------------------------------- byte accounting
 
 def algorithmic_bytes(w, num_emitted: np.ndarray) -> dict:
-    """Bytes each kernel must move for this batch (the algorithmic count):
-    rows kernel: every logit once, the q(x) gathers as 32-byte sectors, the
-    tokens, uniforms and its outputs; draw kernel: the surviving logit row
-    once more and, after a rejection with dense q, that q row, plus outputs."""
-    B, K, V = w.B if num_emitted is None else len(num_emitted), w.K, w.V
+    """Bytes each kernel must move for this batch (the algorithmic count).
+
+    rows_kernel: every logit once, the q(x) gathers (one 32-byte sector each,
+    dense drafts), the logit gathers z(x) (one sector each), the tokens and
+    uniforms, and its outputs.  survivor_kernel: the surviving logit row once
+    more and, after a rejection with dense q, that q row, plus its outputs."""
+    B = len(num_emitted)
+    K, V = w.K, w.V
     es = 2 if w.dtype == "bf16" else 4
     rows = B * (K + 1) * V * es
-    rows += B * K * (4 + (0 if w.onehot else 32) + 4 + 1)   # tokens, q(x), a, flag
-    rows += B * (K + 1) * 4 * 2 + B * 4                        # u, out_tokens, num_emitted
+    rows += B * K * (4 + 32 + (0 if w.onehot else 32) + 4 + 1)   # tokens, z(x), q(x), a, flag
+    rows += B * (K + 1) * 4 * 2 + B * 4                          # u, out_tokens, num_emitted
     rejected = int(np.sum(num_emitted <= K))
     surv = B * V * es + (0 if w.onehot else rejected * V * 4) + B * (4 + 4 + 4)
-    return {"rows": rows, "survivors": surv, "total": rows + surv, "rejected": rejected}
+    return {"rows_kernel": rows, "survivor_kernel": surv, "total": rows + surv, "rejected": rejected}
 
 
 def kernel_source_hash() -> str:
@@ -70,15 +74,16 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per verify_kernel launch from the committed ncu summary, if it
-    was taken on the current kernel source; else None."""
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    (profiles/traffic.json), if it was taken on the current kernel source;
+    else None."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
             d = json.load(fh)
         e = d.get(workload)
         if e and e.get("source_hash") == kernel_source_hash():
-            return e.get("verify_kernel_dram_bytes_per_launch")
+            return e.get("dram_bytes_per_launch", {}).get(kernel)
     except Exception:
         pass
     return None
@@ -193,13 +198,22 @@ def run_gpu(args):
 
     cargs = args_for(d_logits, d_q, d_tok, d_u, out)
 
-    def step(evs=None):
-        # one call = one launch of the persistent verification kernel
-        if evs is not None:
-            evs[0].record(stream)
+    def step():
+        # one call = the two launches of the path (row pass, final draws),
+        # the second chained to the first by programmatic dependent launch
         rc = lib.spec_verify(*cargs)
-        if evs is not None:
-            evs[1].record(stream)
+        if rc:
+            raise RuntimeError(sv.sv_status_string(rc))
+
+    def staged_step(evs):
+        # the same two launches through the per-stage entry points, with
+        # events between them (this breaks the launch chaining, so it is
+        # used for per-kernel durations only)
+        evs[0].record(stream)
+        rc = lib.sv_verify_rows(*cargs)
+        evs[1].record(stream)
+        rc |= lib.sv_sample_survivors(*cargs)
+        evs[2].record(stream)
         if rc:
             raise RuntimeError(sv.sv_status_string(rc))
 
@@ -208,27 +222,34 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    # warm-up (also the parity reference outputs of this batch)
+    # warm-up
     for _ in range(max(args.warmup, 3)):
         step()
     barrier()
 
-    # ---- timed region: K steps, per-kernel events inside it
+    # ---- timed region: K steps of the public call
     clocks = ClockSampler(local)
     clocks.start()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     barrier()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    for i in range(args.steps):
-        step(evs[i])
+    for _ in range(args.steps):
+        step()
     t_end.record(stream)
     barrier()
-    clk = clocks.stop()
     ms_total = t_start.elapsed_time(t_end)
-    kern_ms = [e[0].elapsed_time(e[1]) for e in evs]
     ms_step = ms_total / args.steps
+
+    # ---- per-kernel durations: the same launches, events between them
+    n_k = max(20, min(args.steps, 500))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_k)]
+    for i in range(n_k):
+        staged_step(evs[i])
+    barrier()
+    clk = clocks.stop()
+    rows_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / n_k
+    surv_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / n_k
     if world > 1:
         t = torch.tensor([ms_step], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -239,8 +260,8 @@ def run_gpu(args):
     tokens_per_step = int(num_emitted.sum())
     nbytes = algorithmic_bytes(w, num_emitted)
     peak, peak_kind = peaks()
-    kern_avg = sum(kern_ms) / len(kern_ms)
-    kern_gbs = nbytes["total"] / (kern_avg * 1e-3) / 1e9
+    rows_gbs = nbytes["rows_kernel"] / (rows_ms * 1e-3) / 1e9
+    surv_gbs = nbytes["survivor_kernel"] / (surv_ms * 1e-3) / 1e9
     step_gbs = nbytes["total"] / (ms_step * 1e-3) / 1e9
 
     # ---- end to end through the public call with pinned host buffers
@@ -312,17 +333,19 @@ def run_gpu(args):
                        "parallelism": f"replicas x{world} (shard over sequences)"},
             "tokens_per_s": tokens_per_step * world / (ms_step * 1e-3),
             "hbm_gbs_step": step_gbs,
-            "hbm_frac_of_8tbs_step": step_gbs / NOMINAL_HBM_GBS,
-            "kernels_ms": {"verify_kernel": kern_avg},
+            "hbm_frac_step": {"of_measured": step_gbs / peak, "of_8tbs_nominal": step_gbs / NOMINAL_HBM_GBS},
+            "kernels_ms": {"rows_kernel": rows_ms, "survivor_kernel": surv_ms,
+                           "source": f"{n_k} staged calls with CUDA events between the two launches"},
+            "kernels_gbs": {"rows_kernel": rows_gbs, "survivor_kernel": surv_gbs},
             "algorithmic_bytes": nbytes,
-            "roofline": {"bound": "hbm", "kernel": "verify_kernel",
-                         "achieved": kern_gbs, "peak": peak, "unit": "GB/s",
-                         "frac": kern_gbs / peak, "peak_source": peak_kind,
-                         "traffic": recorded_traffic(w.name)},
+            "roofline": {"bound": "hbm", "kernel": "rows_kernel",
+                         "achieved": rows_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": rows_gbs / peak, "peak_source": peak_kind,
+                         "traffic": recorded_traffic(w.name, "rows_kernel")},
             "e2e": {"value": seqs / (e2e_ms * 1e-3), "unit": "seqs/s",
                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-            "gpu_launches": args.steps,
+            "gpu_launches": 2 * args.steps,
             "clocks": clk,
             "status_bits": st,
             "cpu_baseline": cpu,
@@ -407,7 +430,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
