@@ -8,8 +8,8 @@
 #include <cuda_runtime.h>
 #include <mutex>
 
+#include "sv_final.cuh"
 #include "sv_rows.cuh"
-#include "sv_survivor.cuh"
 
 namespace {
 
@@ -34,8 +34,8 @@ struct Plan {
     int32_t PM;   // row_part slots per row
     int32_t CPS;  // final-draw chunks per sequence
     int32_t fix;  // fractional bits of the fixed-point masses
-    size_t off_part, off_row_cnt, off_row_m, off_row_s, off_acc, off_seq_cnt, off_seq_bad, off_jstar, off_seq_m,
-        off_seq_s, off_surv_cnt, off_seqE, off_seqF, off_rec_a, off_rec_q, bytes;
+    size_t off_part, off_row_side, off_jstar, off_seq_m,
+        off_seq_s, off_seqE, off_seqF, off_rec_a, off_rec_q, bytes;
 };
 
 bool make_plan(int64_t B, int32_t K, int32_t V, Plan &p)
@@ -56,16 +56,10 @@ bool make_plan(int64_t B, int32_t K, int32_t V, Plan &p)
     const size_t Bz = static_cast<size_t>(B), R = static_cast<size_t>(p.R);
     size_t off = 0;
     p.off_part = off;     off = align_up(off + R * p.PM * sizeof(float2));
-    p.off_row_cnt = off;  off = align_up(off + R * sizeof(uint32_t));
-    p.off_row_m = off;    off = align_up(off + R * sizeof(float));
-    p.off_row_s = off;    off = align_up(off + R * sizeof(float));
-    p.off_acc = off;      off = align_up(off + Bz * K * sizeof(uint8_t));
-    p.off_seq_cnt = off;  off = align_up(off + Bz * sizeof(uint32_t));
-    p.off_seq_bad = off;  off = align_up(off + Bz * sizeof(int32_t));
+    p.off_row_side = off; off = align_up(off + R * sizeof(float4));
     p.off_jstar = off;    off = align_up(off + Bz * sizeof(int32_t));
     p.off_seq_m = off;    off = align_up(off + Bz * sizeof(float));
     p.off_seq_s = off;    off = align_up(off + Bz * sizeof(float));
-    p.off_surv_cnt = off; off = align_up(off + Bz * sizeof(uint32_t));
     p.off_seqE = off;     off = align_up(off + Bz * sizeof(long long));
     p.off_seqF = off;     off = align_up(off + Bz * sizeof(long long));
     p.off_rec_a = off;    off = align_up(off + Bz * p.CPS * sizeof(long long));
@@ -180,6 +174,16 @@ cudaError_t launch(sv::Params P, const Plan &plan, int stages, cudaStream_t stre
         e = cudaLaunchKernelEx(&cfg, sv::survivor_kernel<LT, DENSE>, P);
         if (e != cudaSuccess)
             return e;
+        // the final draws: one CTA per sequence, chained the same way
+        cudaLaunchConfig_t fcfg = {};
+        fcfg.gridDim = dim3(static_cast<unsigned>(P.B < 0x7FFFFFFF ? P.B : 0x7FFFFFFF));
+        fcfg.blockDim = dim3(sv::kFinalThreads);
+        fcfg.stream = stream;
+        fcfg.attrs = attr;
+        fcfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&fcfg, sv::final_kernel<LT, DENSE>, P);
+        if (e != cudaSuccess)
+            return e;
     }
     return cudaSuccess;
 }
@@ -234,16 +238,10 @@ sv_status_t run(int stages, const void *logits, sv_dtype_t dtype, const float *q
     P.residual_mass = residual_mass;
     P.status = status_dev;
     P.row_part = reinterpret_cast<float2 *>(ws + plan.off_part);
-    P.row_cnt = reinterpret_cast<uint32_t *>(ws + plan.off_row_cnt);
-    P.row_m = reinterpret_cast<float *>(ws + plan.off_row_m);
-    P.row_s = reinterpret_cast<float *>(ws + plan.off_row_s);
-    P.acc = reinterpret_cast<uint8_t *>(ws + plan.off_acc);
-    P.seq_cnt = reinterpret_cast<uint32_t *>(ws + plan.off_seq_cnt);
-    P.seq_bad = reinterpret_cast<int32_t *>(ws + plan.off_seq_bad);
+    P.row_side = reinterpret_cast<float4 *>(ws + plan.off_row_side);
     P.seq_jstar = reinterpret_cast<int32_t *>(ws + plan.off_jstar);
     P.seq_m = reinterpret_cast<float *>(ws + plan.off_seq_m);
     P.seq_s = reinterpret_cast<float *>(ws + plan.off_seq_s);
-    P.surv_cnt = reinterpret_cast<uint32_t *>(ws + plan.off_surv_cnt);
     P.seq_E = reinterpret_cast<long long *>(ws + plan.off_seqE);
     P.seq_F = reinterpret_cast<long long *>(ws + plan.off_seqF);
     P.rec_a = reinterpret_cast<long long *>(ws + plan.off_rec_a);

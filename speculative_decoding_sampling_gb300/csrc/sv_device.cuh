@@ -62,16 +62,10 @@ struct Params {
     // workspace views; every word is returned to zero by its last reader, so
     // a completed call leaves the whole workspace zero-filled
     float2 *row_part;     // [R * PM]  (max of z, normaliser relative to it) per CTA a row falls in
-    uint32_t *row_cnt;    // [R]       row parts done
-    float *row_m;         // [R]       max of z over the row
-    float *row_s;         // [R]       fp32 normaliser of the row (relative to fl(m*c))
-    uint8_t *acc;         // [B * K]   1 = accepted
-    uint32_t *seq_cnt;    // [B]       rows done
-    int32_t *seq_bad;     // [B]       status bits of the sequence
-    int32_t *seq_jstar;   // [B]       row the final token is drawn from, -1 = bad
+    float4 *row_side;     // [R]       the row's draft token (int bits), z(x), q(x), u
+    int32_t *seq_jstar;   // [B]       row the final token is drawn from, -1 = bad (written by the draw stream)
     float *seq_m;         // [B]       max of z of that row
     float *seq_s;         // [B]       fp32 normaliser of that row
-    uint32_t *surv_cnt;   // [B]       final-draw chunks done
     long long *seq_E;     // [B]       exact sum of pt over the surviving row (dense), 2^-fix_bits units
     long long *seq_F;     // [B]       sum of pt (one-hot normaliser), 2^-fix_bits units
     long long *rec_a;     // [B * CPS] per chunk: mass A, 2^-fix_bits units
@@ -113,12 +107,6 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *p)
     return r;
 }
 
-__device__ __forceinline__ uint8_t ld_cg_u8(const uint8_t *p)
-{
-    uint16_t v;
-    asm volatile("ld.global.cg.u8 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
-    return static_cast<uint8_t>(v);
-}
 
 
 
@@ -281,6 +269,52 @@ __device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigne
 __device__ __forceinline__ int64_t divi(int64_t a, int64_t b)
 {
     return a < 0x80000000ll ? static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b)) : a / b;
+}
+
+// ------------------------------------------------------ flat logits view
+//
+// The B*(K+1) rows of V ids are one array of R*V elements.  From the first
+// 16-byte boundary on it is cut into whole 16-byte vectors 1..nvec; "vector"
+// 0 stands for the h elements before that boundary and vector nvec+1 for the
+// ragged end.  Row-pass CTA g owns the vectors [g*span, (g+1)*span).
+
+// The vector holding element e (e - h + VW > 0 since h < VW).
+template <typename LT>
+__device__ __forceinline__ int64_t vec_of_elem(const Params &P, int64_t e)
+{
+    constexpr int VW = 16 / sizeof(LT);
+    return (e - P.h + VW) / VW;
+}
+
+// The row-pass CTAs holding the first and last ids of row r: its partials
+// are in slots 0 .. last - first of the row.
+template <typename LT>
+__device__ __forceinline__ void row_ctas(const Params &P, int64_t r, int64_t &first, int &n_parts)
+{
+    const int64_t V = P.V;
+    first = vec_of_elem<LT>(P, r * V) / P.span;
+    n_parts = static_cast<int>(vec_of_elem<LT>(P, r * V + V - 1) / P.span - first + 1);
+}
+
+// ---------------------------------------------- release/acquire counters
+//
+// A completion counter bumped with acquire-release semantics: the bump
+// releases this thread's earlier writes (partials, records) and, for the
+// thread that sees the count complete, acquires everyone else's; no full
+// fence is needed on either side.
+
+__device__ __forceinline__ unsigned long long atom_add_acq_rel(unsigned long long *p, unsigned long long v)
+{
+    unsigned long long old;
+    asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
 }
 
 // ------------------------------------------------- programmatic launch

@@ -1,0 +1,299 @@
+// sv_final.cuh -- the final draw of each sequence: one CTA per sequence.
+//
+// Once the draw stream has completed (the kernel boundary), every chunk of
+// every surviving row has its record (A, Qp) and every sequence its
+// normaliser (E or F).  The final token is the first id whose running
+// residual mass exceeds u_K * Z, Z the row's total (inverse CDF in id order,
+// "推测解码：草稿、验证与实际加速", section 算完三个 token 的全部概率, the replay's
+// sampler and its final draw): a block scan over the records finds the chunk,
+// a block scan over the chunk's 128 groups (one per thread, re-formed with
+// the fold's arithmetic) finds the group, and running sums in id order the
+// id.  All boundaries are exact integers in 2^-fb units: u * Z is taken as
+// floor(u * Z) from a 96-bit product, so u * Z < P iff floor(u * Z) < P.
+#pragma once
+
+#include <climits>
+
+#include "sv_survivor.cuh"
+
+namespace sv {
+
+constexpr int kFinalThreads = 128;
+constexpr int kFinalWarps = kFinalThreads / 32;
+
+// A chunk record's boundary mass max(0, A - delta * Qp) in 2^-fb units.
+__device__ __forceinline__ long long rec_value(long long a, float q, float delta)
+{
+    const long long v = a - corr_of(delta, q);
+    return v > 0 ? v : 0;
+}
+
+// Block-wide inclusive scan of one int64 per thread, in thread order; the
+// block total in `tot`.  `sw` holds kFinalWarps values of scratch.
+__device__ __forceinline__ long long block_incl_scan_ll(long long v, long long *sw, long long &tot)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const long long incl = warp_incl_scan_ll(v, lane);
+    if (lane == 31)
+        sw[warp] = incl;
+    __syncthreads();
+    long long off = 0;
+    tot = 0;
+#pragma unroll
+    for (int w = 0; w < kFinalWarps; ++w) {
+        const long long x = sw[w];
+        if (w < warp)
+            off += x;
+        tot += x;
+    }
+    __syncthreads();
+    return incl + off;
+}
+
+// The smallest thread index with `pred`, or kFinalThreads.
+__device__ __forceinline__ int block_first(bool pred, int *si)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, pred);
+    if (lane == 0)
+        si[warp] = m ? warp * 32 + __ffs(m) - 1 : kFinalThreads;
+    __syncthreads();
+    int f = kFinalThreads;
+#pragma unroll
+    for (int w = 0; w < kFinalWarps; ++w)
+        f = min(f, si[w]);
+    __syncthreads();
+    return f;
+}
+
+// The largest value over the block.
+__device__ __forceinline__ int block_max(int v, int *si)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = __reduce_max_sync(0xFFFFFFFFu, v);
+    if (lane == 0)
+        si[warp] = v;
+    __syncthreads();
+    int r = INT_MIN;
+#pragma unroll
+    for (int w = 0; w < kFinalWarps; ++w)
+        r = max(r, si[w]);
+    __syncthreads();
+    return r;
+}
+
+// One round of the id scan: groups g0 .. g0 + 127 of a row, one per thread.
+// Looks for the first id whose boundary (carry + running group values, then
+// running sums in id order within the group) exceeds `rem`; returns it, or
+// -1 with `carry` advanced by the round.  `last_pos` tracks the last id of
+// positive mass seen.  Block-collective.
+template <typename LT, bool DENSE, int MODE>
+__device__ int32_t scan_round(const LT *row, const float *qrow, int32_t g0, int32_t V, bool vec_ok,
+                              const SurvArgs &X, float delta, long long rem, long long &carry, int32_t &last_pos,
+                              long long *sw, int *si)
+{
+    const int tid = threadIdx.x;
+    const int32_t ng = (V + kGroup - 1) / kGroup;
+    const int32_t g = g0 + tid;
+    float z[kGroup], q[kGroup];
+    load_group_any<LT, DENSE>(row, qrow, g, ng, V, vec_ok, z, q);
+    unsigned long long pt2[kGroup / 2];
+    float w[kGroup], qp[kGroup], ws, qs;
+    group_masses<MODE>(z, q, g * kGroup, X, pt2, w, qp, ws, qs);
+    const long long Lg = to_fixed(ws, X.fb) - corr_of(delta, qs);
+    int kpos = -1;
+#pragma unroll
+    for (int k = 0; k < kGroup; ++k)
+        if (w[k] > 0.0f)
+            kpos = k;
+    long long tot;
+    const long long incl = block_incl_scan_ll(Lg, sw, tot) + carry;
+    const int lp = block_max(kpos >= 0 ? g * kGroup + kpos : -1, si);
+    if (lp >= 0)
+        last_pos = lp;
+    const int f = block_first(incl > rem, si);
+    if (f == kFinalThreads) {
+        carry += tot;
+        return -1;
+    }
+    if (tid == f) {
+        // running sums in id order (the group's last boundary is its total,
+        // so an id past rounding falls back to its last id of positive mass)
+        const long long excl = incl - Lg;
+        int32_t tok = g * kGroup + (kpos >= 0 ? kpos : 0);
+        float cw = 0.0f, cq = 0.0f;
+        for (int k = 0; k < kGroup; ++k) {
+            cw = __fadd_rn(cw, w[k]);
+            cq = __fadd_rn(cq, qp[k]);
+            if (w[k] > 0.0f && excl + to_fixed(cw, X.fb) - corr_of(delta, cq) > rem) {
+                tok = g * kGroup + k;
+                break;
+            }
+        }
+        si[0] = tok;
+    }
+    __syncthreads();
+    const int32_t tok = si[0];
+    __syncthreads();
+    return tok;
+}
+
+// The final draw of sequence b and the return of its scratch to zero.
+template <typename LT, bool DENSE>
+__device__ void final_sequence(const Params &P, int64_t b, long long *sw, int *si, long long &s_before)
+{
+    const int tid = threadIdx.x;
+    const int32_t K = P.K, V = P.V, CPS = P.CPS;
+    long long *ra = P.rec_a + b * CPS;
+    float *rq = P.rec_q + b * CPS;
+    const int32_t jstar = __ldcg(&P.seq_jstar[b]);
+    if (jstar >= 0) {
+        const bool rejected = jstar < K;
+        Verdict v;
+        v.jstar = jstar;
+        v.m = __ldcg(&P.seq_m[b]);
+        v.s = __ldcg(&P.seq_s[b]);
+        v.x = (!DENSE && rejected) ? __ldg(&P.tokens[b * K + jstar]) : -1;
+        const LT *row;
+        const float *qrow;
+        seq_rows<LT, DENSE>(P, b, v, row, qrow);
+        const SurvArgs X = surv_args(P, v);
+        const bool vec_ok = (reinterpret_cast<uintptr_t>(row) & 15u) == 0 &&
+                            (qrow == nullptr || (reinterpret_cast<uintptr_t>(qrow) & 15u) == 0);
+        // dense: delta = E - 2^fb = (S' - 1) 2^fb, S' the exact sum of pt;
+        // one-hot: F = sum of pt in 2^-fb units (the residual's normaliser)
+        const long long E = rejected && DENSE ? __ldcg(&P.seq_E[b]) : 0;
+        const long long F = rejected && !DENSE ? __ldcg(&P.seq_F[b]) : 0;
+        const float delta = rejected && DENSE ? static_cast<float>(E - (1ll << P.fix_bits)) : 0.0f;
+        const float u = __ldg(&P.u[b * (K + 1) + K]);
+        // ---- records: thread t holds chunks [t*R, (t+1)*R)
+        const int R = (CPS + kFinalThreads - 1) / kFinalThreads;
+        long long T = 0;
+        int lastc = -1;
+        for (int i = 0; i < R; ++i) {
+            const int c = tid * R + i;
+            if (c < CPS) {
+                const long long vc = rec_value(__ldcg(&ra[c]), __ldcg(&rq[c]), delta);
+                T += vc;
+                if (vc > 0)
+                    lastc = c;
+            }
+        }
+        long long Z;
+        const long long incl = block_incl_scan_ll(T, sw, Z);
+        int32_t tok = -1;
+        const bool degenerate = rejected && !(Z > 0);
+        if (degenerate) {
+            // residual of zero mass after a rejection (impossible in exact
+            // arithmetic): draw from p of the same row instead
+            SurvArgs Xb = X;
+            Xb.x = -1;
+            long long A = 0;
+            const int32_t ng = (V + kGroup - 1) / kGroup;
+            for (int32_t g0 = 0; g0 < ng; g0 += kFinalThreads) {
+                float z[kGroup], q[kGroup];
+                load_group_any<LT, false>(row, nullptr, g0 + tid, ng, V, vec_ok, z, q);
+                unsigned long long pt2[kGroup / 2];
+                float w[kGroup], qp[kGroup], ws, qs;
+                group_masses<kModeBonus>(z, q, (g0 + tid) * kGroup, Xb, pt2, w, qp, ws, qs);
+                A += to_fixed(ws, Xb.fb);
+            }
+            long long Zp;
+            (void)block_incl_scan_ll(A, sw, Zp);
+            const long long t = mul_floor(u, Zp);
+            long long carry = 0;
+            int32_t last_pos = -1;
+            for (int32_t g0 = 0; g0 < ng && tok < 0; g0 += kFinalThreads)
+                tok = scan_round<LT, false, kModeBonus>(row, nullptr, g0, V, vec_ok, Xb, 0.0f, t, carry, last_pos,
+                                                        sw, si);
+            if (tok < 0)
+                tok = last_pos;
+        } else {
+            const long long t = mul_floor(u, Z);
+            // the chunk: the first thread whose running sum passes t, then
+            // its first record that does
+            const int f = block_first(incl > t, si);
+            const int lastc_all = block_max(lastc, si);
+            int32_t sel = -1;
+            long long rem = LLONG_MAX;
+            if (f < kFinalThreads) {
+                if (tid == f) {
+                    long long acc = incl - T;
+                    int c_sel = -1;
+                    for (int i = 0; i < R && c_sel < 0; ++i) {
+                        const int c = tid * R + i;
+                        if (c < CPS) {
+                            const long long vc = rec_value(__ldcg(&ra[c]), __ldcg(&rq[c]), delta);
+                            if (vc > 0 && acc + vc > t)
+                                c_sel = c;
+                            else
+                                acc += vc;
+                        }
+                    }
+                    si[0] = c_sel;
+                    s_before = acc;
+                }
+                __syncthreads();
+                sel = si[0];
+                rem = t - s_before;
+                __syncthreads();
+            }
+            if (sel < 0) { // rounding put the draw past the last chunk: take its last id
+                sel = lastc_all;
+                rem = LLONG_MAX;
+            }
+            if (sel >= 0) {
+                long long carry = 0;
+                int32_t last_pos = -1;
+                constexpr int MODE = LaunchMode<DENSE>::value;
+                tok = scan_round<LT, DENSE, MODE>(row, qrow, sel * kChunkGroups, V, vec_ok, X, delta, rem, carry,
+                                                  last_pos, sw, si);
+                if (tok < 0)
+                    tok = last_pos;
+            }
+        }
+        if (tid == 0) {
+            P.out_tokens[b * (K + 1) + jstar] = tok;
+            if (P.residual_mass) {
+                // Z / 2^fb over the residual's normaliser (S' or F / 2^fb)
+                const long long norm = DENSE ? E : F;
+                P.residual_mass[b] = (rejected && !degenerate && norm > 0)
+                                         ? __fdiv_rn(static_cast<float>(Z), static_cast<float>(norm))
+                                         : 0.0f;
+            }
+            if (degenerate && P.status)
+                atomicOr(P.status, kDegenerate);
+        }
+    }
+    // the sequence is done: return its scratch to zero
+    __syncthreads();
+    for (int32_t c = tid; c < CPS; c += kFinalThreads) {
+        ra[c] = 0;
+        rq[c] = 0.0f;
+    }
+    const int64_t r0 = b * (static_cast<int64_t>(K) + 1);
+    for (int64_t i = tid; i < (static_cast<int64_t>(K) + 1) * P.PM; i += kFinalThreads)
+        P.row_part[r0 * P.PM + i] = make_float2(0.0f, 0.0f);
+    for (int32_t j = tid; j <= K; j += kFinalThreads)
+        P.row_side[r0 + j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (tid == 0) {
+        P.seq_E[b] = 0;
+        P.seq_F[b] = 0;
+        P.seq_jstar[b] = 0;
+        P.seq_m[b] = 0.0f;
+        P.seq_s[b] = 0.0f;
+    }
+}
+
+template <typename LT, bool DENSE>
+__global__ void __launch_bounds__(kFinalThreads) final_kernel(const Params P)
+{
+    __shared__ long long sw[kFinalWarps];
+    __shared__ int si[kFinalWarps];
+    __shared__ long long s_before;
+    pdl_wait_primary();
+    for (int64_t b = blockIdx.x; b < P.B; b += gridDim.x)
+        final_sequence<LT, DENSE>(P, b, sw, si, s_before);
+}
+
+} // namespace sv

@@ -5,16 +5,10 @@
 // loads, the next step in flight while the current one is folded.  Each thread
 // keeps an online (max, normaliser) pair of softmax(z / T) in the base-2 form
 // sum_i exp2(z_i * c - fl(M * c)), c = log2(e) / T (one exp2 per element).
-// The CTA that finishes a row last merges the row's partials and runs the
-// accept test of the draft that row
-// verifies: a = min(1, p(x) / q(x)), accept iff u < a
-// ("推测解码：草稿、验证与实际加速", section 接受与拒绝怎样保住分布, equation for
-// a(x); the replay in section 算完三个 token 的全部概率 accepts when the draw
-// is strictly below the threshold).  The one that finishes a sequence's last
-// row finds the first rejection j* and writes the accepted prefix; later
-// drafts are void (same page, section 候选已知，验证才能并行).  Completion is
-// detected with arrival counters; each is returned to zero by the CTA that
-// saw it complete.
+// Each CTA publishes one (max, normaliser) pair per row it touches, and the
+// CTA holding a row's first id also publishes the row's draft data (x, z(x),
+// q(x), u); the draw stream turns these into the sequence's verdict once the
+// pass has completed (the kernel boundary is the only synchronisation).
 #pragma once
 
 #include <climits>
@@ -99,69 +93,11 @@ __device__ __forceinline__ void fold(const uint4 (&w)[U], float &M, unsigned lon
     }
 }
 
-// Per sequence: first rejection, accepted prefix, flags, and the surviving
-// row's statistics published for the final draw.  One warp.
-template <bool DENSE>
-__device__ void finish_sequence(const Params &P, int64_t b, int lane)
-{
-    const int32_t K = P.K;
-    __threadfence();
-    const int32_t bad = __ldcg(&P.seq_bad[b]);
-    int32_t jstar = K;
-    for (int32_t k0 = 0; k0 < K; k0 += 32) {
-        const int32_t k = k0 + lane;
-        const bool rej = (k < K) && ld_cg_u8(&P.acc[b * K + k]) == 0;
-        const unsigned m = __ballot_sync(0xFFFFFFFFu, rej);
-        if (m) {
-            jstar = k0 + __ffs(m) - 1;
-            break;
-        }
-    }
-    const int64_t rsel = b * (K + 1) + (jstar < K ? jstar : K);
-    const float m_sel = __ldcg(&P.row_m[rsel]);
-    const float s_sel = __ldcg(&P.row_s[rsel]);
-    __syncwarp();
-    for (int32_t j = lane; j <= K; j += 32) {
-        P.row_m[b * (K + 1) + j] = 0.0f;
-        P.row_s[b * (K + 1) + j] = 0.0f;
-    }
-    for (int32_t k = lane; k < K; k += 32)
-        P.acc[b * K + k] = 0;
-    int32_t *out = P.out_tokens + b * (K + 1);
-    if (bad) {
-        for (int32_t k = lane; k <= K; k += 32)
-            out[k] = -1;
-        for (int32_t k = lane; k < K; k += 32) {
-            if (P.accept_flags) P.accept_flags[b * K + k] = -1;
-            if (P.accept_prob) P.accept_prob[b * K + k] = 0.0f;
-        }
-    } else {
-        for (int32_t k = lane; k <= K; k += 32)
-            out[k] = k < jstar ? P.tokens[b * K + k] : -1;
-        if (P.accept_flags)
-            for (int32_t k = lane; k < K; k += 32)
-                P.accept_flags[b * K + k] = k < jstar ? 1 : (k == jstar ? 0 : -1);
-    }
-    if (lane == 0) {
-        if (bad) {
-            P.num_emitted[b] = 0;
-            if (P.residual_mass) P.residual_mass[b] = 0.0f;
-            if (P.status) atomicOr(P.status, bad);
-        } else {
-            P.num_emitted[b] = jstar + 1;
-        }
-        P.seq_jstar[b] = bad ? -1 : jstar;
-        P.seq_m[b] = m_sel;
-        P.seq_s[b] = s_sel;
-        P.seq_cnt[b] = 0u;
-        P.seq_bad[b] = 0;
-    }
-}
-
-// What the last warp of a row needs besides the item partials, fetched at
-// the start of every row item so that its latency hides behind the stream.
+// What a row's accept test needs besides its (max, normaliser): fetched by
+// the epilogue warp of the CTA holding the row's first id, while the row
+// streams, and published beside that CTA's partial.
 struct RowSide {
-    int32_t x;  // draft token verified by this row (j < K)
+    int32_t x;  // draft token verified by this row (j < K), else -1
     float zx;   // its logit
     float qx;   // its draft probability (1 for one-hot drafts)
     float u;    // the row's uniform
@@ -189,67 +125,6 @@ __device__ __forceinline__ RowSide fetch_side(const Params &P, int64_t r)
     return s;
 }
 
-// The last warp of row r merges the row's n_parts partials and tests the
-// draft.
-// `side` is valid in lane 0.
-template <typename LT, bool DENSE>
-__device__ __noinline__ void finish_row(const Params &P, int64_t r, int n_parts, int lane, const RowSide &side)
-{
-    __threadfence();
-    const float c = P.c;
-    const int32_t K = P.K, V = P.V;
-    float M = -INFINITY, S = 0.0f;
-    for (int32_t i = lane; i < n_parts; i += 32) {
-        const float2 pr = __ldcg(&P.row_part[r * P.PM + i]);
-        P.row_part[r * P.PM + i] = make_float2(0.0f, 0.0f);
-        merge_ms(M, S, pr.x, pr.y, c);
-    }
-    warp_merge_ms(M, S, c);
-
-    const int64_t b = divi(r, K + 1);
-    const int32_t j = static_cast<int32_t>(r - b * (K + 1));
-    int last_seq = 0;
-    if (lane == 0) {
-        int32_t bad = 0;
-        const bool row_ok = isfinite(M) && isfinite(S);
-        if (!row_ok)
-            bad |= kBadRow;
-        const float uj = side.u;
-        if (!(uj >= 0.0f && uj < 1.0f))
-            bad |= kBadU;
-        P.row_m[r] = M;
-        P.row_s[r] = S;
-        P.row_cnt[r] = 0u;
-        if (j < K) {
-            const int32_t x = side.x;
-            float a = 0.0f;
-            uint8_t acc = 0;
-            if (x < 0 || x >= V) {
-                bad |= kBadToken;
-            } else {
-                const float qx = side.qx;
-                if (DENSE && !(qx > 0.0f && isfinite(qx)))
-                    bad |= kBadQ;
-                else if (row_ok) {
-                    const float px = __fdiv_rn(term(side.zx, c, mc_of(M, c)), S);
-                    a = fminf(1.0f, __fdiv_rn(px, qx));
-                    acc = uj < a ? 1 : 0;
-                }
-            }
-            P.acc[b * K + j] = acc;
-            if (P.accept_prob)
-                P.accept_prob[b * K + j] = a;
-        }
-        if (bad)
-            atomicOr(&P.seq_bad[b], bad);
-        __threadfence();
-        last_seq = atomicAdd(&P.seq_cnt[b], 1u) == static_cast<unsigned>(K);
-    }
-    last_seq = __shfl_sync(0xFFFFFFFFu, last_seq, 0);
-    if (last_seq)
-        finish_sequence<DENSE>(P, b, lane);
-}
-
 // The flat view of the logits.  The B*(K+1) rows of V ids are one array of
 // R*V elements.  From the first 16-byte boundary on it is cut into whole
 // 16-byte vectors 1..nvec; "vector" 0 stands for the h elements before that
@@ -262,12 +137,6 @@ __device__ __noinline__ void finish_row(const Params &P, int64_t r, int n_parts,
 // the epilogue warp of the CTA that owns them, once for each row they touch.
 // Each row's partial (max, normaliser) pairs come from the CTAs its ids fall
 // in; CTA g writes its pair of row r into slot g - first_cta(r) of the row.
-template <typename LT>
-__device__ __forceinline__ int64_t vec_of_elem(const Params &P, int64_t e)
-{
-    constexpr int VW = 16 / sizeof(LT);
-    return (e - P.h + VW) / VW; // e - h + VW > 0 since h < VW
-}
 
 template <typename LT>
 __device__ __forceinline__ bool streamed(const Params &P, int64_t vv)
@@ -380,16 +249,26 @@ __global__ void __launch_bounds__(kRowCtaThreads, SV_ROW_MIN_CTAS) rows_kernel(c
     auto bar_free = [](int q) { return 1u + kRowSlots + static_cast<uint32_t>(q); };
 
     if (warp == kRowWarps) {
-        // ---- epilogue warp
+        // ---- epilogue warp: the CTA's pair of each row, and the draft data
+        // of the rows whose first id it holds (fetched ahead, in parallel)
+        RowSide pre = {-1, 0.0f, 1.0f, 0.0f};
+        if (lane < n_rows && vec_of_elem<LT>(P, (r0 + lane) * V) / P.span == g)
+            pre = fetch_side<LT, DENSE>(P, r0 + lane);
         for (int k = 0; k < n_rows; ++k) {
             const int64_t r = r0 + k;
-            RowSide side;
-            if (lane == 0)
-                side = fetch_side<LT, DENSE>(P, r); // in flight while the row streams
+            const int64_t first = vec_of_elem<LT>(P, r * V) / P.span;
+            const bool head = g == first; // this CTA holds the row's first id
+            RowSide side = {-1, 0.0f, 1.0f, 0.0f};
+            if (k < 32) {
+                side.x = __shfl_sync(0xFFFFFFFFu, pre.x, k);
+                side.zx = __shfl_sync(0xFFFFFFFFu, pre.zx, k);
+                side.qx = __shfl_sync(0xFFFFFFFFu, pre.qx, k);
+                side.u = __shfl_sync(0xFFFFFFFFu, pre.u, k);
+            } else if (lane == 0 && head) {
+                side = fetch_side<LT, DENSE>(P, r);
+            }
             float M = -INFINITY, S = 0.0f;
             ragged_pair<LT>(P, g, r, lane, M, S);
-            const int64_t first = vec_of_elem<LT>(P, r * V) / P.span;
-            const int n_parts = static_cast<int>(vec_of_elem<LT>(P, r * V + V - 1) / P.span - first + 1);
             const int q = k % kRowSlots;
             bar_sync(bar_full(q), kRowCtaThreads);
             if (lane < kRowWarps) {
@@ -399,15 +278,11 @@ __global__ void __launch_bounds__(kRowCtaThreads, SV_ROW_MIN_CTAS) rows_kernel(c
             if (k + kRowSlots < n_rows)
                 bar_arrive(bar_free(q), kRowCtaThreads);
             warp_common_max(M, S, c);
-            int last = 0;
             if (lane == 0) {
                 P.row_part[r * P.PM + (g - first)] = make_float2(M, S);
-                __threadfence();
-                last = atomicAdd(&P.row_cnt[r], 1u) == static_cast<unsigned>(n_parts - 1);
+                if (head)
+                    P.row_side[r] = make_float4(__int_as_float(side.x), side.zx, side.qx, side.u);
             }
-            last = __shfl_sync(0xFFFFFFFFu, last, 0);
-            if (last)
-                finish_row<LT, DENSE>(P, r, n_parts, lane, side);
         }
         pdl_launch_dependents();
         return;

@@ -40,7 +40,7 @@
 
 #include <climits>
 
-#include "sv_device.cuh"
+#include "sv_verdict.cuh"
 
 namespace sv {
 
@@ -212,102 +212,25 @@ __device__ __forceinline__ long long corr_of(float delta, float qp)
     return to_fixed(__fmul_rn(delta, qp), 0);
 }
 
-// Re-formed warp tile (this lane's group g, already loaded): look for the id
-// whose boundary (A - delta * Qp in 2^-fb units, measured from the chunk
-// start; `run` = the tiles before) first exceeds `rem`, i.e. the first id
-// whose running mass passes the draw.  Returns the id, or -1 with `run`
-// advanced by the tile; `last_pos` tracks the last id of positive mass seen.
-template <int MODE>
-__device__ __forceinline__ int32_t scan_group(const float (&z)[kGroup], const float (&q)[kGroup], int32_t g,
-                                              const SurvArgs &X, float delta, long long rem, long long &run,
-                                              int32_t &last_pos, int lane)
-{
-    unsigned long long pt2[kGroup / 2];
-    float w[kGroup], qp[kGroup], ws, qs;
-    group_masses<MODE>(z, q, g * kGroup, X, pt2, w, qp, ws, qs);
-    int kpos = -1;
-#pragma unroll
-    for (int k = 0; k < kGroup; ++k)
-        if (w[k] > 0.0f)
-            kpos = k;
-    const long long Lv = to_fixed(ws, X.fb) - corr_of(delta, qs);
-    const long long incl = warp_incl_scan_ll(Lv, lane) + run;
-    const unsigned pos = __ballot_sync(0xFFFFFFFFu, kpos >= 0);
-    if (pos) {
-        const int hl = 31 - __clz(pos);
-        const int kk = __shfl_sync(0xFFFFFFFFu, kpos, hl);
-        last_pos = (g - lane + hl) * kGroup + kk;
-    }
-    const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl > rem);
-    int32_t tok = -1;
-    if (hit) {
-        const int l = __ffs(hit) - 1;
-        if (lane == l) {
-            const long long excl = incl - Lv;
-            tok = g * kGroup + (kpos >= 0 ? kpos : 0);
-            // the id within the group: running sums in id order (the group's
-            // last boundary is its total, so an id past rounding falls back
-            // to the last id of positive mass)
-            float cw = 0.0f, cq = 0.0f;
-#pragma unroll
-            for (int k = 0; k < kGroup; ++k) {
-                cw = __fadd_rn(cw, w[k]);
-                cq = __fadd_rn(cq, qp[k]);
-                if (w[k] > 0.0f && excl + to_fixed(cw, X.fb) - corr_of(delta, cq) > rem) {
-                    tok = g * kGroup + k;
-                    break;
-                }
-            }
-        }
-        tok = __shfl_sync(0xFFFFFFFFu, tok, l);
-    }
-    run = __shfl_sync(0xFFFFFFFFu, incl, 31);
-    return tok;
-}
-
-// What the draw learns about a sequence once the rows are done.
-struct SeqView {
-    int32_t jstar; // -1: bad sequence
-    float m, s;
-    int32_t x;     // rejected one-hot draft, else -1
-};
-
-template <bool DENSE>
-__device__ __forceinline__ SeqView load_seq(const Params &P, int64_t b, int lane)
-{
-    SeqView sv = {-1, 0.0f, 1.0f, -1};
-    if (lane == 0) {
-        sv.jstar = __ldcg(&P.seq_jstar[b]);
-        sv.m = __ldcg(&P.seq_m[b]);
-        sv.s = __ldcg(&P.seq_s[b]);
-        if (!DENSE && sv.jstar >= 0 && sv.jstar < P.K)
-            sv.x = __ldg(&P.tokens[b * P.K + sv.jstar]);
-    }
-    sv.jstar = __shfl_sync(0xFFFFFFFFu, sv.jstar, 0);
-    sv.m = __shfl_sync(0xFFFFFFFFu, sv.m, 0);
-    sv.s = __shfl_sync(0xFFFFFFFFu, sv.s, 0);
-    sv.x = __shfl_sync(0xFFFFFFFFu, sv.x, 0);
-    return sv;
-}
 
 // The surviving row of sequence b (and its draft row, dense and rejected).
 template <typename LT, bool DENSE>
-__device__ __forceinline__ void seq_rows(const Params &P, int64_t b, const SeqView &sv, const LT *&row,
+__device__ __forceinline__ void seq_rows(const Params &P, int64_t b, const Verdict &v, const LT *&row,
                                          const float *&qrow)
 {
     const int64_t V = P.V;
-    row = static_cast<const LT *>(P.logits) + (b * (P.K + 1) + (sv.jstar < 0 ? 0 : sv.jstar)) * V;
-    qrow = (DENSE && sv.jstar >= 0 && sv.jstar < P.K) ? P.q + (b * P.K + sv.jstar) * V : nullptr;
+    row = static_cast<const LT *>(P.logits) + (b * (P.K + 1) + (v.jstar < 0 ? 0 : v.jstar)) * V;
+    qrow = (DENSE && v.jstar >= 0 && v.jstar < P.K) ? P.q + (b * P.K + v.jstar) * V : nullptr;
 }
 
-__device__ __forceinline__ SurvArgs surv_args(const Params &P, const SeqView &sv)
+__device__ __forceinline__ SurvArgs surv_args(const Params &P, const Verdict &v)
 {
     SurvArgs X;
     X.c = P.c;
-    X.mc = mc_of(sv.m, P.c);
-    X.inv_s = __frcp_rn(sv.s);
+    X.mc = mc_of(v.m, P.c);
+    X.inv_s = __frcp_rn(v.s);
     X.fb = P.fix_bits;
-    X.x = sv.x;
+    X.x = v.x;
     return X;
 }
 
@@ -347,375 +270,50 @@ __device__ __forceinline__ void fold_group(const float (&z)[kGroup], const float
     Qs = __fadd_rn(Qs, qs);
 }
 
-// Scan the 4 tiles of chunk `ch` of a row (one warp, direct loads) for the id
-// whose boundary first exceeds `rem` (measured from the chunk start).  Falls
-// back to the chunk's last id of positive mass if rounding leaves none.
-// Copy chunk ch of a row into ring stage `st` in the fold's layout (group gl
-// at gl * LB, its draft probabilities after the chunk's logits); lane l
-// copies groups 4l .. 4l+3.  Rows of whole aligned groups go by async copy;
-// others by plain loads (ids past the row as -inf, q as 0).  Returns when
-// the lane's own data has landed (each lane reads only what it copied).
-template <typename LT, bool DENSE>
-__device__ void stage_chunk(uint8_t *st, const LT *row, const float *qrow, int32_t ch, int32_t V, bool ring_ok,
-                            bool vec_ok, int lane)
-{
-    constexpr int LB = DrawShape<LT, DENSE>::LB;
-    constexpr int GL = kChunkGroups / 32;
-    const int32_t ng = (V + kGroup - 1) / kGroup;
-#pragma unroll 1
-    for (int i = 0; i < GL; ++i) {
-        const int gl = lane * GL + i;
-        const int32_t g = ch * kChunkGroups + gl;
-        uint8_t *zs = st + gl * LB;
-        uint8_t *qs = st + kChunkGroups * LB + gl * 32;
-        if (ring_ok) {
-            if (g < ng) {
-                const uint8_t *src = reinterpret_cast<const uint8_t *>(row + static_cast<int64_t>(g) * kGroup);
-                for (int h = 0; h < LB; h += 16)
-                    cp_async16(zs + h, src + h);
-                if (DENSE && qrow) {
-                    const uint8_t *qsrc = reinterpret_cast<const uint8_t *>(qrow + static_cast<int64_t>(g) * kGroup);
-                    cp_async16(qs, qsrc);
-                    cp_async16(qs + 16, qsrc + 16);
-                }
-            }
-        } else {
-            float z[kGroup], q[kGroup];
-            load_group_any<LT, DENSE>(row, qrow, g, ng, V, vec_ok, z, q);
-            for (int k = 0; k < kGroup; ++k) {
-                if constexpr (sizeof(LT) == 2)
-                    reinterpret_cast<uint16_t *>(zs)[k] = static_cast<uint16_t>(__float_as_uint(z[k]) >> 16);
-                else
-                    reinterpret_cast<float *>(zs)[k] = z[k];
-                if (DENSE)
-                    reinterpret_cast<float *>(qs)[k] = q[k];
-            }
-        }
-    }
-    cp_async_commit();
-    cp_async_wait<0>();
-}
-
-// Scan chunk ch (staged in `st`) for the id whose boundary (A - delta * Qp
-// in 2^-fb units, from the chunk start) first exceeds `rem`.  Lane l re-forms
-// groups 4l .. 4l+3 with the fold's per-group arithmetic (so the same group
-// totals); one warp scan over the lanes' sums finds the lane, a walk over its
-// groups the group, and running sums in id order the id.  Falls back to the
-// chunk's last id of positive mass if rounding leaves none.  Rolled loops:
-// this runs once per sequence, from a cold instruction cache.
-template <typename LT, bool DENSE>
-__device__ int32_t scan_chunk(const uint8_t *st, bool has_q, int32_t ch, int32_t V, const SurvArgs &X, float delta,
-                              long long rem, int lane)
-{
-    constexpr int MODE = LaunchMode<DENSE>::value;
-    constexpr int GL = kChunkGroups / 32;
-    const int32_t ng = (V + kGroup - 1) / kGroup;
-    const int32_t gbase = ch * kChunkGroups + lane * GL;
-    auto group = [&](int i, float (&w)[kGroup], float (&qp)[kGroup]) {
-        float z[kGroup], q[kGroup];
-        load_group_smem<LT, DENSE>(st, lane * GL + i, gbase + i < ng, z, q);
-        if (!has_q)
-            for (int k = 0; k < kGroup; ++k)
-                q[k] = 0.0f;
-        unsigned long long pt2[kGroup / 2];
-        float ws, qs;
-        group_masses<MODE>(z, q, (gbase + i) * kGroup, X, pt2, w, qp, ws, qs);
-        return to_fixed(ws, X.fb) - corr_of(delta, qs);
-    };
-    long long Ll = 0;
-    int lastg = -1, lastk = -1;
-#pragma unroll 1
-    for (int i = 0; i < GL; ++i) {
-        float w[kGroup], qp[kGroup];
-        Ll += group(i, w, qp);
-        for (int k = 0; k < kGroup; ++k)
-            if (w[k] > 0.0f) {
-                lastg = i;
-                lastk = k;
-            }
-    }
-    const long long incl = warp_incl_scan_ll(Ll, lane);
-    const unsigned pos = __ballot_sync(0xFFFFFFFFu, lastg >= 0);
-    int32_t last_pos = -1;
-    if (pos) {
-        const int hl = 31 - __clz(pos);
-        const int lg = __shfl_sync(0xFFFFFFFFu, lastg, hl), lk = __shfl_sync(0xFFFFFFFFu, lastk, hl);
-        last_pos = (ch * kChunkGroups + hl * GL + lg) * kGroup + lk;
-    }
-    const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl > rem);
-    if (!hit)
-        return last_pos;
-    const int l = __ffs(hit) - 1;
-    int32_t tok = -1;
-    if (lane == l) {
-        long long excl = incl - Ll;
-#pragma unroll 1
-        for (int i = 0; i < GL && tok < 0; ++i) {
-            float w[kGroup], qp[kGroup];
-            const long long Lg = group(i, w, qp);
-            if (excl + Lg > rem) {
-                // running sums in id order (the group's last boundary is its
-                // total, so an id past rounding falls back to its last id of
-                // positive mass)
-                float cw = 0.0f, cq = 0.0f;
-                int kpos = -1;
-                for (int k = 0; k < kGroup; ++k) {
-                    cw = __fadd_rn(cw, w[k]);
-                    cq = __fadd_rn(cq, qp[k]);
-                    if (w[k] > 0.0f) {
-                        kpos = k;
-                        if (excl + to_fixed(cw, X.fb) - corr_of(delta, cq) > rem) {
-                            tok = (gbase + i) * kGroup + k;
-                            break;
-                        }
-                    }
-                }
-                if (tok < 0)
-                    tok = (gbase + i) * kGroup + (kpos >= 0 ? kpos : 0);
-            }
-            excl += Lg;
-        }
-        if (tok < 0)
-            tok = last_pos;
-    }
-    return __shfl_sync(0xFFFFFFFFu, tok, l);
-}
-
-// A sequence's chunk records in batches of kRecBatch: lane l holds records
-// base + 8l .. base + 8l + 7 (raw A and Qp; 0 past the end).
-constexpr int kRecLane = 8;
-constexpr int kRecBatch = 32 * kRecLane;
-
-__device__ __forceinline__ void load_recs(const long long *ra, const float *rq, int32_t base, int32_t n, int lane,
-                                          long long (&a)[kRecLane], float (&q)[kRecLane])
-{
-#pragma unroll
-    for (int i = 0; i < kRecLane; ++i) {
-        const int32_t c = base + lane * kRecLane + i;
-        a[i] = c < n ? __ldcg(ra + c) : 0;
-        q[i] = c < n ? __ldcg(rq + c) : 0.0f;
-    }
-}
-
-// A record's boundary mass max(0, A - delta * Qp) in 2^-fb units.
-__device__ __forceinline__ long long rec_value(long long a, float q, float delta)
-{
-    const long long v = a - corr_of(delta, q);
-    return v > 0 ? v : 0;
-}
-
-// The accepted-draft draw from p of a row, for a rejection whose residual
-// came out with no mass (impossible in exact arithmetic): two passes over
-// the whole row with direct loads (total, then the scan).
-template <typename LT>
-__device__ int32_t draw_from_p(const LT *row, int32_t V, bool vec_ok, SurvArgs X, float u, int lane)
-{
-    X.x = -1;
-    const int32_t ng = (V + kGroup - 1) / kGroup;
-    float q[kGroup];
-#pragma unroll
-    for (int k = 0; k < kGroup; ++k)
-        q[k] = 0.0f;
-    long long A = 0;
-    for (int32_t g0 = 0; g0 < ng; g0 += 32) {
-        float z[kGroup], qq[kGroup];
-        load_group<LT, false>(row, nullptr, g0 + lane, ng, V, vec_ok, z, qq);
-        unsigned long long pt2[kGroup / 2];
-        float w[kGroup], qp[kGroup], ws, qs;
-        group_masses<kModeBonus>(z, q, (g0 + lane) * kGroup, X, pt2, w, qp, ws, qs);
-        A += to_fixed(ws, X.fb);
-    }
-    const long long t = mul_floor(u, warp_sum_ll(A));
-    long long run = 0;
-    int32_t last_pos = -1;
-    for (int32_t g0 = 0; g0 < ng; g0 += 32) {
-        float z[kGroup], qq[kGroup];
-        load_group<LT, false>(row, nullptr, g0 + lane, ng, V, vec_ok, z, qq);
-        const int32_t tok = scan_group<kModeBonus>(z, q, g0 + lane, X, 0.0f, t, run, last_pos, lane);
-        if (tok >= 0)
-            return tok;
-    }
-    return last_pos;
-}
-
-// Combine the chunk records of sequence b, draw the token, clear the
-// scratch.  One warp: the one that completed the sequence's last chunk; `st`
-// is a free stage of its ring.  Two rounds of loads in the common case
-// (V <= 262144): the sequence's scalars with its records, then the chosen
-// chunk.
-template <typename LT, bool DENSE>
-__device__ __noinline__ void final_draw(const Params &P, int64_t b, int lane, uint8_t *st)
-{
-    __threadfence();
-    const int32_t K = P.K, V = P.V, CPS = P.CPS;
-    long long *ra = P.rec_a + b * CPS;
-    float *rq = P.rec_q + b * CPS;
-    // ---- round 1: scalars and the first batch of records, all in flight
-    long long a0[kRecLane];
-    float q0[kRecLane];
-    load_recs(ra, rq, 0, CPS, lane, a0, q0);
-    const SeqView sv = load_seq<DENSE>(P, b, lane);
-    const long long Eraw = __ldcg(&P.seq_E[b]), Fraw = __ldcg(&P.seq_F[b]);
-    const float u = __ldg(&P.u[b * (K + 1) + K]);
-    if (sv.jstar >= 0) {
-        const LT *row;
-        const float *qrow;
-        seq_rows<LT, DENSE>(P, b, sv, row, qrow);
-        const SurvArgs X = surv_args(P, sv);
-        const bool rejected = sv.jstar < K;
-        const bool vec_ok = (reinterpret_cast<uintptr_t>(row) & 15u) == 0 &&
-                            (qrow == nullptr || (reinterpret_cast<uintptr_t>(qrow) & 15u) == 0);
-        // dense: delta = E - 2^fb = (S' - 1) 2^fb, S' the exact sum of pt;
-        // one-hot: F = sum of pt in 2^-fb units (the residual's normaliser)
-        const long long E = rejected && DENSE ? Eraw : 0, F = rejected && !DENSE ? Fraw : 0;
-        const float delta = rejected && DENSE ? static_cast<float>(E - (1ll << P.fix_bits)) : 0.0f;
-        const int nb = (CPS + kRecBatch - 1) / kRecBatch;
-        // ---- the total Z (the first batch's values kept for the search)
-        long long v0[kRecLane], Z = 0;
-        for (int bt = 0; bt < nb; ++bt) {
-            long long a[kRecLane];
-            float q[kRecLane];
-            if (bt > 0)
-                load_recs(ra, rq, bt * kRecBatch, CPS, lane, a, q);
-            long long s = 0;
-#pragma unroll
-            for (int i = 0; i < kRecLane; ++i) {
-                const long long v = bt == 0 ? rec_value(a0[i], q0[i], delta) : rec_value(a[i], q[i], delta);
-                if (bt == 0)
-                    v0[i] = v;
-                s += v;
-            }
-            Z += warp_sum_ll(s);
-        }
-        int32_t tok = -1;
-        const bool degenerate = rejected && !(Z > 0);
-        if (degenerate) {
-            tok = draw_from_p<LT>(row, V, vec_ok, X, u, lane);
-        } else {
-            // the first id whose running mass exceeds floor(u * Z): u * Z < P
-            // iff floor(u * Z) < P for an integer P
-            const long long t = mul_floor(u, Z);
-            long long run = 0, rem = 0;
-            int32_t sel = -1, lastc = -1;
-            for (int bt = 0; bt < nb && sel < 0; ++bt) {
-                long long v[kRecLane], L = 0;
-                if (bt == 0) {
-#pragma unroll
-                    for (int i = 0; i < kRecLane; ++i)
-                        v[i] = v0[i];
-                } else {
-                    long long a[kRecLane];
-                    float q[kRecLane];
-                    load_recs(ra, rq, bt * kRecBatch, CPS, lane, a, q);
-#pragma unroll
-                    for (int i = 0; i < kRecLane; ++i)
-                        v[i] = rec_value(a[i], q[i], delta);
-                }
-                int lp = -1;
-#pragma unroll
-                for (int i = 0; i < kRecLane; ++i) {
-                    L += v[i];
-                    if (v[i] > 0)
-                        lp = i;
-                }
-                const long long incl = warp_incl_scan_ll(L, lane) + run;
-                const unsigned pos = __ballot_sync(0xFFFFFFFFu, lp >= 0);
-                if (pos) {
-                    const int hl = 31 - __clz(pos);
-                    lastc = bt * kRecBatch + hl * kRecLane + __shfl_sync(0xFFFFFFFFu, lp, hl);
-                }
-                const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl > t);
-                if (hit) {
-                    const int l = __ffs(hit) - 1;
-                    int32_t c = -1;
-                    long long before = 0;
-                    if (lane == l) {
-                        long long acc = incl - L;
-                        for (int i = 0; i < kRecLane; ++i) {
-                            if (v[i] > 0 && acc + v[i] > t) {
-                                c = bt * kRecBatch + lane * kRecLane + i;
-                                before = acc;
-                                break;
-                            }
-                            acc += v[i];
-                        }
-                        if (c < 0) { // not reached with exact integer sums
-                            c = bt * kRecBatch + lane * kRecLane + (lp >= 0 ? lp : 0);
-                            before = t;
-                        }
-                    }
-                    sel = __shfl_sync(0xFFFFFFFFu, c, l);
-                    rem = t - __shfl_sync(0xFFFFFFFFu, before, l);
-                }
-                run = __shfl_sync(0xFFFFFFFFu, incl, 31);
-            }
-            if (sel < 0) { // rounding put the draw past the last chunk: take its last id
-                sel = lastc;
-                rem = LLONG_MAX;
-            }
-            if (sel >= 0) {
-                stage_chunk<LT, DENSE>(st, row, qrow, sel, V, P.ring_ok != 0, vec_ok, lane);
-                tok = scan_chunk<LT, DENSE>(st, qrow != nullptr, sel, V, X, delta, rem, lane);
-            }
-        }
-        if (lane == 0) {
-            P.out_tokens[b * (K + 1) + sv.jstar] = tok;
-            if (P.residual_mass) {
-                // Z / 2^fb over the residual's normaliser (S' or F / 2^fb)
-                const long long norm = DENSE ? E : F;
-                P.residual_mass[b] = (rejected && !degenerate && norm > 0)
-                                         ? __fdiv_rn(static_cast<float>(Z), static_cast<float>(norm))
-                                         : 0.0f;
-            }
-            if (degenerate && P.status)
-                atomicOr(P.status, kDegenerate);
-        }
-    }
-    // every chunk of the sequence is done: return its scratch to zero
-    for (int32_t i = lane; i < CPS; i += 32) {
-        ra[i] = 0;
-        rq[i] = 0.0f;
-    }
-    if (lane == 0) {
-        P.surv_cnt[b] = 0u;
-        P.seq_E[b] = 0;
-        P.seq_F[b] = 0;
-        P.seq_jstar[b] = 0;
-        P.seq_m[b] = 0.0f;
-        P.seq_s[b] = 0.0f;
-    }
-}
+// What a ring stage's consumer needs about the chunk's sequence: written by
+// the issue side (which computed the verdict) when it issues the chunk.
+struct StageInfo {
+    int32_t jstar; // -1: bad sequence (nothing to fold)
+    float m, s;
+    int32_t x;
+};
 
 // The chunks [c0, c1) of one warp.  RING: rows of whole, 16-byte aligned
 // groups stream through the warp's ring, kDrawStages - 1 chunks ahead, a
 // lane copying (and later reading) its own 4 groups of each chunk; otherwise
-// each lane loads its groups directly.
+// each lane loads its groups directly.  The issue side meets each sequence
+// first and computes its verdict (the warp that issues a sequence's chunk 0
+// also writes the sequence's outputs); the consumer folds the chunks,
+// writes one record per chunk and, per sequence, adds its share of the
+// normaliser.
 template <typename LT, bool DENSE, bool RING>
-__device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t c1, int lane, uint8_t *ring)
+__device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t c1, int lane, uint8_t *ring,
+                                           StageInfo *info)
 {
     using Shape = DrawShape<LT, DENSE>;
     constexpr int LB = Shape::LB;
-    const int32_t V = P.V, CPS = P.CPS;
+    const int32_t V = P.V, K = P.K, CPS = P.CPS;
     const int32_t ng = (V + kGroup - 1) / kGroup;
     const int64_t nchunks = c1 - c0;
 
-    // ---- issue side (RING): the chunk kDrawStages - 1 ahead of the consumer
+    // ---- issue side: the chunk kDrawStages - 1 ahead of the consumer
     int64_t ib = c0 / CPS;
     int32_t icis = static_cast<int32_t>(c0 - ib * CPS);
     int ist = 0;       // ring stage of the next issued chunk
-    int64_t iseq = -1; // sequence whose rows irow / iq point into
+    int64_t iseq = -1; // sequence whose verdict iv holds
+    Verdict iv = {-1, 0.0f, 1.0f, -1};
     const LT *irow = nullptr;
     const float *iq = nullptr;
-    bool ivalid = false;
     auto issue = [&](int64_t k) {
-        if (RING && k < nchunks) {
+        if (k < nchunks) {
             if (ib != iseq) {
-                const SeqView sv = load_seq<DENSE>(P, ib, lane);
-                seq_rows<LT, DENSE>(P, ib, sv, irow, iq);
-                ivalid = sv.jstar >= 0;
+                iv = seq_verdict<LT, DENSE>(P, ib, lane, icis == 0);
+                seq_rows<LT, DENSE>(P, ib, iv, irow, iq);
                 iseq = ib;
             }
-            if (ivalid) {
+            if (lane == 0)
+                info[ist] = StageInfo{iv.jstar, iv.m, iv.s, iv.x};
+            if (RING && iv.jstar >= 0) {
                 uint8_t *st = ring + ist * Shape::kChunkBytes;
                 const int32_t g0 = icis * kChunkGroups + lane;
                 const uint8_t *src = reinterpret_cast<const uint8_t *>(irow + static_cast<int64_t>(g0) * kGroup);
@@ -756,10 +354,9 @@ __device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t 
     const float *cq = nullptr;
     const unsigned long long E0 = DENSE ? pack2(2.0f, 2.0f) : 0ull;
     unsigned long long Ehi = E0, Elo = 0ull; // see fold_group
-    int32_t nch = 0; // chunks of `cur` done
-    auto flush = [&](uint8_t *free_stage) {
-        // the sequence's normaliser share and its chunk count; the warp that
-        // completes the sequence draws its token
+    auto flush = [&]() {
+        // the sequence's share of its normaliser: E = sum pt (dense) or
+        // F = sum pt (one-hot), in 2^-fb units; read by the final kernel
         float h0, h1, l0, l1;
         unpack2(Ehi, h0, h1);
         unpack2(Elo, l0, l1);
@@ -767,24 +364,11 @@ __device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t 
         if (DENSE)
             e += to_fixed(l0, X.fb) + to_fixed(l1, X.fb) - 2 * to_fixed(2.0f, X.fb);
         const long long E = warp_sum_ll(e);
-        int last = 0;
-        if (lane == 0) {
-            if (cvalid && cdraft) {
-                if (DENSE)
-                    atomicAdd(reinterpret_cast<unsigned long long *>(&P.seq_E[cur]), static_cast<unsigned long long>(E));
-                else
-                    atomicAdd(reinterpret_cast<unsigned long long *>(&P.seq_F[cur]), static_cast<unsigned long long>(E));
-            }
-            __threadfence();
-            last = atomicAdd(&P.surv_cnt[cur], static_cast<unsigned>(nch)) + static_cast<unsigned>(nch) ==
-                   static_cast<unsigned>(CPS);
-        }
-        last = __shfl_sync(0xFFFFFFFFu, last, 0);
-        if (last)
-            final_draw<LT, DENSE>(P, cur, lane, free_stage);
+        if (lane == 0 && cvalid && cdraft)
+            atomicAdd(reinterpret_cast<unsigned long long *>(DENSE ? &P.seq_E[cur] : &P.seq_F[cur]),
+                      static_cast<unsigned long long>(E));
         Ehi = E0;
         Elo = 0ull;
-        nch = 0;
     };
 
 #pragma unroll 1
@@ -792,19 +376,19 @@ __device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t 
         issue(s);
 #pragma unroll 1
     for (int64_t k = 0; k < nchunks; ++k) {
-        // a new sequence: close the last one while the stage about to take
-        // chunk k + kDrawStages - 1 (chunk k - 1's) is still free
-        if (cb != cur && cur >= 0)
-            flush(ring + (cst + kDrawStages - 1) % kDrawStages * Shape::kChunkBytes);
         issue(k + kDrawStages - 1);
         if (RING)
             cp_async_wait<kDrawStages - 1>();
         if (cb != cur) {
-            const SeqView sv = load_seq<DENSE>(P, cb, lane);
-            seq_rows<LT, DENSE>(P, cb, sv, crow, cq);
-            X = surv_args(P, sv);
-            cvalid = sv.jstar >= 0;
-            cdraft = sv.jstar >= 0 && sv.jstar < P.K;
+            if (cur >= 0)
+                flush();
+            __syncwarp();
+            const StageInfo si = info[cst];
+            const Verdict v = {si.jstar, si.m, si.s, si.x};
+            seq_rows<LT, DENSE>(P, cb, v, crow, cq);
+            X = surv_args(P, v);
+            cvalid = v.jstar >= 0;
+            cdraft = v.jstar >= 0 && v.jstar < K;
             cvec = (reinterpret_cast<uintptr_t>(crow) & 15u) == 0 &&
                    (cq == nullptr || (reinterpret_cast<uintptr_t>(cq) & 15u) == 0);
             cur = cb;
@@ -836,37 +420,38 @@ __device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t 
             P.rec_a[cb * CPS + ccis] = at;
             P.rec_q[cb * CPS + ccis] = qt;
         }
-        ++nch;
         cst = cst + 1 == kDrawStages ? 0 : cst + 1;
         if (++ccis == CPS) {
             ccis = 0;
             ++cb;
         }
     }
-    cp_async_wait<0>();
-    flush(ring);
+    if (RING)
+        cp_async_wait<0>();
+    flush();
 }
 
-// The final draws.  Each warp takes a contiguous range of the call's chunks;
-// the warp that completes a sequence's last chunk draws its token.  Launched
-// behind the row pass with programmatic dependent launch: it waits in
-// griddepcontrol.wait until the row pass has completed.
+// The draw stream.  Each warp takes a contiguous range of the call's chunks.
+// Launched behind the row pass with programmatic dependent launch: it waits
+// in griddepcontrol.wait until the row pass has completed.
 template <typename LT, bool DENSE>
 __global__ void __launch_bounds__(kDrawWarps * 32, SV_MIN_CTAS) survivor_kernel(const Params P)
 {
     extern __shared__ __align__(128) uint8_t smem[]; // DrawShape::kWarpBytes per warp
+    __shared__ StageInfo info[kDrawWarps][kDrawStages];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint8_t *ring = smem + warp * DrawShape<LT, DENSE>::kWarpBytes;
     pdl_wait_primary();
     const int64_t W = static_cast<int64_t>(blockIdx.x) * kDrawWarps + warp;
     const int64_t NW = static_cast<int64_t>(gridDim.x) * kDrawWarps;
     const int64_t c0 = W * P.NC / NW, c1 = (W + 1) * P.NC / NW;
-    if (c0 >= c1)
-        return;
-    if (P.ring_ok)
-        draw_range<LT, DENSE, true>(P, c0, c1, lane, ring);
-    else
-        draw_range<LT, DENSE, false>(P, c0, c1, lane, ring);
+    if (c0 < c1) {
+        if (P.ring_ok)
+            draw_range<LT, DENSE, true>(P, c0, c1, lane, ring, info[warp]);
+        else
+            draw_range<LT, DENSE, false>(P, c0, c1, lane, ring, info[warp]);
+    }
+    pdl_launch_dependents();
 }
 
 } // namespace sv
