@@ -1,9 +1,9 @@
 #!/usr/bin/env python3
 """Benchmark of the speculative-sampling verification step on GB300.
 
-One step = one spec_verify call over a whole batch: two launches, the row
-pass (rows_kernel) and the final draws (survivor_kernel), with inputs
-resident in HBM.  Prints ONE JSON line on rank 0.
+One step = one spec_verify call over a whole batch: three launches, the row
+pass (rows_kernel), the draw stream (survivor_kernel) and the final draws
+(final_kernel), with inputs resident in HBM.  Prints ONE JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle, timed on the host
@@ -51,8 +51,9 @@ def algorithmic_bytes(w, num_emitted: np.ndarray) -> dict:
 
     rows_kernel: every logit once, the q(x) gathers (one 32-byte sector each,
     dense drafts), the logit gathers z(x) (one sector each), the tokens and
-    uniforms, and its outputs.  survivor_kernel: the surviving logit row once
-    more and, after a rejection with dense q, that q row, plus its outputs."""
+    uniforms.  draw kernels (survivor_kernel + final_kernel): the surviving
+    logit row once more and, after a rejection with dense q, that q row, plus
+    the outputs."""
     B = len(num_emitted)
     K, V = w.K, w.V
     es = 2 if w.dtype == "bf16" else 4
@@ -61,7 +62,7 @@ def algorithmic_bytes(w, num_emitted: np.ndarray) -> dict:
     rows += B * (K + 1) * 4 * 2 + B * 4                          # u, out_tokens, num_emitted
     rejected = int(np.sum(num_emitted <= K))
     surv = B * V * es + (0 if w.onehot else rejected * V * 4) + B * (4 + 4 + 4)
-    return {"rows_kernel": rows, "survivor_kernel": surv, "total": rows + surv, "rejected": rejected}
+    return {"rows_kernel": rows, "draw_kernels": surv, "total": rows + surv, "rejected": rejected}
 
 
 def kernel_source_hash() -> str:
@@ -198,17 +199,18 @@ def run_gpu(args):
 
     cargs = args_for(d_logits, d_q, d_tok, d_u, out)
 
-    def step():
-        # one call = the two launches of the path (row pass, final draws),
-        # the second chained to the first by programmatic dependent launch
-        rc = lib.spec_verify(*cargs)
+    def step(s):
+        # one call = the three launches of the path (row pass, draw stream,
+        # final draws), each chained to the one before by programmatic
+        # dependent launch
+        rc = lib.spec_verify(*cargs[:-1], s.cuda_stream)
         if rc:
             raise RuntimeError(sv.sv_status_string(rc))
 
     def staged_step(evs):
-        # the same two launches through the per-stage entry points, with
-        # events between them (this breaks the launch chaining, so it is
-        # used for per-kernel durations only)
+        # the same launches through the per-stage entry points, with events
+        # between the row pass and the draws (this breaks the launch chaining
+        # there, so it is used for per-kernel durations only)
         evs[0].record(stream)
         rc = lib.sv_verify_rows(*cargs)
         evs[1].record(stream)
@@ -224,22 +226,42 @@ def run_gpu(args):
 
     # warm-up
     for _ in range(max(args.warmup, 3)):
-        step()
+        step(stream)
     barrier()
 
-    # ---- timed region: K steps of the public call
+    # the public call captured once in a CUDA graph: the timed region
+    # replays it, so host launch overhead stays out of the device timing
+    gstream = torch.cuda.Stream(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gstream):
+        step(gstream)
+    graph.replay()
+    barrier()
+
+    # ---- timed region: K steps of the public call (graph replays)
     clocks = ClockSampler(local)
     clocks.start()
     barrier()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for _ in range(args.steps):
-        step()
-    t_end.record(stream)
+    with torch.cuda.stream(gstream):
+        t_start.record(gstream)
+        for _ in range(args.steps):
+            graph.replay()
+        t_end.record(gstream)
     barrier()
     ms_total = t_start.elapsed_time(t_end)
     ms_step = ms_total / args.steps
+
+    # the same K steps as eager calls from the host (for reference)
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for _ in range(args.steps):
+        step(stream)
+    e_end.record(stream)
+    barrier()
+    ms_step_eager = e_start.elapsed_time(e_end) / args.steps
 
     # ---- per-kernel durations: the same launches, events between them
     n_k = max(20, min(args.steps, 500))
@@ -261,7 +283,7 @@ def run_gpu(args):
     nbytes = algorithmic_bytes(w, num_emitted)
     peak, peak_kind = peaks()
     rows_gbs = nbytes["rows_kernel"] / (rows_ms * 1e-3) / 1e9
-    surv_gbs = nbytes["survivor_kernel"] / (surv_ms * 1e-3) / 1e9
+    surv_gbs = nbytes["draw_kernels"] / (surv_ms * 1e-3) / 1e9
     step_gbs = nbytes["total"] / (ms_step * 1e-3) / 1e9
 
     # ---- end to end through the public call with pinned host buffers
@@ -334,9 +356,12 @@ def run_gpu(args):
             "tokens_per_s": tokens_per_step * world / (ms_step * 1e-3),
             "hbm_gbs_step": step_gbs,
             "hbm_frac_step": {"of_measured": step_gbs / peak, "of_8tbs_nominal": step_gbs / NOMINAL_HBM_GBS},
-            "kernels_ms": {"rows_kernel": rows_ms, "survivor_kernel": surv_ms,
-                           "source": f"{n_k} staged calls with CUDA events between the two launches"},
-            "kernels_gbs": {"rows_kernel": rows_gbs, "survivor_kernel": surv_gbs},
+            "ms_per_step_eager": ms_step_eager,
+            "timing": "CUDA-graph replay of the public C-ABI call (one call per replay); "
+                      "ms_per_step_eager: the same calls issued from the host",
+            "kernels_ms": {"rows_kernel": rows_ms, "survivor_kernel+final_kernel": surv_ms,
+                           "source": f"{n_k} staged calls with CUDA events between the row pass and the draws"},
+            "kernels_gbs": {"rows_kernel": rows_gbs, "survivor_kernel+final_kernel": surv_gbs},
             "algorithmic_bytes": nbytes,
             "roofline": {"bound": "hbm", "kernel": "rows_kernel",
                          "achieved": rows_gbs, "peak": peak, "unit": "GB/s",
@@ -345,7 +370,7 @@ def run_gpu(args):
             "e2e": {"value": seqs / (e2e_ms * 1e-3), "unit": "seqs/s",
                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": 3 * args.steps,
             "clocks": clk,
             "status_bits": st,
             "cpu_baseline": cpu,
