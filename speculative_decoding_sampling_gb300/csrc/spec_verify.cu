@@ -34,8 +34,7 @@ struct Plan {
     int32_t PM;   // row_part slots per row
     int32_t CPS;  // final-draw chunks per sequence
     int32_t fix;  // fractional bits of the fixed-point masses
-    size_t off_part, off_row_side, off_jstar, off_seq_m,
-        off_seq_s, off_seqE, off_seqF, off_rec_a, off_rec_q, bytes;
+    size_t off_part, off_row_side, off_seq_info, off_seqE, off_seqF, off_rec_a, off_rec_q, bytes;
 };
 
 bool make_plan(int64_t B, int32_t K, int32_t V, Plan &p)
@@ -57,9 +56,7 @@ bool make_plan(int64_t B, int32_t K, int32_t V, Plan &p)
     size_t off = 0;
     p.off_part = off;     off = align_up(off + R * p.PM * sizeof(float2));
     p.off_row_side = off; off = align_up(off + R * sizeof(float4));
-    p.off_jstar = off;    off = align_up(off + Bz * sizeof(int32_t));
-    p.off_seq_m = off;    off = align_up(off + Bz * sizeof(float));
-    p.off_seq_s = off;    off = align_up(off + Bz * sizeof(float));
+    p.off_seq_info = off; off = align_up(off + Bz * sizeof(int4));
     p.off_seqE = off;     off = align_up(off + Bz * sizeof(long long));
     p.off_seqF = off;     off = align_up(off + Bz * sizeof(long long));
     p.off_rec_a = off;    off = align_up(off + Bz * p.CPS * sizeof(long long));
@@ -178,6 +175,7 @@ cudaError_t launch(sv::Params P, const Plan &plan, int stages, cudaStream_t stre
         cudaLaunchConfig_t fcfg = {};
         fcfg.gridDim = dim3(static_cast<unsigned>(P.B < 0x7FFFFFFF ? P.B : 0x7FFFFFFF));
         fcfg.blockDim = dim3(sv::kFinalThreads);
+        fcfg.dynamicSmemBytes = static_cast<size_t>(plan.CPS) * (sizeof(long long) + sizeof(float));
         fcfg.stream = stream;
         fcfg.attrs = attr;
         fcfg.numAttrs = 1;
@@ -239,9 +237,7 @@ sv_status_t run(int stages, const void *logits, sv_dtype_t dtype, const float *q
     P.status = status_dev;
     P.row_part = reinterpret_cast<float2 *>(ws + plan.off_part);
     P.row_side = reinterpret_cast<float4 *>(ws + plan.off_row_side);
-    P.seq_jstar = reinterpret_cast<int32_t *>(ws + plan.off_jstar);
-    P.seq_m = reinterpret_cast<float *>(ws + plan.off_seq_m);
-    P.seq_s = reinterpret_cast<float *>(ws + plan.off_seq_s);
+    P.seq_info = reinterpret_cast<int4 *>(ws + plan.off_seq_info);
     P.seq_E = reinterpret_cast<long long *>(ws + plan.off_seqE);
     P.seq_F = reinterpret_cast<long long *>(ws + plan.off_seqF);
     P.rec_a = reinterpret_cast<long long *>(ws + plan.off_rec_a);

@@ -63,9 +63,8 @@ struct Params {
     // a completed call leaves the whole workspace zero-filled
     float2 *row_part;     // [R * PM]  (max of z, normaliser relative to it) per CTA a row falls in
     float4 *row_side;     // [R]       the row's draft token (int bits), z(x), q(x), u
-    int32_t *seq_jstar;   // [B]       row the final token is drawn from, -1 = bad (written by the draw stream)
-    float *seq_m;         // [B]       max of z of that row
-    float *seq_s;         // [B]       fp32 normaliser of that row
+    int4 *seq_info;       // [B]       the verdict for the final kernel: j* (-1 = bad sequence), bits of the
+                          //           surviving row's max m and normaliser s, the rejected draft x (one-hot) or -1
     long long *seq_E;     // [B]       exact sum of pt over the surviving row (dense), 2^-fix_bits units
     long long *seq_F;     // [B]       sum of pt (one-hot normaliser), 2^-fix_bits units
     long long *rec_a;     // [B * CPS] per chunk: mass A, 2^-fix_bits units

@@ -82,6 +82,52 @@ __device__ __forceinline__ int block_max(int v, int *si)
     return r;
 }
 
+// Block-wide inclusive scan of one int64 per thread (thread order) fused
+// with the search for the first thread whose prefix exceeds a threshold and
+// the maximum of `mx` over the block: two barriers.  The threshold is `thr`,
+// or floor(u * total) when `u` is not negative.  Each call site passes its
+// own scratch, so no barrier is needed after the call.
+struct ScanFirst {
+    long long incl, tot, thr;
+    int first, mx;
+};
+
+__device__ __forceinline__ ScanFirst block_scan_first(long long v, long long thr, float u, int mx, long long *s_tot,
+                                                      int *s_mx, int *s_first)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    ScanFirst r;
+    r.incl = warp_incl_scan_ll(v, lane);
+    const int wmx = __reduce_max_sync(0xFFFFFFFFu, mx);
+    if (lane == 31)
+        s_tot[warp] = r.incl;
+    if (lane == 0)
+        s_mx[warp] = wmx;
+    __syncthreads();
+    long long off = 0;
+    r.tot = 0;
+    r.mx = INT_MIN;
+#pragma unroll
+    for (int w = 0; w < kFinalWarps; ++w) {
+        const long long x = s_tot[w];
+        if (w < warp)
+            off += x;
+        r.tot += x;
+        r.mx = max(r.mx, s_mx[w]);
+    }
+    r.incl += off;
+    r.thr = u >= 0.0f ? mul_floor(u, r.tot) : thr;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, r.incl > r.thr);
+    if (lane == 0)
+        s_first[warp] = m ? warp * 32 + __ffs(m) - 1 : kFinalThreads;
+    __syncthreads();
+    r.first = kFinalThreads;
+#pragma unroll
+    for (int w = 0; w < kFinalWarps; ++w)
+        r.first = min(r.first, s_first[w]);
+    return r;
+}
+
 // One round of the id scan: groups g0 .. g0 + 127 of a row, one per thread.
 // Looks for the first id whose boundary (carry + running group values, then
 // running sums in id order within the group) exceeds `rem`; returns it, or
@@ -138,22 +184,49 @@ __device__ int32_t scan_round(const LT *row, const float *qrow, int32_t g0, int3
     return tok;
 }
 
+// Scratch of the final kernel's block-wide steps.
+struct FinalSmem {
+    long long sw[kFinalWarps];
+    int si[kFinalWarps];
+    long long tot[2][kFinalWarps];
+    int mx[2][kFinalWarps];
+    int first[2][kFinalWarps];
+    long long before;
+    int sel;
+};
+
 // The final draw of sequence b and the return of its scratch to zero.
+// Two rounds of loads: the sequence's verdict, normaliser, uniform and
+// chunk records together; then the chosen chunk (one group per thread).
 template <typename LT, bool DENSE>
-__device__ void final_sequence(const Params &P, int64_t b, long long *sw, int *si, long long &s_before)
+__device__ void final_sequence(const Params &P, int64_t b, FinalSmem &sm, long long *s_v)
 {
     const int tid = threadIdx.x;
     const int32_t K = P.K, V = P.V, CPS = P.CPS;
     long long *ra = P.rec_a + b * CPS;
     float *rq = P.rec_q + b * CPS;
-    const int32_t jstar = __ldcg(&P.seq_jstar[b]);
+    // ---- round 1, all in flight together
+    const int4 info = __ldcg(&P.seq_info[b]);
+    const long long Eraw = __ldcg(&P.seq_E[b]), Fraw = __ldcg(&P.seq_F[b]);
+    const float u = __ldg(&P.u[b * (K + 1) + K]);
+    const int R = (CPS + kFinalThreads - 1) / kFinalThreads; // thread t holds chunks [t*R, (t+1)*R)
+    for (int i = 0; i < R; ++i) {
+        const int c = tid * R + i;
+        if (c < CPS) {
+            const long long a = __ldcg(&ra[c]);
+            const float q = __ldcg(&rq[c]);
+            s_v[c] = a; // raw; turned into boundary masses below
+            reinterpret_cast<float *>(s_v + CPS)[c] = q;
+        }
+    }
+    const int32_t jstar = info.x;
     if (jstar >= 0) {
         const bool rejected = jstar < K;
         Verdict v;
         v.jstar = jstar;
-        v.m = __ldcg(&P.seq_m[b]);
-        v.s = __ldcg(&P.seq_s[b]);
-        v.x = (!DENSE && rejected) ? __ldg(&P.tokens[b * K + jstar]) : -1;
+        v.m = __int_as_float(info.y);
+        v.s = __int_as_float(info.z);
+        v.x = info.w;
         const LT *row;
         const float *qrow;
         seq_rows<LT, DENSE>(P, b, v, row, qrow);
@@ -162,25 +235,25 @@ __device__ void final_sequence(const Params &P, int64_t b, long long *sw, int *s
                             (qrow == nullptr || (reinterpret_cast<uintptr_t>(qrow) & 15u) == 0);
         // dense: delta = E - 2^fb = (S' - 1) 2^fb, S' the exact sum of pt;
         // one-hot: F = sum of pt in 2^-fb units (the residual's normaliser)
-        const long long E = rejected && DENSE ? __ldcg(&P.seq_E[b]) : 0;
-        const long long F = rejected && !DENSE ? __ldcg(&P.seq_F[b]) : 0;
+        const long long E = rejected && DENSE ? Eraw : 0;
+        const long long F = rejected && !DENSE ? Fraw : 0;
         const float delta = rejected && DENSE ? static_cast<float>(E - (1ll << P.fix_bits)) : 0.0f;
-        const float u = __ldg(&P.u[b * (K + 1) + K]);
-        // ---- records: thread t holds chunks [t*R, (t+1)*R)
-        const int R = (CPS + kFinalThreads - 1) / kFinalThreads;
+        // ---- the chunk: block scan over the threads' record sums, the
+        // first thread whose running sum passes floor(u * Z)
         long long T = 0;
         int lastc = -1;
         for (int i = 0; i < R; ++i) {
             const int c = tid * R + i;
             if (c < CPS) {
-                const long long vc = rec_value(__ldcg(&ra[c]), __ldcg(&rq[c]), delta);
+                const long long vc = rec_value(s_v[c], reinterpret_cast<const float *>(s_v + CPS)[c], delta);
+                s_v[c] = vc;
                 T += vc;
                 if (vc > 0)
                     lastc = c;
             }
         }
-        long long Z;
-        const long long incl = block_incl_scan_ll(T, sw, Z);
+        const ScanFirst sr = block_scan_first(T, 0, u, lastc, sm.tot[0], sm.mx[0], sm.first[0]);
+        const long long Z = sr.tot;
         int32_t tok = -1;
         const bool degenerate = rejected && !(Z > 0);
         if (degenerate) {
@@ -199,61 +272,83 @@ __device__ void final_sequence(const Params &P, int64_t b, long long *sw, int *s
                 A += to_fixed(ws, Xb.fb);
             }
             long long Zp;
-            (void)block_incl_scan_ll(A, sw, Zp);
+            (void)block_incl_scan_ll(A, sm.sw, Zp);
             const long long t = mul_floor(u, Zp);
             long long carry = 0;
             int32_t last_pos = -1;
             for (int32_t g0 = 0; g0 < ng && tok < 0; g0 += kFinalThreads)
                 tok = scan_round<LT, false, kModeBonus>(row, nullptr, g0, V, vec_ok, Xb, 0.0f, t, carry, last_pos,
-                                                        sw, si);
+                                                        sm.sw, sm.si);
             if (tok < 0)
                 tok = last_pos;
         } else {
-            const long long t = mul_floor(u, Z);
-            // the chunk: the first thread whose running sum passes t, then
-            // its first record that does
-            const int f = block_first(incl > t, si);
-            const int lastc_all = block_max(lastc, si);
-            int32_t sel = -1;
-            long long rem = LLONG_MAX;
-            if (f < kFinalThreads) {
-                if (tid == f) {
-                    long long acc = incl - T;
-                    int c_sel = -1;
-                    for (int i = 0; i < R && c_sel < 0; ++i) {
-                        const int c = tid * R + i;
-                        if (c < CPS) {
-                            const long long vc = rec_value(__ldcg(&ra[c]), __ldcg(&rq[c]), delta);
-                            if (vc > 0 && acc + vc > t)
-                                c_sel = c;
-                            else
-                                acc += vc;
-                        }
+            const long long t = sr.thr;
+            if (tid == sr.first) {
+                long long acc = sr.incl - T;
+                int c_sel = -1;
+                for (int i = 0; i < R && c_sel < 0; ++i) {
+                    const int c = tid * R + i;
+                    if (c < CPS) {
+                        const long long vc = s_v[c];
+                        if (vc > 0 && acc + vc > t)
+                            c_sel = c;
+                        else
+                            acc += vc;
                     }
-                    si[0] = c_sel;
-                    s_before = acc;
                 }
-                __syncthreads();
-                sel = si[0];
-                rem = t - s_before;
-                __syncthreads();
+                sm.sel = c_sel;
+                sm.before = acc;
             }
+            __syncthreads();
+            int32_t sel = sr.first < kFinalThreads ? sm.sel : -1;
+            long long rem = t - sm.before;
             if (sel < 0) { // rounding put the draw past the last chunk: take its last id
-                sel = lastc_all;
+                sel = sr.mx;
                 rem = LLONG_MAX;
             }
             if (sel >= 0) {
-                long long carry = 0;
-                int32_t last_pos = -1;
+                // ---- round 2: the chunk's 128 groups, one per thread
                 constexpr int MODE = LaunchMode<DENSE>::value;
-                tok = scan_round<LT, DENSE, MODE>(row, qrow, sel * kChunkGroups, V, vec_ok, X, delta, rem, carry,
-                                                  last_pos, sw, si);
-                if (tok < 0)
-                    tok = last_pos;
+                const int32_t ng = (V + kGroup - 1) / kGroup;
+                const int32_t g = sel * kChunkGroups + tid;
+                float z[kGroup], q[kGroup];
+                load_group_any<LT, DENSE>(row, qrow, g, ng, V, vec_ok, z, q);
+                unsigned long long pt2[kGroup / 2];
+                float w[kGroup], qp[kGroup], ws, qs;
+                group_masses<MODE>(z, q, g * kGroup, X, pt2, w, qp, ws, qs);
+                const long long Lg = to_fixed(ws, X.fb) - corr_of(delta, qs);
+                int kpos = -1;
+#pragma unroll
+                for (int k = 0; k < kGroup; ++k)
+                    if (w[k] > 0.0f)
+                        kpos = k;
+                const ScanFirst gr = block_scan_first(Lg, rem, -1.0f, kpos >= 0 ? g * kGroup + kpos : -1,
+                                                      sm.tot[1], sm.mx[1], sm.first[1]);
+                if (tid == gr.first) {
+                    // running sums in id order (the group's last boundary is
+                    // its total, so an id past rounding falls back to its last
+                    // id of positive mass)
+                    const long long excl = gr.incl - Lg;
+                    int32_t tk = g * kGroup + (kpos >= 0 ? kpos : 0);
+                    float cw = 0.0f, cq = 0.0f;
+                    for (int k = 0; k < kGroup; ++k) {
+                        cw = __fadd_rn(cw, w[k]);
+                        cq = __fadd_rn(cq, qp[k]);
+                        if (w[k] > 0.0f && excl + to_fixed(cw, X.fb) - corr_of(delta, cq) > rem) {
+                            tk = g * kGroup + k;
+                            break;
+                        }
+                    }
+                    P.out_tokens[b * (K + 1) + jstar] = tk;
+                } else if (gr.first == kFinalThreads && tid == 0) {
+                    P.out_tokens[b * (K + 1) + jstar] = gr.mx; // the chunk's last id of positive mass
+                }
+                tok = -2; // written above
             }
         }
         if (tid == 0) {
-            P.out_tokens[b * (K + 1) + jstar] = tok;
+            if (tok != -2)
+                P.out_tokens[b * (K + 1) + jstar] = tok;
             if (P.residual_mass) {
                 // Z / 2^fb over the residual's normaliser (S' or F / 2^fb)
                 const long long norm = DENSE ? E : F;
@@ -279,21 +374,21 @@ __device__ void final_sequence(const Params &P, int64_t b, long long *sw, int *s
     if (tid == 0) {
         P.seq_E[b] = 0;
         P.seq_F[b] = 0;
-        P.seq_jstar[b] = 0;
-        P.seq_m[b] = 0.0f;
-        P.seq_s[b] = 0.0f;
+        P.seq_info[b] = make_int4(0, 0, 0, 0);
     }
+    __syncthreads(); // the block's scratch is reused by the next sequence
 }
 
+// The final draws: one CTA per sequence (grid-stride beyond the grid size).
+// Dynamic shared memory: CPS chunk records (8 + 4 bytes each).
 template <typename LT, bool DENSE>
 __global__ void __launch_bounds__(kFinalThreads) final_kernel(const Params P)
 {
-    __shared__ long long sw[kFinalWarps];
-    __shared__ int si[kFinalWarps];
-    __shared__ long long s_before;
+    __shared__ FinalSmem sm;
+    extern __shared__ __align__(16) long long s_v[];
     pdl_wait_primary();
     for (int64_t b = blockIdx.x; b < P.B; b += gridDim.x)
-        final_sequence<LT, DENSE>(P, b, sw, si, s_before);
+        final_sequence<LT, DENSE>(P, b, sm, s_v);
 }
 
 } // namespace sv

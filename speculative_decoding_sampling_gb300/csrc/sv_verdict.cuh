@@ -116,9 +116,8 @@ __device__ Verdict seq_verdict(const Params &P, int64_t b, int lane, bool write)
             } else {
                 P.num_emitted[b] = jstar + 1;
             }
-            P.seq_jstar[b] = bad ? -1 : jstar;
-            P.seq_m[b] = m_sel;
-            P.seq_s[b] = s_sel;
+            P.seq_info[b] = make_int4(bad ? -1 : jstar, __float_as_int(m_sel), __float_as_int(s_sel),
+                                      (!DENSE && !bad && jstar < K) ? xsel : -1);
         }
     }
     Verdict v;
