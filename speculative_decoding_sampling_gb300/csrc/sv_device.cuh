@@ -291,8 +291,8 @@ template <typename LT>
 __device__ __forceinline__ void row_ctas(const Params &P, int64_t r, int64_t &first, int &n_parts)
 {
     const int64_t V = P.V;
-    first = vec_of_elem<LT>(P, r * V) / P.span;
-    n_parts = static_cast<int>(vec_of_elem<LT>(P, r * V + V - 1) / P.span - first + 1);
+    first = divi(vec_of_elem<LT>(P, r * V), P.span);
+    n_parts = static_cast<int>(divi(vec_of_elem<LT>(P, r * V + V - 1), P.span) - first + 1);
 }
 
 // ---------------------------------------------- release/acquire counters

@@ -143,7 +143,7 @@ __device__ __forceinline__ bool streamed(const Params &P, int64_t vv)
 {
     constexpr int VW = 16 / sizeof(LT);
     const int64_t e0 = P.h + (vv - 1) * VW;
-    return vv >= 1 && vv <= P.nvec && e0 / P.V == (e0 + VW - 1) / P.V;
+    return vv >= 1 && vv <= P.nvec && divi(e0, P.V) == divi(e0 + VW - 1, P.V);
 }
 
 // The streamed vectors of row r inside vectors [vbeg, vend), as offsets
@@ -184,7 +184,7 @@ __device__ __forceinline__ void ragged_pair(const Params &P, int64_t g, int64_t 
         vv = vl;
         i = lane - 24;
     }
-    if (vv < 0 || vv / P.span != g || streamed<LT>(P, vv))
+    if (vv < 0 || divi(vv, P.span) != g || streamed<LT>(P, vv))
         return;
     const int64_t e = P.h + (vv - 1) * VW + i;
     if (e >= 0 && e < P.total && e / P.V == r) {
@@ -252,11 +252,11 @@ __global__ void __launch_bounds__(kRowCtaThreads, SV_ROW_MIN_CTAS) rows_kernel(c
         // ---- epilogue warp: the CTA's pair of each row, and the draft data
         // of the rows whose first id it holds (fetched ahead, in parallel)
         RowSide pre = {-1, 0.0f, 1.0f, 0.0f};
-        if (lane < n_rows && vec_of_elem<LT>(P, (r0 + lane) * V) / P.span == g)
+        if (lane < n_rows && divi(vec_of_elem<LT>(P, (r0 + lane) * V), P.span) == g)
             pre = fetch_side<LT, DENSE>(P, r0 + lane);
         for (int k = 0; k < n_rows; ++k) {
             const int64_t r = r0 + k;
-            const int64_t first = vec_of_elem<LT>(P, r * V) / P.span;
+            const int64_t first = divi(vec_of_elem<LT>(P, r * V), P.span);
             const bool head = g == first; // this CTA holds the row's first id
             RowSide side = {-1, 0.0f, 1.0f, 0.0f};
             if (k < 32) {

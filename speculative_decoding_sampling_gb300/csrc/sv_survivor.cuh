@@ -39,6 +39,7 @@
 #pragma once
 
 #include <climits>
+#include <type_traits>
 
 #include "sv_verdict.cuh"
 
@@ -241,33 +242,67 @@ struct LaunchMode {
     static constexpr int value = DENSE ? kModeDense : kModeOneHot;
 };
 
-// Fold one group into the lane's running totals of its chunk (A, Qs) and
-// sequence: E2 = (Ehi, Elo) packed pairs, an error-free (Fast2Sum) running
-// sum of pt per id parity (dense); E2's first pair alone, a plain sum of pt
-// (one-hot).
-template <bool DENSE>
+// How a chunk of the draw stream is folded: the residual of a rejection
+// with dense q, the one-hot residual, or p itself (every draft accepted; the
+// same masses as the dense form with q = 0 and the one-hot form with no x).
+// kFoldOneHotNoX: a chunk of a one-hot residual that does not hold the
+// rejected draft id (every chunk but one): the masses are p itself, with
+// the normaliser sum kept.
+enum { kFoldDense = 0, kFoldOneHot = 1, kFoldBonus = 2, kFoldOneHotNoX = 3 };
+
+// Fold one group into the lane's running totals: the chunk's A (sum of the
+// group masses in 2^-fb units) and Qs (sum of qp), and the sequence's
+// normaliser share -- (Ehi, Elo), an error-free (Fast2Sum) running sum of pt
+// per id parity (dense), or Ehi alone, a plain sum of pt (one-hot).  Only
+// the group totals are formed; they equal group_masses' bit for bit (the
+// same per-pair arithmetic, added in the same order).
+template <int KIND>
 __device__ __forceinline__ void fold_group(const float (&z)[kGroup], const float (&q)[kGroup], int32_t e0,
                                            const SurvArgs &X, unsigned long long &Ehi, unsigned long long &Elo,
                                            long long &A, float &Qs)
 {
-    constexpr int MODE = LaunchMode<DENSE>::value;
-    unsigned long long pt2[kGroup / 2];
-    float w[kGroup], qp[kGroup], ws, qs;
-    group_masses<MODE>(z, q, e0, X, pt2, w, qp, ws, qs);
+    const unsigned long long c2 = pack2(X.c, X.c), nmc2 = pack2(-X.mc, -X.mc), inv2 = pack2(X.inv_s, X.inv_s);
     const unsigned long long m1 = pack2(-1.0f, -1.0f);
+    unsigned long long wsum = 0ull, qsum = 0ull; // packed (+0, +0)
+    const bool xin = KIND == kFoldOneHot && static_cast<unsigned>(X.x - e0) < static_cast<unsigned>(kGroup);
 #pragma unroll
     for (int h = 0; h < kGroup / 2; ++h) {
-        if (DENSE) { // |Ehi| >= 2 > every pt
-            const unsigned long long s = add2(Ehi, pt2[h]);
+        const int k = 2 * h;
+        float y0, y1;
+        unpack2(fma2(pack2(z[k], z[k + 1]), c2, nmc2), y0, y1);
+        const unsigned long long pt2 = mul2(pack2(ex2(y0), ex2(y1)), inv2);
+        if (KIND == kFoldDense) { // |Ehi| >= 2 > every pt
+            const unsigned long long s = add2(Ehi, pt2);
             const unsigned long long tt = fma2(Ehi, m1, s);       // s - Ehi
-            Elo = add2(Elo, fma2(tt, m1, pt2[h]));               // + (pt - tt)
+            Elo = add2(Elo, fma2(tt, m1, pt2));                  // + (pt - tt)
             Ehi = s;
+            float d0, d1;
+            unpack2(fma2(pack2(q[k], q[k + 1]), m1, pt2), d0, d1); // pt - q
+            wsum = add2(wsum, pack2(fmaxf(d0, 0.0f), fmaxf(d1, 0.0f)));
+            qsum = add2(qsum, pack2(d0 > 0.0f ? q[k] : 0.0f, d1 > 0.0f ? q[k + 1] : 0.0f));
+        } else if (KIND == kFoldOneHotNoX) {
+            Ehi = add2(Ehi, pt2);
+            wsum = add2(wsum, pt2);
+        } else if (KIND == kFoldOneHot) {
+            Ehi = add2(Ehi, pt2);
+            unsigned long long w2 = pt2;
+            if (xin) { // the rejected draft's own id carries no residual mass
+                float p0, p1;
+                unpack2(pt2, p0, p1);
+                w2 = pack2(e0 + k == X.x ? 0.0f : p0, e0 + k + 1 == X.x ? 0.0f : p1);
+            }
+            wsum = add2(wsum, w2);
         } else {
-            Ehi = add2(Ehi, pt2[h]);
+            wsum = add2(wsum, pt2);
         }
     }
-    A += to_fixed(ws, X.fb);
-    Qs = __fadd_rn(Qs, qs);
+    float a0, a1;
+    unpack2(wsum, a0, a1);
+    A += to_fixed(__fadd_rn(a0, a1), X.fb);
+    if (KIND == kFoldDense) {
+        unpack2(qsum, a0, a1);
+        Qs = __fadd_rn(Qs, __fadd_rn(a0, a1));
+    }
 }
 
 // What a ring stage's consumer needs about the chunk's sequence: written by
@@ -397,22 +432,32 @@ __device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t 
         const int32_t g0 = ccis * kChunkGroups + lane;
         long long A = 0;
         float Qs = 0.0f;
+        auto fold_chunk = [&](auto kind) {
+            constexpr int KIND = decltype(kind)::value;
+            constexpr bool WQ = KIND == kFoldDense;
 #pragma unroll
-        for (int t = 0; t < kChunkTiles; ++t) {
-            const int32_t g = g0 + 32 * t;
-            const bool in = cvalid && g < ng;
-            float z[kGroup], q[kGroup];
-            if (RING)
-                load_group_smem<LT, DENSE>(st, 32 * t + lane, in, z, q);
-            else
-                load_group_any<LT, DENSE>(crow, cq, in ? g : ng, ng, V, cvec, z, q);
-            if (DENSE && cq == nullptr) {
-#pragma unroll
-                for (int j = 0; j < kGroup; ++j)
-                    q[j] = 0.0f;
+            for (int t = 0; t < kChunkTiles; ++t) {
+                const int32_t g = g0 + 32 * t;
+                const bool in = cvalid && g < ng;
+                float z[kGroup], q[kGroup];
+                if (RING)
+                    load_group_smem<LT, WQ>(st, 32 * t + lane, in, z, q);
+                else
+                    load_group_any<LT, WQ>(crow, cq, in ? g : ng, ng, V, cvec, z, q);
+                fold_group<KIND>(z, q, g * kGroup, X, Ehi, Elo, A, Qs);
             }
-            fold_group<DENSE>(z, q, g * kGroup, X, Ehi, Elo, A, Qs);
+        };
+        if (DENSE && cdraft)
+            fold_chunk(std::integral_constant<int, kFoldDense>{});
+        else if (!DENSE && cdraft) {
+            // the rejected draft's id lies in one chunk of its row
+            if (static_cast<unsigned>(X.x - ccis * kChunkGroups * kGroup) < static_cast<unsigned>(kChunkGroups * kGroup))
+                fold_chunk(std::integral_constant<int, kFoldOneHot>{});
+            else
+                fold_chunk(std::integral_constant<int, kFoldOneHotNoX>{});
         }
+        else
+            fold_chunk(std::integral_constant<int, kFoldBonus>{});
         // the chunk's record
         const long long at = warp_sum_ll(A);
         const float qt = DENSE ? warp_sum_f(Qs) : 0.0f;
