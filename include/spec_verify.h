@@ -68,9 +68,8 @@ typedef enum { SV_BF16 = 0, SV_FP32 = 1 } sv_dtype_t;
 #define SV_BAD_ROW 8             /* a logit row with NaN / +inf / no finite  */
 #define SV_DEGENERATE_RESIDUAL 16 /* residual mass 0 after a rejection: the  */
                                   /* token was drawn from p instead          */
-#define SV_INTERNAL_TIMEOUT 32   /* a bounded wait inside a kernel ran out  */
-                                  /* (never expected): outputs are undefined */
-                                  /* and the workspace must be re-zeroed     */
+#define SV_INTERNAL_TIMEOUT 32   /* reserved: no kernel of this version     */
+                                  /* waits on a flag, so it is never set     */
 
 /* Largest vocabulary supported. */
 #define SV_MAX_V (1 << 21)
@@ -119,16 +118,17 @@ sv_status_t spec_verify(const void *target_logits, sv_dtype_t logits_dtype,
 /* The two stages of spec_verify, for callers that time or schedule them
  * separately.  Same arguments and meaning as spec_verify.
  *
- * sv_verify_rows: the row pass over all B*(K+1) rows (max and softmax
- * normaliser of every row, the accept test of every draft), then per sequence
- * the first rejection; writes accept_flags, accept_prob, num_emitted, the
- * accepted prefix of out_tokens and its -1 padding, and leaves in the
- * workspace which row each sequence draws its final token from.
+ * sv_verify_rows: the row pass over all B*(K+1) rows: the max and softmax
+ * normaliser of every row, in pieces, and the draft data of every row
+ * (x, z(x), q(x), u), left in the workspace.  Writes no output.
  *
- * sv_sample_survivors: per sequence, the draw of the final token from the
- * residual (after a rejection) or from p_K (all accepted); writes
+ * sv_sample_survivors: per sequence, the accept tests and the first
+ * rejection (accept_flags, accept_prob, num_emitted, the accepted prefix of
+ * out_tokens and its -1 padding, status bits), then the draw of the final
+ * token from the residual (after a rejection) or from p_K (all accepted):
  * out_tokens[b, num_emitted-1] and residual_mass.  Must follow
- * sv_verify_rows on the same stream with the same workspace and inputs. */
+ * sv_verify_rows on the same stream with the same workspace and inputs; it
+ * returns the workspace to zero. */
 sv_status_t sv_verify_rows(const void *target_logits, sv_dtype_t logits_dtype,
                            const float *draft_probs,
                            const int32_t *draft_tokens, const float *uniforms,

@@ -1,6 +1,7 @@
 // spec_verify.cu -- C ABI of the verification library: argument checks,
-// workspace layout, and the two launches (row pass, final draws) on the
-// caller's stream.  The operation itself is documented in spec_verify.h.
+// workspace layout, and the three launches (row pass, draw stream, final
+// draws) on the caller's stream, each chained to the one before by
+// programmatic dependent launch.  The operation itself is documented in spec_verify.h.
 #include "spec_verify.h"
 
 #include <cmath>
@@ -326,7 +327,7 @@ const char *sv_status_string(sv_status_t status)
 // workspace: a server whose device memory is reserved up front by its own
 // pool and that forbids cudaMalloc on the request path, or a plugin interface
 // that passes a plugin its input and output buffers but no allocator.  For
-// them, spec_verify_noalloc runs the same two kernels with their scratch in a
+// them, spec_verify_noalloc runs the same three kernels with their scratch in a
 // fixed-size array that lives in the library's device image.  The array is
 // shared by every call on a device and keeps the last call's contents, so
 // each call clears the bytes it needs before launching; calls that overlap on

@@ -205,7 +205,7 @@ __device__ void final_sequence(const Params &P, int64_t b, FinalSmem &sm, long l
     const int32_t K = P.K, V = P.V, CPS = P.CPS;
     long long *ra = P.rec_a + b * CPS;
     float *rq = P.rec_q + b * CPS;
-    // ---- round 1, all in flight together
+    // ---- first load round, all in flight together
     const int4 info = __ldcg(&P.seq_info[b]);
     const long long Eraw = __ldcg(&P.seq_E[b]), Fraw = __ldcg(&P.seq_F[b]);
     const float u = __ldg(&P.u[b * (K + 1) + K]);
@@ -307,7 +307,7 @@ __device__ void final_sequence(const Params &P, int64_t b, FinalSmem &sm, long l
                 rem = LLONG_MAX;
             }
             if (sel >= 0) {
-                // ---- round 2: the chunk's 128 groups, one per thread
+                // ---- second load round: the chunk's 128 groups, one per thread
                 constexpr int MODE = LaunchMode<DENSE>::value;
                 const int32_t ng = (V + kGroup - 1) / kGroup;
                 const int32_t g = sel * kChunkGroups + tid;
