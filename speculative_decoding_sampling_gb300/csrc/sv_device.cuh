@@ -184,27 +184,22 @@ __device__ __forceinline__ void merge_ms(float &M, float &S, float M2, float S2,
 
 // --------------------------------------------------- exact fixed-point mass
 
-// A finite fp32 value w as the nearest integer multiple of 2^-fb (halves
-// away from zero), for |w| * 2^fb < 2^62.  Sums of these integers are exact
-// and independent of the order of summation.  Integer ALU only: w = m * 2^(e-150)
-// with a 24-bit m, so w * 2^fb = m * 2^s, s = e - 150 + fb, is a shift of m
-// (rounded when s < 0).  The float-to-64-bit-integer conversion instruction
-// is avoided on purpose: it runs on the double-precision pipe, which is
-// narrow on this GPU.
+// A finite fp32 value w as the nearest integer multiple of 2^-fb (ties to
+// even), for |w| * 2^fb < 2^55.  Sums of these integers are exact and
+// independent of the order of summation.  x = |w| * 2^fb is exact (a power
+// of two scale); it is split as x = hi * 2^32 + lo with hi = trunc(x / 2^32)
+// (< 2^23, exact) and lo = x - hi * 2^32 (exact: x has 24 significant bits
+// and lo keeps the ones below 2^32), and only lo is rounded, by a 32-bit
+// conversion.  The float-to-64-bit-integer conversion instruction is
+// avoided on purpose: it runs on the double-precision pipe, which is narrow
+// on this GPU.
 __device__ __forceinline__ long long to_fixed(float w, int fb)
 {
-    const uint32_t b = __float_as_uint(w);
-    const int e = static_cast<int>((b >> 23) & 0xFFu);
-    const uint32_t m = (b & 0x7FFFFFu) | 0x800000u;
-    const int s = e - 150 + fb;
-    long long r;
-    if (s >= 0)
-        r = static_cast<long long>(m) << (s < 38 ? s : 38);
-    else
-        r = -s < 32 ? static_cast<long long>((m + (1u << (-s - 1))) >> -s) : 0;
-    if (e == 0)
-        r = 0; // zero or subnormal: below 2^-126
-    return (b >> 31) ? -r : r;
+    const float x = __fmul_rn(fabsf(w), __int_as_float((127 + fb) << 23));
+    const float hi = truncf(__fmul_rn(x, 2.3283064365386963e-10f)); // x / 2^32
+    const float lo = __fmaf_rn(hi, -4294967296.0f, x);
+    const long long r = (static_cast<long long>(__float2uint_rz(hi)) << 32) + __float2uint_rn(lo);
+    return w < 0.0f ? -r : r;
 }
 
 // floor(u * Z) for u in [0, 1) and 0 <= Z < 2^62, exactly: u = mu * 2^-k with
