@@ -35,7 +35,7 @@ struct Plan {
     int32_t PM;   // row_part slots per row
     int32_t CPS;  // final-draw chunks per sequence
     int32_t fix;  // fractional bits of the fixed-point masses
-    size_t off_part, off_row_side, off_seq_info, off_seqE, off_seqF, off_rec_a, off_rec_q, bytes;
+    size_t off_part, off_row_side, off_seq_info, off_seqE, off_rec_a, off_rec_q, bytes;
 };
 
 bool make_plan(int64_t B, int32_t K, int32_t V, Plan &p)
@@ -59,7 +59,6 @@ bool make_plan(int64_t B, int32_t K, int32_t V, Plan &p)
     p.off_row_side = off; off = align_up(off + R * sizeof(float4));
     p.off_seq_info = off; off = align_up(off + Bz * sizeof(int4));
     p.off_seqE = off;     off = align_up(off + Bz * sizeof(long long));
-    p.off_seqF = off;     off = align_up(off + Bz * sizeof(long long));
     p.off_rec_a = off;    off = align_up(off + Bz * p.CPS * sizeof(long long));
     p.off_rec_q = off;    off = align_up(off + Bz * p.CPS * sizeof(float));
     p.bytes = off;
@@ -240,7 +239,6 @@ sv_status_t run(int stages, const void *logits, sv_dtype_t dtype, const float *q
     P.row_side = reinterpret_cast<float4 *>(ws + plan.off_row_side);
     P.seq_info = reinterpret_cast<int4 *>(ws + plan.off_seq_info);
     P.seq_E = reinterpret_cast<long long *>(ws + plan.off_seqE);
-    P.seq_F = reinterpret_cast<long long *>(ws + plan.off_seqF);
     P.rec_a = reinterpret_cast<long long *>(ws + plan.off_rec_a);
     P.rec_q = reinterpret_cast<float *>(ws + plan.off_rec_q);
     P.PM = plan.PM;

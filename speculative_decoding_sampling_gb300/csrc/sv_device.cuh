@@ -66,7 +66,6 @@ struct Params {
     int4 *seq_info;       // [B]       the verdict for the final kernel: j* (-1 = bad sequence), bits of the
                           //           surviving row's max m and normaliser s, the rejected draft x (one-hot) or -1
     long long *seq_E;     // [B]       exact sum of pt over the surviving row (dense), 2^-fix_bits units
-    long long *seq_F;     // [B]       sum of pt (one-hot normaliser), 2^-fix_bits units
     long long *rec_a;     // [B * CPS] per chunk: mass A, 2^-fix_bits units
     float *rec_q;         // [B * CPS] per chunk: Qp
     int64_t total;        // R * V elements of the logits

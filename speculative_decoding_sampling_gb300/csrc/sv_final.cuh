@@ -145,7 +145,7 @@ __device__ int32_t scan_round(const LT *row, const float *qrow, int32_t g0, int3
     load_group_any<LT, DENSE>(row, qrow, g, ng, V, vec_ok, z, q);
     unsigned long long pt2[kGroup / 2];
     float w[kGroup], qp[kGroup], ws, qs;
-    group_masses<MODE>(z, q, g * kGroup, X, pt2, w, qp, ws, qs);
+    group_masses<MODE, DENSE>(z, q, g * kGroup, X, pt2, w, qp, ws, qs);
     const long long Lg = to_fixed(ws, X.fb) - corr_of(delta, qs);
     int kpos = -1;
 #pragma unroll
@@ -207,7 +207,7 @@ __device__ void final_sequence(const Params &P, int64_t b, FinalSmem &sm, long l
     float *rq = P.rec_q + b * CPS;
     // ---- first load round, all in flight together
     const int4 info = __ldcg(&P.seq_info[b]);
-    const long long Eraw = __ldcg(&P.seq_E[b]), Fraw = __ldcg(&P.seq_F[b]);
+    const long long Eraw = DENSE ? __ldcg(&P.seq_E[b]) : 0;
     const float u = __ldg(&P.u[b * (K + 1) + K]);
     const int R = (CPS + kFinalThreads - 1) / kFinalThreads; // thread t holds chunks [t*R, (t+1)*R)
     for (int i = 0; i < R; ++i) {
@@ -234,9 +234,10 @@ __device__ void final_sequence(const Params &P, int64_t b, FinalSmem &sm, long l
         const bool vec_ok = (reinterpret_cast<uintptr_t>(row) & 15u) == 0 &&
                             (qrow == nullptr || (reinterpret_cast<uintptr_t>(qrow) & 15u) == 0);
         // dense: delta = E - 2^fb = (S' - 1) 2^fb, S' the exact sum of pt;
-        // one-hot: F = sum of pt in 2^-fb units (the residual's normaliser)
+        // one-hot: the residual's mass is 1 - p(x), p(x) as the accept test
+        // took it (z(x) from the row pass's side data)
         const long long E = rejected && DENSE ? Eraw : 0;
-        const long long F = rejected && !DENSE ? Fraw : 0;
+        const float zx = rejected && !DENSE ? __ldcg(&P.row_side[b * (K + 1) + jstar]).y : 0.0f;
         const float delta = rejected && DENSE ? static_cast<float>(E - (1ll << P.fix_bits)) : 0.0f;
         // ---- the chunk: block scan over the threads' record sums, the
         // first thread whose running sum passes floor(u * Z)
@@ -268,7 +269,7 @@ __device__ void final_sequence(const Params &P, int64_t b, FinalSmem &sm, long l
                 load_group_any<LT, false>(row, nullptr, g0 + tid, ng, V, vec_ok, z, q);
                 unsigned long long pt2[kGroup / 2];
                 float w[kGroup], qp[kGroup], ws, qs;
-                group_masses<kModeBonus>(z, q, (g0 + tid) * kGroup, Xb, pt2, w, qp, ws, qs);
+                group_masses<kModeBonus, false>(z, q, (g0 + tid) * kGroup, Xb, pt2, w, qp, ws, qs);
                 A += to_fixed(ws, Xb.fb);
             }
             long long Zp;
@@ -315,7 +316,7 @@ __device__ void final_sequence(const Params &P, int64_t b, FinalSmem &sm, long l
                 load_group_any<LT, DENSE>(row, qrow, g, ng, V, vec_ok, z, q);
                 unsigned long long pt2[kGroup / 2];
                 float w[kGroup], qp[kGroup], ws, qs;
-                group_masses<MODE>(z, q, g * kGroup, X, pt2, w, qp, ws, qs);
+                group_masses<MODE, DENSE>(z, q, g * kGroup, X, pt2, w, qp, ws, qs);
                 const long long Lg = to_fixed(ws, X.fb) - corr_of(delta, qs);
                 int kpos = -1;
 #pragma unroll
@@ -350,11 +351,14 @@ __device__ void final_sequence(const Params &P, int64_t b, FinalSmem &sm, long l
             if (tok != -2)
                 P.out_tokens[b * (K + 1) + jstar] = tok;
             if (P.residual_mass) {
-                // Z / 2^fb over the residual's normaliser (S' or F / 2^fb)
-                const long long norm = DENSE ? E : F;
-                P.residual_mass[b] = (rejected && !degenerate && norm > 0)
-                                         ? __fdiv_rn(static_cast<float>(Z), static_cast<float>(norm))
-                                         : 0.0f;
+                float rm = 0.0f;
+                if (rejected && !degenerate) {
+                    if (DENSE) // Z / 2^fb over the residual's normaliser S'
+                        rm = E > 0 ? __fdiv_rn(static_cast<float>(Z), static_cast<float>(E)) : 0.0f;
+                    else
+                        rm = __fsub_rn(1.0f, __fdiv_rn(term(zx, X.c, X.mc), v.s));
+                }
+                P.residual_mass[b] = rm;
             }
             if (degenerate && P.status)
                 atomicOr(P.status, kDegenerate);
@@ -373,7 +377,6 @@ __device__ void final_sequence(const Params &P, int64_t b, FinalSmem &sm, long l
         P.row_side[r0 + j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if (tid == 0) {
         P.seq_E[b] = 0;
-        P.seq_F[b] = 0;
         P.seq_info[b] = make_int4(0, 0, 0, 0);
     }
     __syncthreads(); // the block's scratch is reused by the next sequence

@@ -166,8 +166,10 @@ __device__ __forceinline__ void load_group_any(const LT *row, const float *qrow,
 // Ids are taken in pairs (2h, 2h+1) with packed fp32 arithmetic; each total
 // is added in the fixed order ((x0 + x2) + x4) + x6 + ((x1 + x3) + x5) + x7.
 // The fold and the draw's scan both use this routine, so they see identical
-// group totals.
-template <int MODE>
+// group totals.  NORM: pt_i = e_i / s~ (dense launches); otherwise pt_i = e_i
+// (a one-hot or extra-token draw needs no normaliser: its boundaries are
+// relative to its own total).
+template <int MODE, bool NORM>
 __device__ __forceinline__ void group_masses(const float (&z)[kGroup], const float (&q)[kGroup], int32_t e0,
                                              const SurvArgs &X, unsigned long long (&pt2)[kGroup / 2],
                                              float (&w)[kGroup], float (&qp)[kGroup], float &ws, float &qs)
@@ -180,7 +182,7 @@ __device__ __forceinline__ void group_masses(const float (&z)[kGroup], const flo
         const int k = 2 * h;
         float y0, y1;
         unpack2(fma2(pack2(z[k], z[k + 1]), c2, nmc2), y0, y1);
-        pt2[h] = mul2(pack2(ex2(y0), ex2(y1)), inv2);
+        pt2[h] = NORM ? mul2(pack2(ex2(y0), ex2(y1)), inv2) : pack2(ex2(y0), ex2(y1));
         if (MODE == kModeDense) {
             float d0, d1;
             unpack2(fma2(pack2(q[k], q[k + 1]), m1, pt2[h]), d0, d1); // pt - q
@@ -246,17 +248,16 @@ struct LaunchMode {
 // with dense q, the one-hot residual, or p itself (every draft accepted; the
 // same masses as the dense form with q = 0 and the one-hot form with no x).
 // kFoldOneHotNoX: a chunk of a one-hot residual that does not hold the
-// rejected draft id (every chunk but one): the masses are p itself, with
-// the normaliser sum kept.
+// rejected draft id (every chunk but one): the masses are p itself.
 enum { kFoldDense = 0, kFoldOneHot = 1, kFoldBonus = 2, kFoldOneHotNoX = 3 };
 
 // Fold one group into the lane's running totals: the chunk's A (sum of the
-// group masses in 2^-fb units) and Qs (sum of qp), and the sequence's
-// normaliser share -- (Ehi, Elo), an error-free (Fast2Sum) running sum of pt
-// per id parity (dense), or Ehi alone, a plain sum of pt (one-hot).  Only
-// the group totals are formed; they equal group_masses' bit for bit (the
-// same per-pair arithmetic, added in the same order).
-template <int KIND>
+// group masses in 2^-fb units) and Qs (sum of qp), and, for a dense
+// rejection, the sequence's normaliser share (Ehi, Elo), an error-free
+// (Fast2Sum) running sum of pt per id parity.  Only the group totals are
+// formed; they equal group_masses' bit for bit (the same per-pair
+// arithmetic, added in the same order).
+template <int KIND, bool NORM>
 __device__ __forceinline__ void fold_group(const float (&z)[kGroup], const float (&q)[kGroup], int32_t e0,
                                            const SurvArgs &X, unsigned long long &Ehi, unsigned long long &Elo,
                                            long long &A, float &Qs)
@@ -270,7 +271,7 @@ __device__ __forceinline__ void fold_group(const float (&z)[kGroup], const float
         const int k = 2 * h;
         float y0, y1;
         unpack2(fma2(pack2(z[k], z[k + 1]), c2, nmc2), y0, y1);
-        const unsigned long long pt2 = mul2(pack2(ex2(y0), ex2(y1)), inv2);
+        const unsigned long long pt2 = NORM ? mul2(pack2(ex2(y0), ex2(y1)), inv2) : pack2(ex2(y0), ex2(y1));
         if (KIND == kFoldDense) { // |Ehi| >= 2 > every pt
             const unsigned long long s = add2(Ehi, pt2);
             const unsigned long long tt = fma2(Ehi, m1, s);       // s - Ehi
@@ -281,10 +282,8 @@ __device__ __forceinline__ void fold_group(const float (&z)[kGroup], const float
             wsum = add2(wsum, pack2(fmaxf(d0, 0.0f), fmaxf(d1, 0.0f)));
             qsum = add2(qsum, pack2(d0 > 0.0f ? q[k] : 0.0f, d1 > 0.0f ? q[k + 1] : 0.0f));
         } else if (KIND == kFoldOneHotNoX) {
-            Ehi = add2(Ehi, pt2);
             wsum = add2(wsum, pt2);
         } else if (KIND == kFoldOneHot) {
-            Ehi = add2(Ehi, pt2);
             unsigned long long w2 = pt2;
             if (xin) { // the rejected draft's own id carries no residual mass
                 float p0, p1;
@@ -390,20 +389,20 @@ __device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t 
     const unsigned long long E0 = DENSE ? pack2(2.0f, 2.0f) : 0ull;
     unsigned long long Ehi = E0, Elo = 0ull; // see fold_group
     auto flush = [&]() {
-        // the sequence's share of its normaliser: E = sum pt (dense) or
-        // F = sum pt (one-hot), in 2^-fb units; read by the final kernel
-        float h0, h1, l0, l1;
-        unpack2(Ehi, h0, h1);
-        unpack2(Elo, l0, l1);
-        long long e = to_fixed(h0, X.fb) + to_fixed(h1, X.fb);
-        if (DENSE)
-            e += to_fixed(l0, X.fb) + to_fixed(l1, X.fb) - 2 * to_fixed(2.0f, X.fb);
-        const long long E = warp_sum_ll(e);
-        if (lane == 0 && cvalid && cdraft)
-            atomicAdd(reinterpret_cast<unsigned long long *>(DENSE ? &P.seq_E[cur] : &P.seq_F[cur]),
-                      static_cast<unsigned long long>(E));
-        Ehi = E0;
-        Elo = 0ull;
+        // the dense rejection's share of its normaliser E = sum pt, in 2^-fb
+        // units; read by the final kernel
+        if (DENSE) {
+            float h0, h1, l0, l1;
+            unpack2(Ehi, h0, h1);
+            unpack2(Elo, l0, l1);
+            const long long e = to_fixed(h0, X.fb) + to_fixed(h1, X.fb) + to_fixed(l0, X.fb) + to_fixed(l1, X.fb) -
+                                2 * to_fixed(2.0f, X.fb);
+            const long long E = warp_sum_ll(e);
+            if (lane == 0 && cvalid && cdraft)
+                atomicAdd(reinterpret_cast<unsigned long long *>(&P.seq_E[cur]), static_cast<unsigned long long>(E));
+            Ehi = E0;
+            Elo = 0ull;
+        }
     };
 
 #pragma unroll 1
@@ -444,7 +443,7 @@ __device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t 
                     load_group_smem<LT, WQ>(st, 32 * t + lane, in, z, q);
                 else
                     load_group_any<LT, WQ>(crow, cq, in ? g : ng, ng, V, cvec, z, q);
-                fold_group<KIND>(z, q, g * kGroup, X, Ehi, Elo, A, Qs);
+                fold_group<KIND, DENSE>(z, q, g * kGroup, X, Ehi, Elo, A, Qs);
             }
         };
         if (DENSE && cdraft)
@@ -476,7 +475,8 @@ __device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t 
     flush();
 }
 
-// The draw stream.  Each warp takes a contiguous range of the call's chunks.
+// The draw stream.  Each warp takes a contiguous range of the call's chunks
+// (within one sequence when there are at least as many warps as sequences).
 // Launched behind the row pass with programmatic dependent launch: it waits
 // in griddepcontrol.wait until the row pass has completed.
 template <typename LT, bool DENSE>
@@ -489,7 +489,20 @@ __global__ void __launch_bounds__(kDrawWarps * 32, SV_MIN_CTAS) survivor_kernel(
     pdl_wait_primary();
     const int64_t W = static_cast<int64_t>(blockIdx.x) * kDrawWarps + warp;
     const int64_t NW = static_cast<int64_t>(gridDim.x) * kDrawWarps;
-    const int64_t c0 = W * P.NC / NW, c1 = (W + 1) * P.NC / NW;
+    int64_t c0, c1;
+    if (NW >= P.B) {
+        // every sequence its own group of warps (sequence b: warps
+        // [ceil(b NW / B), ceil((b+1) NW / B))), its chunks split evenly
+        // among them: no warp meets a second sequence and its verdict
+        const int64_t b = W * P.B / NW;
+        const int64_t w0 = (b * NW + P.B - 1) / P.B, w1 = ((b + 1) * NW + P.B - 1) / P.B;
+        const int64_t i = W - w0, n = w1 - w0;
+        c0 = b * P.CPS + i * P.CPS / n;
+        c1 = b * P.CPS + (i + 1) * P.CPS / n;
+    } else {
+        c0 = W * P.NC / NW;
+        c1 = (W + 1) * P.NC / NW;
+    }
     if (c0 < c1) {
         if (P.ring_ok)
             draw_range<LT, DENSE, true>(P, c0, c1, lane, ring, info[warp]);
