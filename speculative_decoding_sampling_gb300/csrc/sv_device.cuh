@@ -358,6 +358,20 @@ __device__ __forceinline__ float warp_sum_f(float v)
     return v;
 }
 
+// Sum over the warp of values in [0, 2^58): three pieces (bits 0-20, 21-41,
+// 42 on) summed as 32-bit lane values, each sum below 2^27: exact.
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
+{
+    const uint32_t lo = static_cast<uint32_t>(v), hi = static_cast<uint32_t>(v >> 32);
+    const uint32_t p0 = lo & 0x1FFFFFu;
+    const uint32_t p1 = __funnelshift_r(lo, hi, 21) & 0x1FFFFFu;
+    const uint32_t p2 = hi >> 10;
+    const unsigned long long s0 = __reduce_add_sync(0xFFFFFFFFu, p0);
+    const unsigned long long s1 = __reduce_add_sync(0xFFFFFFFFu, p1);
+    const unsigned long long s2 = __reduce_add_sync(0xFFFFFFFFu, p2);
+    return s0 + (s1 << 21) + (s2 << 42);
+}
+
 __device__ __forceinline__ long long warp_incl_scan_ll(long long v, int lane)
 {
 #pragma unroll

@@ -331,7 +331,7 @@ __device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t 
     const int64_t nchunks = c1 - c0;
 
     // ---- issue side: the chunk kDrawStages - 1 ahead of the consumer
-    int64_t ib = c0 / CPS;
+    int64_t ib = divi(c0, CPS);
     int32_t icis = static_cast<int32_t>(c0 - ib * CPS);
     int ist = 0;       // ring stage of the next issued chunk
     int64_t iseq = -1; // sequence whose verdict iv holds
@@ -353,9 +353,10 @@ __device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t 
                 const uint8_t *src = reinterpret_cast<const uint8_t *>(irow + static_cast<int64_t>(g0) * kGroup);
                 const uint8_t *qsrc =
                     DENSE && iq ? reinterpret_cast<const uint8_t *>(iq + static_cast<int64_t>(g0) * kGroup) : nullptr;
+                const bool full = (icis + 1) * kChunkGroups <= ng; // every group of the chunk in the row
 #pragma unroll
                 for (int t = 0; t < kChunkTiles; ++t) {
-                    if (g0 + 32 * t < ng) {
+                    if (full || g0 + 32 * t < ng) {
                         const int gl = 32 * t + lane;
 #pragma unroll
                         for (int h = 0; h < LB; h += 16)
@@ -378,7 +379,7 @@ __device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t 
     };
 
     // ---- consumer side
-    int64_t cb = c0 / CPS;
+    int64_t cb = divi(c0, CPS);
     int32_t ccis = static_cast<int32_t>(c0 - cb * CPS);
     int cst = 0;      // ring stage of chunk k
     int64_t cur = -1; // sequence whose totals are being accumulated
@@ -429,6 +430,7 @@ __device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t 
         }
         const uint8_t *st = ring + cst * Shape::kChunkBytes;
         const int32_t g0 = ccis * kChunkGroups + lane;
+        const bool full = (ccis + 1) * kChunkGroups <= ng; // every group of the chunk in the row
         long long A = 0;
         float Qs = 0.0f;
         auto fold_chunk = [&](auto kind) {
@@ -437,7 +439,7 @@ __device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t 
 #pragma unroll
             for (int t = 0; t < kChunkTiles; ++t) {
                 const int32_t g = g0 + 32 * t;
-                const bool in = cvalid && g < ng;
+                const bool in = cvalid && (full || g < ng);
                 float z[kGroup], q[kGroup];
                 if (RING)
                     load_group_smem<LT, WQ>(st, 32 * t + lane, in, z, q);
@@ -458,7 +460,7 @@ __device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t 
         else
             fold_chunk(std::integral_constant<int, kFoldBonus>{});
         // the chunk's record
-        const long long at = warp_sum_ll(A);
+        const long long at = static_cast<long long>(warp_sum_u64(static_cast<unsigned long long>(A)));
         const float qt = DENSE ? warp_sum_f(Qs) : 0.0f;
         if (lane == 0) {
             P.rec_a[cb * CPS + ccis] = at;
@@ -494,14 +496,14 @@ __global__ void __launch_bounds__(kDrawWarps * 32, SV_MIN_CTAS) survivor_kernel(
         // every sequence its own group of warps (sequence b: warps
         // [ceil(b NW / B), ceil((b+1) NW / B))), its chunks split evenly
         // among them: no warp meets a second sequence and its verdict
-        const int64_t b = W * P.B / NW;
-        const int64_t w0 = (b * NW + P.B - 1) / P.B, w1 = ((b + 1) * NW + P.B - 1) / P.B;
+        const int64_t b = divi(W * P.B, NW);
+        const int64_t w0 = divi(b * NW + P.B - 1, P.B), w1 = divi((b + 1) * NW + P.B - 1, P.B);
         const int64_t i = W - w0, n = w1 - w0;
-        c0 = b * P.CPS + i * P.CPS / n;
-        c1 = b * P.CPS + (i + 1) * P.CPS / n;
+        c0 = b * P.CPS + divi(i * P.CPS, n);
+        c1 = b * P.CPS + divi((i + 1) * P.CPS, n);
     } else {
-        c0 = W * P.NC / NW;
-        c1 = (W + 1) * P.NC / NW;
+        c0 = divi(W * P.NC, NW);
+        c1 = divi((W + 1) * P.NC, NW);
     }
     if (c0 < c1) {
         if (P.ring_ok)
