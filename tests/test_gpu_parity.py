@@ -179,3 +179,30 @@ def test_misaligned_base_pointers(orc):
     u = torch.from_numpy(inp.u).cuda()
     cand = G.run(logits, q, tok, u, inp.T)
     _check(orc, inp, cand)
+
+
+@pytest.mark.parametrize("onehot", [False, True], ids=["dense", "onehot"])
+def test_many_short_sequences(orc, onehot):
+    """More sequences than draw warps (B = 5000, V = 300): each warp's chunk
+    range then spans several sequences, each with its own verdict."""
+    base = synth.WORKLOADS["b8_k4_v32000_bf16"]
+    w = base.with_(name="many", B=5000, K=2, V=300, Tq=0.0 if onehot else 0.8,
+                   onehot_p=0.5 if onehot else 0.0)
+    inp = synth.generate(w, seed=31 + int(onehot))
+    cand = G.run_inputs(inp)
+    assert cand["status"] == 0
+    _check(orc, inp, cand)
+
+
+@pytest.mark.parametrize("onehot", [False, True], ids=["dense", "onehot"])
+def test_largest_vocabulary(orc, onehot):
+    """V = SV_MAX_V (2^21): 2048 draw chunks per row, 22 fraction bits for
+    the largest fixed-point totals."""
+    from speculative_decoding_sampling_gb300 import _native as N
+    base = synth.WORKLOADS["b8_k4_v32000_bf16"]
+    w = base.with_(name="maxv", B=3, K=2, V=N.SV_MAX_V, Tq=0.0 if onehot else 0.8,
+                   onehot_p=0.5 if onehot else 0.0)
+    inp = synth.generate(w, seed=41 + int(onehot))
+    cand = G.run_inputs(inp)
+    assert cand["status"] == 0
+    _check(orc, inp, cand)
