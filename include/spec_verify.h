@@ -92,6 +92,11 @@ size_t sv_workspace_bytes(int64_t B, int32_t K, int32_t V);
  *   uniforms       [B, K+1] fp32 in [0, 1); u[b,k] tests draft k, u[b,K] is
  *                  the final draw used for the correction or extra token.
  *   temperature    T > 0, applied to the target logits only.
+ * Input pointers may be device memory or page-locked host memory mapped into
+ * the device's address space (cudaHostAlloc / cudaHostRegister); host inputs
+ * are read in place by the kernels, so only the bytes the step touches cross
+ * the host link: every logit once, the surviving rows' logits again, the
+ * draft probabilities of the rejected rows and the drafted entries of q.
  * Outputs:
  *   out_tokens     [B, K+1] int32: accepted drafts, then the drawn token, then
  *                  -1 padding.

@@ -61,23 +61,38 @@ def _ptr(t: torch.Tensor | None) -> int | None:
     return None if t is None else t.data_ptr()
 
 
-def _check(t: torch.Tensor, name: str, dtype, shape, device):
+def _check(t: torch.Tensor, name: str, dtype, shape, device, host_ok: bool = False):
     if t.dtype != dtype:
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
-    if t.device != device:
-        raise ValueError(f"{name}: expected device {device}, got {t.device}")
+    if t.device != device and not (host_ok and _pinned(t)):
+        raise ValueError(f"{name}: expected device {device}" + (" or page-locked host memory" if host_ok else "")
+                         + f", got {t.device}")
     if not t.is_contiguous():
         raise ValueError(f"{name}: must be contiguous")
+
+
+def _exec_device(target_logits: torch.Tensor) -> torch.device:
+    """The GPU a call runs on: the logits' own, or the current one for
+    page-locked host logits."""
+    if target_logits.is_cuda:
+        return target_logits.device
+    if _pinned(target_logits):
+        return torch.device("cuda", torch.cuda.current_device())
+    raise ValueError("target_logits must be a CUDA tensor or page-locked host memory")
+
+
+def _pinned(t: torch.Tensor) -> bool:
+    """A page-locked CPU tensor: mapped into every device's address space, so
+    the kernels read it in place (only the bytes they touch cross the link)."""
+    return t.device.type == "cpu" and t.is_pinned()
 
 
 def _call(fn_name: str, target_logits, draft_probs, draft_tokens, uniforms,
           temperature, out_tokens, num_emitted, accept_flags, accept_prob,
           residual_mass, status, workspace, stream):
-    if not target_logits.is_cuda:
-        raise ValueError("target_logits must be a CUDA tensor")
-    dev = target_logits.device
+    dev = _exec_device(target_logits)
     if target_logits.dim() != 3:
         raise ValueError("target_logits must be [B, K+1, V]")
     B, K1, V = target_logits.shape
@@ -93,13 +108,13 @@ def _call(fn_name: str, target_logits, draft_probs, draft_tokens, uniforms,
     if not target_logits.is_contiguous():
         raise ValueError("target_logits must be contiguous")
     if draft_probs is not None:
-        _check(draft_probs, "draft_probs", torch.float32, (B, K, V), dev)
+        _check(draft_probs, "draft_probs", torch.float32, (B, K, V), dev, host_ok=True)
     if draft_tokens is None:
         if K > 0:
             raise ValueError("draft_tokens required when K > 0")
     else:
-        _check(draft_tokens, "draft_tokens", torch.int32, (B, K), dev)
-    _check(uniforms, "uniforms", torch.float32, (B, K + 1), dev)
+        _check(draft_tokens, "draft_tokens", torch.int32, (B, K), dev, host_ok=True)
+    _check(uniforms, "uniforms", torch.float32, (B, K + 1), dev, host_ok=True)
     for name, t, dtype, shape in (("out_tokens", out_tokens, torch.int32, (B, K + 1)),
                                   ("num_emitted", num_emitted, torch.int32, (B,)),
                                   ("accept_flags", accept_flags, torch.int8, (B, K)),
@@ -130,7 +145,7 @@ def _call(fn_name: str, target_logits, draft_probs, draft_tokens, uniforms,
 def _outputs(target_logits, want_probs, out):
     B, K1, V = target_logits.shape
     K = K1 - 1
-    dev = target_logits.device
+    dev = _exec_device(target_logits)
     o = dict(out or {})
     o.setdefault("out_tokens", torch.empty((B, K + 1), dtype=torch.int32, device=dev))
     o.setdefault("num_emitted", torch.empty((B,), dtype=torch.int32, device=dev))
@@ -154,7 +169,10 @@ def spec_verify(target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
 
     target_logits [B, K+1, V] bf16/fp32; draft_probs [B, K, V] fp32 or None
     (one-hot drafts); draft_tokens [B, K] int32; uniforms [B, K+1] fp32 in
-    [0, 1) with uniforms[:, K] the final draw; temperature > 0.
+    [0, 1) with uniforms[:, K] the final draw; temperature > 0.  The inputs
+    may be CUDA tensors or page-locked (pinned) CPU tensors, which the
+    kernels read in place: a pinned draft_probs sends only the rows the
+    draws use (the rejected ones) and the drafted entries over the link.
     `out` may supply preallocated output tensors by name; `status` an int32
     [1] device tensor that receives SV_BAD_* bits.  Runs asynchronously on
     `stream` (default: the current stream)."""

@@ -206,3 +206,30 @@ def test_largest_vocabulary(orc, onehot):
     cand = G.run_inputs(inp)
     assert cand["status"] == 0
     _check(orc, inp, cand)
+
+
+@pytest.mark.parametrize("where", ["q_pinned", "all_pinned"])
+def test_pinned_host_inputs_read_in_place(orc, where):
+    """Page-locked host inputs are read in place by the kernels and give the
+    same results as device-resident ones."""
+    import speculative_decoding_sampling_gb300 as sv
+    w = synth.WORKLOADS["b64_k5_v128256_bf16_topp"].with_(B=12, V=20000)
+    inp = synth.generate(w, seed=51)
+    lg, q, tok, u = G.to_device(inp)
+    ref = G.run(lg, q, tok, u, inp.T)
+    hq = q.cpu().pin_memory()
+    if where == "all_pinned":
+        hlg = lg.cpu().pin_memory()
+        htok, hu = tok.cpu().pin_memory(), u.cpu().pin_memory()
+    else:
+        hlg, htok, hu = lg, tok, u
+    status = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    res = sv.spec_verify(hlg, hq, htok, hu, inp.T, status=status)
+    torch.cuda.synchronize()
+    got = {"out_tokens": res.out_tokens.cpu().numpy(), "num_emitted": res.num_emitted.cpu().numpy(),
+           "accept_flags": res.accept_flags.cpu().numpy(), "accept_prob": res.accept_prob.cpu().numpy(),
+           "residual_mass": res.residual_mass.cpu().numpy(), "status": int(status.item())}
+    for k in ("out_tokens", "num_emitted", "accept_flags", "accept_prob", "residual_mass"):
+        assert np.array_equal(got[k], ref[k]), k
+    assert got["status"] == ref["status"]
+    _check(orc, inp, got)
