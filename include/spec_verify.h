@@ -120,6 +120,31 @@ sv_status_t spec_verify(const void *target_logits, sv_dtype_t logits_dtype,
                         int32_t *status_dev, void *workspace,
                         size_t workspace_bytes, void *stream);
 
+/* spec_verify, plus the call's acceptance statistics, counted by the verdict
+ * of every sequence (atomic adds into stats_dev; no extra launch).  What the
+ * pages ask a deployment to record per round -- candidates, accepted
+ * drafts, tokens committed ("推测解码：草稿、验证与实际加速", section
+ * 在相同负载和质量下比较, the table of what to record) -- and what their
+ * engine's acceptance-rate monitor feeds its adaptive draft length ("推测解码
+ * 采样验证优化策略 —— 深度调研报告", part 1 §2, the engine's monitor step and
+ * _adjust_K).  stats_dev: SV_STATS_WORDS(K) uint64 counters in device memory,
+ * 8-byte aligned, added to (zero them to start a window):
+ *   [0] sequences verified          [1] drafts proposed (K per sequence)
+ *   [2] drafts accepted             [3] tokens emitted (accepted + 1)
+ *   [4 + n] sequences that accepted exactly n drafts, n = 0..K
+ * Sequences with bad data (num_emitted = 0) count in none of them.
+ * Returns SV_EINVAL when stats_dev is NULL or misaligned. */
+#define SV_STATS_WORDS(K) (4 + (K) + 1)
+sv_status_t spec_verify_stats(const void *target_logits, sv_dtype_t logits_dtype,
+                              const float *draft_probs, const int32_t *draft_tokens,
+                              const float *uniforms, float temperature, int64_t B,
+                              int32_t K, int32_t V, int32_t *out_tokens,
+                              int32_t *num_emitted, int8_t *accept_flags,
+                              float *accept_prob, float *residual_mass,
+                              int32_t *status_dev, void *workspace,
+                              size_t workspace_bytes, uint64_t *stats_dev,
+                              void *stream);
+
 /* The two stages of spec_verify, for callers that time or schedule them
  * separately.  Same arguments and meaning as spec_verify.
  *

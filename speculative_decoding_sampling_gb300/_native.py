@@ -13,8 +13,13 @@ SV_INTERNAL_TIMEOUT = 32
 SV_MAX_V = 1 << 21
 
 # every function the header declares, in declaration order
-EXPORTS = ["sv_workspace_bytes", "spec_verify", "sv_verify_rows",
+EXPORTS = ["sv_workspace_bytes", "spec_verify", "spec_verify_stats", "sv_verify_rows",
            "sv_sample_survivors", "sv_status_string"]
+
+
+def stats_words(K: int) -> int:
+    """SV_STATS_WORDS(K): the counters spec_verify_stats adds to."""
+    return 4 + K + 1
 
 _VERIFY_ARGTYPES = [
     ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
@@ -46,6 +51,8 @@ def lib() -> ctypes.CDLL:
             fn = getattr(L, name)
             fn.restype = ctypes.c_int
             fn.argtypes = _VERIFY_ARGTYPES
+        L.spec_verify_stats.restype = ctypes.c_int
+        L.spec_verify_stats.argtypes = _VERIFY_ARGTYPES[:-1] + [ctypes.c_void_p, ctypes.c_void_p]
         L.sv_status_string.restype = ctypes.c_char_p
         L.sv_status_string.argtypes = [ctypes.c_int]
         _lib = L

@@ -91,7 +91,7 @@ def _pinned(t: torch.Tensor) -> bool:
 
 def _call(fn_name: str, target_logits, draft_probs, draft_tokens, uniforms,
           temperature, out_tokens, num_emitted, accept_flags, accept_prob,
-          residual_mass, status, workspace, stream):
+          residual_mass, status, workspace, stream, stats=None):
     dev = _exec_device(target_logits)
     if target_logits.dim() != 3:
         raise ValueError("target_logits must be [B, K+1, V]")
@@ -132,12 +132,16 @@ def _call(fn_name: str, target_logits, draft_probs, draft_tokens, uniforms,
         raise ValueError(f"workspace must hold {need} bytes on {dev}")
     if stream is None:
         stream = torch.cuda.current_stream(dev)
-    rc = getattr(N.lib(), fn_name)(
-        target_logits.data_ptr(), dt, _ptr(draft_probs), _ptr(draft_tokens),
-        uniforms.data_ptr(), float(temperature), B, K, V, _ptr(out_tokens),
-        _ptr(num_emitted), _ptr(accept_flags), _ptr(accept_prob),
-        _ptr(residual_mass), _ptr(status), workspace.data_ptr(),
-        workspace.numel() * workspace.element_size(), stream.cuda_stream)
+    args = [target_logits.data_ptr(), dt, _ptr(draft_probs), _ptr(draft_tokens),
+            uniforms.data_ptr(), float(temperature), B, K, V, _ptr(out_tokens),
+            _ptr(num_emitted), _ptr(accept_flags), _ptr(accept_prob),
+            _ptr(residual_mass), _ptr(status), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size()]
+    if stats is not None:
+        _check(stats, "stats", torch.int64, (N.stats_words(K),), dev)
+        fn_name = "spec_verify_stats"
+        args.append(stats.data_ptr())
+    rc = getattr(N.lib(), fn_name)(*args, stream.cuda_stream)
     if rc != N.SV_OK:
         raise SpecVerifyError(rc)
 
@@ -164,7 +168,8 @@ def spec_verify(target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
                 temperature: float, *, want_probs: bool = True,
                 out: dict | None = None, status: torch.Tensor | None = None,
                 workspace: torch.Tensor | None = None,
-                stream: torch.cuda.Stream | None = None) -> SpecVerifyResult:
+                stream: torch.cuda.Stream | None = None,
+                stats: torch.Tensor | None = None) -> SpecVerifyResult:
     """Verify a batch of drafts against target logits on the GPU.
 
     target_logits [B, K+1, V] bf16/fp32; draft_probs [B, K, V] fp32 or None
@@ -174,14 +179,16 @@ def spec_verify(target_logits: torch.Tensor, draft_probs: torch.Tensor | None,
     kernels read in place: a pinned draft_probs sends only the rows the
     draws use (the rejected ones) and the drafted entries over the link.
     `out` may supply preallocated output tensors by name; `status` an int32
-    [1] device tensor that receives SV_BAD_* bits.  Runs asynchronously on
-    `stream` (default: the current stream)."""
+    [1] device tensor that receives SV_BAD_* bits; `stats` an int64
+    [SV_STATS_WORDS(K)] device tensor the verdicts add the call's acceptance
+    counters to (spec_verify_stats).  Runs asynchronously on `stream`
+    (default: the current stream)."""
     o = _outputs(target_logits, want_probs, out)
     if status is not None:
         o["status"] = status
     _call("spec_verify", target_logits, draft_probs, draft_tokens, uniforms,
           temperature, o["out_tokens"], o["num_emitted"], o["accept_flags"],
-          o["accept_prob"], o["residual_mass"], o["status"], workspace, stream)
+          o["accept_prob"], o["residual_mass"], o["status"], workspace, stream, stats)
     return SpecVerifyResult(o["out_tokens"], o["num_emitted"], o["accept_flags"],
                             o["accept_prob"], o["residual_mass"], o["status"])
 

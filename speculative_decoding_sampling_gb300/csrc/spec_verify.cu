@@ -189,7 +189,8 @@ cudaError_t launch(sv::Params P, const Plan &plan, int stages, cudaStream_t stre
 sv_status_t run(int stages, const void *logits, sv_dtype_t dtype, const float *q, const int32_t *tokens,
                 const float *u, float T, int64_t B, int32_t K, int32_t V, int32_t *out_tokens,
                 int32_t *num_emitted, int8_t *accept_flags, float *accept_prob, float *residual_mass,
-                int32_t *status_dev, void *workspace, size_t workspace_bytes, void *stream)
+                int32_t *status_dev, void *workspace, size_t workspace_bytes, void *stream,
+                unsigned long long *stats = nullptr)
 {
     if (B < 0 || K < 0 || V < 1)
         return SV_EINVAL;
@@ -209,7 +210,7 @@ sv_status_t run(int stages, const void *logits, sv_dtype_t dtype, const float *q
     if (!aligned(logits, esize) || (q && !aligned(q, 4)) || (tokens && !aligned(tokens, 4)) ||
         !aligned(u, 4) || !aligned(out_tokens, 4) || !aligned(num_emitted, 4) ||
         (accept_prob && !aligned(accept_prob, 4)) || (residual_mass && !aligned(residual_mass, 4)) ||
-        (status_dev && !aligned(status_dev, 4)) || !aligned(workspace, kAlign))
+        (status_dev && !aligned(status_dev, 4)) || (stats && !aligned(stats, 8)) || !aligned(workspace, kAlign))
         return SV_EINVAL;
     Plan plan;
     if (!make_plan(B, K, V, plan))
@@ -235,6 +236,7 @@ sv_status_t run(int stages, const void *logits, sv_dtype_t dtype, const float *q
     P.accept_prob = accept_prob;
     P.residual_mass = residual_mass;
     P.status = status_dev;
+    P.stats = stats;
     P.row_part = reinterpret_cast<float2 *>(ws + plan.off_part);
     P.row_side = reinterpret_cast<float4 *>(ws + plan.off_row_side);
     P.seq_info = reinterpret_cast<int4 *>(ws + plan.off_seq_info);
@@ -279,6 +281,19 @@ sv_status_t spec_verify(const void *target_logits, sv_dtype_t logits_dtype, cons
     return run(kBoth, target_logits, logits_dtype, draft_probs, draft_tokens, uniforms, temperature, B, K, V,
                out_tokens, num_emitted, accept_flags, accept_prob, residual_mass, status_dev, workspace,
                workspace_bytes, stream);
+}
+
+sv_status_t spec_verify_stats(const void *target_logits, sv_dtype_t logits_dtype, const float *draft_probs,
+                              const int32_t *draft_tokens, const float *uniforms, float temperature, int64_t B,
+                              int32_t K, int32_t V, int32_t *out_tokens, int32_t *num_emitted, int8_t *accept_flags,
+                              float *accept_prob, float *residual_mass, int32_t *status_dev, void *workspace,
+                              size_t workspace_bytes, uint64_t *stats_dev, void *stream)
+{
+    if (!stats_dev)
+        return SV_EINVAL;
+    return run(kBoth, target_logits, logits_dtype, draft_probs, draft_tokens, uniforms, temperature, B, K, V,
+               out_tokens, num_emitted, accept_flags, accept_prob, residual_mass, status_dev, workspace,
+               workspace_bytes, stream, reinterpret_cast<unsigned long long *>(stats_dev));
 }
 
 sv_status_t sv_verify_rows(const void *target_logits, sv_dtype_t logits_dtype, const float *draft_probs,

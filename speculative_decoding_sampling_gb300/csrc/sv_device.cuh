@@ -59,6 +59,7 @@ struct Params {
     float *accept_prob;
     float *residual_mass;
     int32_t *status;
+    unsigned long long *stats; // acceptance statistics (SV_STATS_WORDS(K) counters), or nullptr
     // workspace views; every word is returned to zero by its last reader, so
     // a completed call leaves the whole workspace zero-filled
     float2 *row_part;     // [R * PM]  (max of z, normaliser relative to it) per CTA a row falls in

@@ -115,6 +115,14 @@ __device__ Verdict seq_verdict(const Params &P, int64_t b, int lane, bool write)
                 if (P.status) atomicOr(P.status, bad);
             } else {
                 P.num_emitted[b] = jstar + 1;
+                if (P.stats) { // the call's acceptance statistics (sequences with bad data count in none)
+                    unsigned long long *st = P.stats;
+                    atomicAdd(&st[0], 1ull);
+                    atomicAdd(&st[1], static_cast<unsigned long long>(K));
+                    atomicAdd(&st[2], static_cast<unsigned long long>(jstar));
+                    atomicAdd(&st[3], static_cast<unsigned long long>(jstar + 1));
+                    atomicAdd(&st[4 + jstar], 1ull);
+                }
             }
             P.seq_info[b] = make_int4(bad ? -1 : jstar, __float_as_int(m_sel), __float_as_int(s_sel),
                                       (!DENSE && !bad && jstar < K) ? xsel : -1);

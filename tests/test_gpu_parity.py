@@ -233,3 +233,33 @@ def test_pinned_host_inputs_read_in_place(orc, where):
         assert np.array_equal(got[k], ref[k]), k
     assert got["status"] == ref["status"]
     _check(orc, inp, got)
+
+
+def test_acceptance_statistics_counters(orc):
+    """spec_verify_stats: the verdicts' counters equal those counted from the
+    outputs, add up over calls, and leave out sequences with bad data."""
+    import speculative_decoding_sampling_gb300 as sv
+    from speculative_decoding_sampling_gb300.adaptive import RoundStats, stats_buffer
+    w = synth.WORKLOADS["b8_k4_v32000_bf16"].with_(B=40, V=3000)
+    inp = synth.generate(w, seed=61)
+    inp.u[3, 0] = 1.5                       # a bad uniform: sequence 3 emits nothing
+    lg, q, tok, u = G.to_device(inp)
+    B, K = inp.tokens.shape
+    stats = stats_buffer(K)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    res = sv.spec_verify(lg, q, tok, u, inp.T, status=status, stats=stats)
+    sv.spec_verify(lg, q, tok, u, inp.T, status=status, stats=stats)
+    torch.cuda.synchronize()
+    n = res.num_emitted.cpu().numpy()
+    ok = n > 0
+    assert not ok[3] and ok.sum() == B - 1
+    s = RoundStats.from_counters(stats.cpu())
+    assert s.sequences == 2 * ok.sum()
+    assert s.proposed == 2 * K * ok.sum()
+    assert s.accepted == 2 * (n[ok] - 1).sum()
+    assert s.emitted == 2 * n[ok].sum()
+    assert s.accepted_hist == tuple(2 * int(((n - 1) == a)[ok].sum()) for a in range(K + 1))
+    _check(orc, inp, {"out_tokens": res.out_tokens.cpu().numpy(), "num_emitted": n,
+                      "accept_flags": res.accept_flags.cpu().numpy(),
+                      "accept_prob": res.accept_prob.cpu().numpy(),
+                      "residual_mass": res.residual_mass.cpu().numpy(), "status": int(status.item())})
