@@ -217,8 +217,13 @@ __device__ void final_sequence(const Params &P, int64_t b, FinalSmem &sm, long l
             const float q = __ldcg(&rq[c]);
             s_v[c] = a; // raw; turned into boundary masses below
             reinterpret_cast<float *>(s_v + CPS)[c] = q;
+            ra[c] = 0; // the scratch goes back to zero as soon as it is read
+            rq[c] = 0.0f;
         }
     }
+    const int64_t r0 = b * (static_cast<int64_t>(K) + 1);
+    for (int64_t i = tid; i < (static_cast<int64_t>(K) + 1) * P.PM; i += kFinalThreads)
+        P.row_part[r0 * P.PM + i] = make_float2(0.0f, 0.0f); // not read here
     const int32_t jstar = info.x;
     if (jstar >= 0) {
         const bool rejected = jstar < K;
@@ -255,6 +260,14 @@ __device__ void final_sequence(const Params &P, int64_t b, FinalSmem &sm, long l
         }
         const ScanFirst sr = block_scan_first(T, 0, u, lastc, sm.tot[0], sm.mx[0], sm.first[0]);
         const long long Z = sr.tot;
+        // every thread has read the sequence's info, normaliser and side
+        // data before the scan's barriers
+        for (int32_t j = tid; j <= K; j += kFinalThreads)
+            P.row_side[r0 + j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (tid == 0) {
+            P.seq_E[b] = 0;
+            P.seq_info[b] = make_int4(0, 0, 0, 0);
+        }
         int32_t tok = -1;
         const bool degenerate = rejected && !(Z > 0);
         if (degenerate) {
@@ -363,21 +376,15 @@ __device__ void final_sequence(const Params &P, int64_t b, FinalSmem &sm, long l
             if (degenerate && P.status)
                 atomicOr(P.status, kDegenerate);
         }
-    }
-    // the sequence is done: return its scratch to zero
-    __syncthreads();
-    for (int32_t c = tid; c < CPS; c += kFinalThreads) {
-        ra[c] = 0;
-        rq[c] = 0.0f;
-    }
-    const int64_t r0 = b * (static_cast<int64_t>(K) + 1);
-    for (int64_t i = tid; i < (static_cast<int64_t>(K) + 1) * P.PM; i += kFinalThreads)
-        P.row_part[r0 * P.PM + i] = make_float2(0.0f, 0.0f);
-    for (int32_t j = tid; j <= K; j += kFinalThreads)
-        P.row_side[r0 + j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if (tid == 0) {
-        P.seq_E[b] = 0;
-        P.seq_info[b] = make_int4(0, 0, 0, 0);
+    } else {
+        // a sequence with bad data: nothing to draw, only scratch to clear
+        __syncthreads(); // every thread has read the info
+        for (int32_t j = tid; j <= K; j += kFinalThreads)
+            P.row_side[r0 + j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (tid == 0) {
+            P.seq_E[b] = 0;
+            P.seq_info[b] = make_int4(0, 0, 0, 0);
+        }
     }
     __syncthreads(); // the block's scratch is reused by the next sequence
 }
