@@ -85,7 +85,8 @@ __device__ __forceinline__ int block_max(int v, int *si)
 // Block-wide inclusive scan of one int64 per thread (thread order) fused
 // with the search for the first thread whose prefix exceeds a threshold and
 // the maximum of `mx` over the block: two barriers.  The threshold is `thr`,
-// or floor(u * total) when `u` is not negative.  Each call site passes its
+// or floor(u * total) when `u` is not negative.  With `s_excl`, every
+// thread's exclusive prefix is left there, visible after the call.  Each call site passes its
 // own scratch, so no barrier is needed after the call.
 struct ScanFirst {
     long long incl, tot, thr;
@@ -93,7 +94,7 @@ struct ScanFirst {
 };
 
 __device__ __forceinline__ ScanFirst block_scan_first(long long v, long long thr, float u, int mx, long long *s_tot,
-                                                      int *s_mx, int *s_first)
+                                                      int *s_mx, int *s_first, long long *s_excl = nullptr)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     ScanFirst r;
@@ -116,6 +117,8 @@ __device__ __forceinline__ ScanFirst block_scan_first(long long v, long long thr
         r.mx = max(r.mx, s_mx[w]);
     }
     r.incl += off;
+    if (s_excl) // each thread's exclusive prefix, for the search after the call
+        s_excl[threadIdx.x] = r.incl - v;
     r.thr = u >= 0.0f ? mul_floor(u, r.tot) : thr;
     const unsigned m = __ballot_sync(0xFFFFFFFFu, r.incl > r.thr);
     if (lane == 0)
@@ -191,8 +194,7 @@ struct FinalSmem {
     long long tot[2][kFinalWarps];
     int mx[2][kFinalWarps];
     int first[2][kFinalWarps];
-    long long before;
-    int sel;
+    long long excl[kFinalThreads];
 };
 
 // The final draw of sequence b and the return of its scratch to zero.
@@ -258,7 +260,7 @@ __device__ void final_sequence(const Params &P, int64_t b, FinalSmem &sm, long l
                     lastc = c;
             }
         }
-        const ScanFirst sr = block_scan_first(T, 0, u, lastc, sm.tot[0], sm.mx[0], sm.first[0]);
+        const ScanFirst sr = block_scan_first(T, 0, u, lastc, sm.tot[0], sm.mx[0], sm.first[0], sm.excl);
         const long long Z = sr.tot;
         // every thread has read the sequence's info, normaliser and side
         // data before the scan's barriers
@@ -297,25 +299,24 @@ __device__ void final_sequence(const Params &P, int64_t b, FinalSmem &sm, long l
                 tok = last_pos;
         } else {
             const long long t = sr.thr;
-            if (tid == sr.first) {
-                long long acc = sr.incl - T;
-                int c_sel = -1;
-                for (int i = 0; i < R && c_sel < 0; ++i) {
-                    const int c = tid * R + i;
+            // every thread walks the chosen thread's chunks itself (the
+            // records and the prefixes are in shared memory): no barrier
+            int32_t sel = -1;
+            long long acc = 0;
+            if (sr.first < kFinalThreads) {
+                acc = sm.excl[sr.first];
+                for (int i = 0; i < R && sel < 0; ++i) {
+                    const int c = sr.first * R + i;
                     if (c < CPS) {
                         const long long vc = s_v[c];
                         if (vc > 0 && acc + vc > t)
-                            c_sel = c;
+                            sel = c;
                         else
                             acc += vc;
                     }
                 }
-                sm.sel = c_sel;
-                sm.before = acc;
             }
-            __syncthreads();
-            int32_t sel = sr.first < kFinalThreads ? sm.sel : -1;
-            long long rem = t - sm.before;
+            long long rem = t - acc;
             if (sel < 0) { // rounding put the draw past the last chunk: take its last id
                 sel = sr.mx;
                 rem = LLONG_MAX;
@@ -342,18 +343,20 @@ __device__ void final_sequence(const Params &P, int64_t b, FinalSmem &sm, long l
                     // running sums in id order (the group's last boundary is
                     // its total, so an id past rounding falls back to its last
                     // id of positive mass)
+                    // (all 8 boundaries formed independently, the first
+                    // passing one taken)
                     const long long excl = gr.incl - Lg;
-                    int32_t tk = g * kGroup + (kpos >= 0 ? kpos : 0);
                     float cw = 0.0f, cq = 0.0f;
+                    unsigned hit = 0u;
+#pragma unroll
                     for (int k = 0; k < kGroup; ++k) {
                         cw = __fadd_rn(cw, w[k]);
                         cq = __fadd_rn(cq, qp[k]);
-                        if (w[k] > 0.0f && excl + to_fixed(cw, X.fb) - corr_of(delta, cq) > rem) {
-                            tk = g * kGroup + k;
-                            break;
-                        }
+                        if (w[k] > 0.0f && excl + to_fixed(cw, X.fb) - corr_of(delta, cq) > rem)
+                            hit |= 1u << k;
                     }
-                    P.out_tokens[b * (K + 1) + jstar] = tk;
+                    P.out_tokens[b * (K + 1) + jstar] =
+                        g * kGroup + (hit ? __ffs(hit) - 1 : (kpos >= 0 ? kpos : 0));
                 } else if (gr.first == kFinalThreads && tid == 0) {
                     P.out_tokens[b * (K + 1) + jstar] = gr.mx; // the chunk's last id of positive mass
                 }
