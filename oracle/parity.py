@@ -21,6 +21,8 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
+from . import ORC_DEGENERATE_RESIDUAL as _DEGENERATE
+
 TOL_PROB = 1e-5
 WINDOW = 1e-5
 MAX_EXCUSED_FRACTION = 1e-4
@@ -109,7 +111,9 @@ def _check_sequence(orc, logits, q, tokens, u, T, cand, b, ores, oi, rep, depth,
     c_prob = cand.get("accept_prob")
     c_mass = cand.get("residual_mass")
 
-    if ores.status[oi] != 0:
+    # bad data (every bit but the degenerate-residual report, which still
+    # emits its tokens): the sequence emits nothing
+    if int(ores.status[oi]) & ~_DEGENERATE:
         if not (c_n == 0 and (c_tok == -1).all() and
                 (c_flags is None or (c_flags == -1).all())):
             rep.failures.append((b, "invalid sequence emitted tokens", int(ores.status[oi])))

@@ -35,7 +35,7 @@ struct Plan {
     int32_t PM;   // row_part slots per row
     int32_t CPS;  // final-draw chunks per sequence
     int32_t fix;  // fractional bits of the fixed-point masses
-    size_t off_part, off_row_side, off_seq_info, off_seqE, off_rec_a, off_rec_q, bytes;
+    size_t off_part, off_row_side, off_seq_info, off_seqE, off_cnt, off_rec_a, off_rec_q, bytes;
 };
 
 bool make_plan(int64_t B, int32_t K, int32_t V, Plan &p)
@@ -59,6 +59,7 @@ bool make_plan(int64_t B, int32_t K, int32_t V, Plan &p)
     p.off_row_side = off; off = align_up(off + R * sizeof(float4));
     p.off_seq_info = off; off = align_up(off + Bz * sizeof(int4));
     p.off_seqE = off;     off = align_up(off + Bz * sizeof(long long));
+    p.off_cnt = off;      off = align_up(off + Bz * sizeof(uint32_t));
     p.off_rec_a = off;    off = align_up(off + Bz * p.CPS * sizeof(long long));
     p.off_rec_q = off;    off = align_up(off + Bz * p.CPS * sizeof(float));
     p.bytes = off;
@@ -155,6 +156,13 @@ cudaError_t launch(sv::Params P, const Plan &plan, int stages, cudaStream_t stre
     if (stages & kSurvivors) {
         // at least one chunk per warp
         const int64_t grid = clamp_grid(ceil_div(P.NC, sv::kDrawWarps), res.draw);
+        // a stream that fills every SM, with at least as many draw warps as
+        // sequences: each sequence has its own warps, and the last of them
+        // makes its final draw (no final kernel, whose CTAs would only be
+        // placed once the stream's CTAs leave).  A smaller stream leaves SMs
+        // free, where the final kernel's CTAs wait for it and draw with
+        // block-wide scans, sooner than one warp can.
+        P.inline_final = grid == res.draw && grid * sv::kDrawWarps >= P.B ? 1 : 0;
         // programmatic dependent launch: the draw's CTAs may be scheduled
         // while the row pass drains; they wait in griddepcontrol.wait for
         // its completion before reading anything it wrote
@@ -171,6 +179,8 @@ cudaError_t launch(sv::Params P, const Plan &plan, int stages, cudaStream_t stre
         e = cudaLaunchKernelEx(&cfg, sv::survivor_kernel<LT, DENSE>, P);
         if (e != cudaSuccess)
             return e;
+        if (P.inline_final)
+            return cudaSuccess;
         // the final draws: one CTA per sequence, chained the same way
         cudaLaunchConfig_t fcfg = {};
         fcfg.gridDim = dim3(static_cast<unsigned>(P.B < 0x7FFFFFFF ? P.B : 0x7FFFFFFF));
@@ -241,6 +251,8 @@ sv_status_t run(int stages, const void *logits, sv_dtype_t dtype, const float *q
     P.row_side = reinterpret_cast<float4 *>(ws + plan.off_row_side);
     P.seq_info = reinterpret_cast<int4 *>(ws + plan.off_seq_info);
     P.seq_E = reinterpret_cast<long long *>(ws + plan.off_seqE);
+    P.seq_cnt = reinterpret_cast<uint32_t *>(ws + plan.off_cnt);
+    P.inline_final = 0;
     P.rec_a = reinterpret_cast<long long *>(ws + plan.off_rec_a);
     P.rec_q = reinterpret_cast<float *>(ws + plan.off_rec_q);
     P.PM = plan.PM;

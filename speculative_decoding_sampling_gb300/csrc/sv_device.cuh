@@ -67,6 +67,7 @@ struct Params {
     int4 *seq_info;       // [B]       the verdict for the final kernel: j* (-1 = bad sequence), bits of the
                           //           surviving row's max m and normaliser s, the rejected draft x (one-hot) or -1
     long long *seq_E;     // [B]       exact sum of pt over the surviving row (dense), 2^-fix_bits units
+    uint32_t *seq_cnt;    // [B]       draw-stream chunks of the sequence folded so far (inline final draws)
     long long *rec_a;     // [B * CPS] per chunk: mass A, 2^-fix_bits units
     float *rec_q;         // [B * CPS] per chunk: Qp
     int64_t total;        // R * V elements of the logits
@@ -78,6 +79,7 @@ struct Params {
     int32_t CPS;          // final-draw chunks per sequence
     int64_t NC;           // final-draw chunks of the call, B * CPS
     int32_t ring_ok;      // rows of whole 16-byte aligned groups: the draw streams through its rings
+    int32_t inline_final; // every sequence has its own draw warps, the last of which makes its final draw
     int32_t fix_bits;     // fractional bits of the fixed-point masses
 };
 

@@ -404,4 +404,332 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const Params P)
         final_sequence<LT, DENSE>(P, b, sm, s_v);
 }
 
+// ---------------------------------------------------------------------------
+// The final draw inside the draw stream.  When every sequence has its own
+// group of draw warps, the warp that completes a sequence's chunk count
+// draws its token: a warp scan over the chunk records (each lane a
+// contiguous run of chunks) picks the chunk, the chunk is staged in the
+// warp's idle ring (each lane its own groups 32 t + lane, as in the stream),
+// and a warp scan over its groups, tile by tile, picks the group and then the
+// id -- the same exact boundaries as the final kernel.
+
+// The chunk of a row holding boundary floor(u * Z) among the chunk masses
+// `mass(c)`, each lane a contiguous run of chunks (up to 8 kept in
+// registers): sets sel (the row's last chunk of positive mass, with before =
+// LLONG_MIN, when rounding puts the boundary past the last chunk; -1 when
+// every mass is 0), the mass before it and the boundary; returns the total Z.
+// Warp-collective.
+template <typename Mass>
+__device__ long long chunk_select(int32_t nc, float u, Mass mass, int lane, int32_t &sel, long long &before,
+                                  long long &thr)
+{
+    constexpr int kRegs = 8;
+    const int32_t R = (nc + 31) / 32;
+    const int32_t c_lo = min(nc, lane * R), c_hi = min(nc, c_lo + R);
+    long long vr[kRegs];
+#pragma unroll
+    for (int i = 0; i < kRegs; ++i)
+        vr[i] = c_lo + i < c_hi ? mass(c_lo + i) : 0;
+    long long T = 0;
+    int32_t lastc = -1;
+#pragma unroll
+    for (int i = 0; i < kRegs; ++i) {
+        T += vr[i];
+        if (vr[i] > 0)
+            lastc = c_lo + i;
+    }
+    for (int32_t c = c_lo + kRegs; c < c_hi; ++c) {
+        const long long vc = mass(c);
+        T += vc;
+        if (vc > 0)
+            lastc = c;
+    }
+    const long long incl = warp_incl_scan_ll(T, lane);
+    const long long Z = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    thr = mul_floor(u, Z);
+    const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl > thr);
+    const int32_t last_all = __reduce_max_sync(0xFFFFFFFFu, lastc);
+    if (!hit) {
+        sel = last_all;
+        before = LLONG_MIN;
+        return Z;
+    }
+    const int src = __ffs(hit) - 1;
+    int32_t s = -1;
+    long long acc = incl - T;
+#pragma unroll
+    for (int i = 0; i < kRegs; ++i) {
+        if (s < 0 && c_lo + i < c_hi) {
+            if (vr[i] > 0 && acc + vr[i] > thr)
+                s = c_lo + i;
+            else
+                acc += vr[i];
+        }
+    }
+    if (lane == src) {
+        for (int32_t c = c_lo + kRegs; s < 0 && c < c_hi; ++c) {
+            const long long vc = mass(c);
+            if (vc > 0 && acc + vc > thr)
+                s = c;
+            else
+                acc += vc;
+        }
+    }
+    sel = __shfl_sync(0xFFFFFFFFu, s, src);
+    before = __shfl_sync(0xFFFFFFFFu, acc, src);
+    if (sel < 0) { // not reached with exact running sums; kept as the final kernel's fallback
+        sel = last_all;
+        before = LLONG_MIN;
+    }
+    return Z;
+}
+
+// Stage chunk `sel` of a row (and of its draft row, WANT_Q) in ring stage
+// `st`, in the stream's layout; lane l fetches (and later reads) groups
+// 32 t + l.  RING: 16-byte async copies; otherwise element loads and shared
+// stores.
+template <typename LT, bool WANT_Q, bool RING>
+__device__ __forceinline__ void fetch_chunk(const LT *row, const float *qrow, int32_t sel, int32_t V, bool vec_ok,
+                                            int lane, uint8_t *st)
+{
+    constexpr int LB = kGroup * static_cast<int>(sizeof(LT));
+    const int32_t ng = (V + kGroup - 1) / kGroup;
+#pragma unroll
+    for (int t = 0; t < kChunkTiles; ++t) {
+        const int gl = 32 * t + lane;
+        const int32_t g = sel * kChunkGroups + gl;
+        if (g < ng) {
+            if constexpr (RING) {
+                const uint8_t *src = reinterpret_cast<const uint8_t *>(row + static_cast<int64_t>(g) * kGroup);
+#pragma unroll
+                for (int h = 0; h < LB; h += 16)
+                    cp_async16(st + gl * LB + h, src + h);
+                if (WANT_Q) {
+                    const uint8_t *qsrc = reinterpret_cast<const uint8_t *>(qrow + static_cast<int64_t>(g) * kGroup);
+                    cp_async16(st + kChunkGroups * LB + gl * 32, qsrc);
+                    cp_async16(st + kChunkGroups * LB + gl * 32 + 16, qsrc + 16);
+                }
+            } else {
+                float z[kGroup], q[kGroup];
+                load_group<LT, WANT_Q>(row, qrow, g, ng, V, vec_ok, z, q);
+#pragma unroll
+                for (int k = 0; k < kGroup; ++k) {
+                    if constexpr (sizeof(LT) == 2)
+                        reinterpret_cast<uint16_t *>(st + gl * LB)[k] =
+                            static_cast<uint16_t>(__float_as_uint(z[k]) >> 16); // exact: z came from bf16
+                    else
+                        reinterpret_cast<float *>(st + gl * LB)[k] = z[k];
+                    if (WANT_Q)
+                        reinterpret_cast<float *>(st + kChunkGroups * LB + gl * 32)[k] = q[k];
+                }
+            }
+        }
+    }
+    if constexpr (RING) {
+        cp_async_commit();
+        cp_async_wait<0>();
+    }
+    __syncwarp(); // the scan reads other lanes' groups
+}
+
+// The id of the staged chunk `sel` whose boundary first exceeds `rem`
+// (boundaries relative to the chunk's start), or the chunk's last id of
+// positive mass when none does.  Each lane forms the group values of its own
+// groups 32 t + lane into `sL` (128 entries of shared scratch), then takes
+// four consecutive ones, 4 lane .. 4 lane + 3, for a single warp scan; the
+// lane holding the first group whose running sum passes `rem` searches its
+// ids.  Warp-collective.
+template <typename LT, bool WANT_Q, int MODE, bool NORM>
+__device__ int32_t chunk_id_scan_stage(const uint8_t *st, int32_t sel, int32_t V, const SurvArgs &X, float delta,
+                                       long long rem, int lane, long long *sL)
+{
+    const int32_t ng = (V + kGroup - 1) / kGroup;
+    const int32_t gbase = sel * kChunkGroups;
+    int lastid = -1;
+#pragma unroll 1
+    for (int t = 0; t < kChunkTiles; ++t) {
+        const int gl = 32 * t + lane;
+        const int32_t g = gbase + gl;
+        float z[kGroup], q[kGroup];
+        load_group_smem<LT, WANT_Q>(st, gl, g < ng, z, q);
+        unsigned long long pt2[kGroup / 2];
+        float w[kGroup], qp[kGroup], ws, qs;
+        group_masses<MODE, NORM>(z, q, g * kGroup, X, pt2, w, qp, ws, qs);
+        sL[gl] = to_fixed(ws, X.fb) - corr_of(delta, qs);
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k)
+            if (w[k] > 0.0f)
+                lastid = g * kGroup + k;
+    }
+    __syncwarp();
+    static_assert(kChunkGroups == 4 * 32, "four consecutive groups per lane");
+    long long L[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        L[i] = sL[4 * lane + i];
+    const long long T = (L[0] + L[1]) + (L[2] + L[3]);
+    const long long incl = warp_incl_scan_ll(T, lane);
+    // the first of the lane's groups whose running sum passes rem
+    long long run = incl - T;
+    int hit_i = -1;
+    long long excl_hit = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (hit_i < 0 && run + L[i] > rem) {
+            hit_i = i;
+            excl_hit = run;
+        }
+        run += L[i];
+    }
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, hit_i >= 0);
+    if (!m)
+        return __reduce_max_sync(0xFFFFFFFFu, lastid);
+    const int hl = __ffs(m) - 1;
+    int32_t tok = -1;
+    if (lane == hl) {
+        // running sums in id order (the group's last boundary is its total,
+        // so an id past rounding falls back to its last id of positive mass)
+        const int gl = 4 * lane + hit_i;
+        const int32_t g = gbase + gl;
+        float z[kGroup], q[kGroup];
+        load_group_smem<LT, WANT_Q>(st, gl, g < ng, z, q);
+        unsigned long long pt2[kGroup / 2];
+        float w[kGroup], qp[kGroup], ws, qs;
+        group_masses<MODE, NORM>(z, q, g * kGroup, X, pt2, w, qp, ws, qs);
+        int kpos = 0;
+        float cw = 0.0f, cq = 0.0f;
+        unsigned hitk = 0u;
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) {
+            if (w[k] > 0.0f)
+                kpos = k;
+            cw = __fadd_rn(cw, w[k]);
+            cq = __fadd_rn(cq, qp[k]);
+            if (w[k] > 0.0f && excl_hit + to_fixed(cw, X.fb) - corr_of(delta, cq) > rem)
+                hitk |= 1u << k;
+        }
+        tok = g * kGroup + (hitk ? __ffs(hitk) - 1 : kpos);
+    }
+    return __shfl_sync(0xFFFFFFFFu, tok, hl);
+}
+
+template <typename LT, bool DENSE, bool RING>
+__device__ void final_inline(const Params &P, int64_t b, const Verdict &v, int lane, uint8_t *stage)
+{
+    const int32_t K = P.K, V = P.V, CPS = P.CPS;
+    long long *ra = P.rec_a + b * CPS;
+    float *rq = P.rec_q + b * CPS;
+    // the group values of the chosen chunk: in the ring's second stage
+    long long *sL = reinterpret_cast<long long *>(stage + DrawShape<LT, DENSE>::kChunkBytes);
+    // the sequence's scratch goes back to zero once it has been read (every
+    // lane's loads of it have been consumed by the warp's shuffles first)
+    auto zero_scratch = [&]() {
+        __syncwarp();
+        for (int32_t c = lane; c < CPS; c += 32) {
+            ra[c] = 0;
+            rq[c] = 0.0f;
+        }
+        const int64_t r0 = b * (static_cast<int64_t>(K) + 1);
+        for (int64_t i = lane; i < (static_cast<int64_t>(K) + 1) * P.PM; i += 32)
+            P.row_part[r0 * P.PM + i] = make_float2(0.0f, 0.0f);
+        for (int32_t j = lane; j <= K; j += 32)
+            P.row_side[r0 + j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (lane == 0) {
+            P.seq_E[b] = 0;
+            P.seq_info[b] = make_int4(0, 0, 0, 0);
+            P.seq_cnt[b] = 0u;
+        }
+    };
+    const int32_t jstar = v.jstar;
+    if (jstar < 0) { // a sequence with bad data: nothing to draw
+        zero_scratch();
+        return;
+    }
+    const bool rejected = jstar < K;
+    const LT *row;
+    const float *qrow;
+    seq_rows<LT, DENSE>(P, b, v, row, qrow);
+    const SurvArgs X = surv_args(P, v);
+    const bool vec_ok = (reinterpret_cast<uintptr_t>(row) & 15u) == 0 &&
+                        (qrow == nullptr || (reinterpret_cast<uintptr_t>(qrow) & 15u) == 0);
+    const float u = __ldg(&P.u[b * (K + 1) + K]);
+    // dense: delta = E - 2^fb = (S' - 1) 2^fb, S' the exact sum of pt;
+    // one-hot: the residual's mass is 1 - p(x), p(x) as the accept test
+    // took it (z(x) from the row pass's side data)
+    const long long E = rejected && DENSE ? static_cast<long long>(__ldcg(&P.seq_E[b])) : 0;
+    const float zx = rejected && !DENSE && lane == 0 ? __ldcg(&P.row_side[b * (K + 1) + jstar]).y : 0.0f;
+    const float delta = rejected && DENSE ? static_cast<float>(E - (1ll << P.fix_bits)) : 0.0f;
+    int32_t sel;
+    long long before, thr;
+    const long long Z = chunk_select(
+        CPS, u, [&](int32_t c) { return rec_value(__ldcg(&ra[c]), __ldcg(&rq[c]), delta); }, lane, sel, before, thr);
+    const bool degenerate = rejected && !(Z > 0);
+    if (lane == 0) {
+        if (P.residual_mass) {
+            float rm = 0.0f;
+            if (rejected && !degenerate) {
+                if (DENSE) // Z / 2^fb over the residual's normaliser S'
+                    rm = E > 0 ? __fdiv_rn(static_cast<float>(Z), static_cast<float>(E)) : 0.0f;
+                else
+                    rm = __fsub_rn(1.0f, __fdiv_rn(term(zx, X.c, X.mc), v.s));
+            }
+            P.residual_mass[b] = rm;
+        }
+        if (degenerate && P.status)
+            atomicOr(P.status, kDegenerate);
+    }
+    zero_scratch();
+    int32_t tok = -1;
+    constexpr int MODE = LaunchMode<DENSE>::value;
+    if (degenerate) {
+        // residual of zero mass after a rejection (impossible in exact
+        // arithmetic): draw from p of the same row instead -- the chunk
+        // masses of p one chunk at a time, then the chosen chunk's ids
+        SurvArgs Xb = X;
+        Xb.x = -1;
+        const int32_t ng = (V + kGroup - 1) / kGroup;
+        auto chunk_mass = [&](int32_t c) {
+            fetch_chunk<LT, false, RING>(row, nullptr, c, V, vec_ok, lane, stage);
+            long long A = 0;
+#pragma unroll 1
+            for (int t = 0; t < kChunkTiles; ++t) {
+                const int gl = 32 * t + lane;
+                const int32_t g = c * kChunkGroups + gl;
+                float z[kGroup], q[kGroup];
+                load_group_smem<LT, false>(stage, gl, g < ng, z, q);
+                unsigned long long pt2[kGroup / 2];
+                float w[kGroup], qp[kGroup], ws, qs;
+                group_masses<kModeBonus, false>(z, q, g * kGroup, Xb, pt2, w, qp, ws, qs);
+                A += to_fixed(ws, Xb.fb);
+            }
+            return warp_sum_ll(A);
+        };
+        long long Zp = 0;
+        for (int32_t c = 0; c < CPS; ++c)
+            Zp += chunk_mass(c);
+        const long long t = mul_floor(u, Zp);
+        long long acc = 0;
+        int32_t c = 0;
+        for (; c < CPS - 1; ++c) {
+            const long long m = chunk_mass(c);
+            if (m > 0 && acc + m > t)
+                break;
+            acc += m;
+        }
+        fetch_chunk<LT, false, RING>(row, nullptr, c, V, vec_ok, lane, stage);
+        tok = chunk_id_scan_stage<LT, false, kModeBonus, false>(stage, c, V, Xb, 0.0f, t - acc, lane, sL);
+    } else if (sel >= 0) {
+        const long long rem = before == LLONG_MIN ? LLONG_MAX : thr - before;
+        if (DENSE && qrow != nullptr) {
+            fetch_chunk<LT, true, RING>(row, qrow, sel, V, vec_ok, lane, stage);
+            tok = chunk_id_scan_stage<LT, true, MODE, DENSE>(stage, sel, V, X, delta, rem, lane, sL);
+        } else {
+            fetch_chunk<LT, false, RING>(row, nullptr, sel, V, vec_ok, lane, stage);
+            tok = chunk_id_scan_stage<LT, false, MODE, DENSE>(stage, sel, V, X, delta, rem, lane, sL);
+        }
+    }
+    if (lane == 0)
+        P.out_tokens[b * (K + 1) + jstar] = tok;
+}
+
 } // namespace sv

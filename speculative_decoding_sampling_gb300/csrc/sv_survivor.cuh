@@ -304,6 +304,11 @@ __device__ __forceinline__ void fold_group(const float (&z)[kGroup], const float
     }
 }
 
+// The final draw of sequence b by the draw warp that completes its chunk
+// count, staging the chosen chunk in ring stage `stage` (sv_final.cuh).
+template <typename LT, bool DENSE, bool RING>
+__device__ void final_inline(const Params &P, int64_t b, const Verdict &v, int lane, uint8_t *stage);
+
 // What a ring stage's consumer needs about the chunk's sequence: written by
 // the issue side (which computed the verdict) when it issues the chunk.
 struct StageInfo {
@@ -384,6 +389,8 @@ __device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t 
     int cst = 0;      // ring stage of chunk k
     int64_t cur = -1; // sequence whose totals are being accumulated
     SurvArgs X = {};
+    Verdict cv = {-1, 0.0f, 1.0f, -1};
+    int32_t ccount = 0; // chunks of `cur` folded by this warp
     bool cvalid = false, cdraft = false, cvec = false;
     const LT *crow = nullptr;
     const float *cq = nullptr;
@@ -420,6 +427,7 @@ __device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t 
             __syncwarp();
             const StageInfo si = info[cst];
             const Verdict v = {si.jstar, si.m, si.s, si.x};
+            cv = v;
             seq_rows<LT, DENSE>(P, cb, v, crow, cq);
             X = surv_args(P, v);
             cvalid = v.jstar >= 0;
@@ -466,6 +474,7 @@ __device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t 
             P.rec_a[cb * CPS + ccis] = at;
             P.rec_q[cb * CPS + ccis] = qt;
         }
+        ++ccount;
         cst = cst + 1 == kDrawStages ? 0 : cst + 1;
         if (++ccis == CPS) {
             ccis = 0;
@@ -475,6 +484,21 @@ __device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t 
     if (RING)
         cp_async_wait<0>();
     flush();
+    if (P.inline_final) {
+        // the range held chunks of one sequence only: count them in
+        // (release: this warp's records and normaliser share first); the warp
+        // completing the count (acquire: everyone else's) makes the draw,
+        // staging its chunk in the now idle ring
+        uint32_t last = 0;
+        if (lane == 0) {
+            const uint32_t old = atom_add_acq_rel(&P.seq_cnt[cur], static_cast<uint32_t>(ccount));
+            last = old + static_cast<uint32_t>(ccount) == static_cast<uint32_t>(CPS);
+        }
+        if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
+            __syncwarp();
+            final_inline<LT, DENSE, RING>(P, cur, cv, lane, ring);
+        }
+    }
 }
 
 // The draw stream.  Each warp takes a contiguous range of the call's chunks

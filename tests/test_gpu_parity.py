@@ -102,6 +102,49 @@ def test_p_equals_q_all_accepted(orc):
     _check(orc, inp, cand)
 
 
+@pytest.mark.parametrize("V", [128000, 128001], ids=["whole_groups", "ragged"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("onehot", [False, True], ids=["dense", "onehot"])
+def test_stream_filling_shapes(orc, V, dtype, onehot):
+    """Enough chunks (B = 24, about 125 a sequence) for the draw stream to
+    fill every SM while each sequence keeps its own warps: the last of them
+    makes the sequence's final draw.  An odd V puts rows off 16-byte
+    boundaries, so the chunks are loaded element by element."""
+    base = synth.WORKLOADS["b8_k4_v32000_bf16"]
+    w = base.with_(name="fill", B=24, K=3, V=V, dtype=dtype,
+                   Tq=0.0 if onehot else 0.8, onehot_p=0.5 if onehot else 0.0)
+    inp = synth.generate(w, seed=31 + V % 7)
+    cand = G.run_inputs(inp)
+    assert cand["status"] == 0
+    _check(orc, inp, cand)
+
+
+@pytest.mark.parametrize("B,V", [(8, 777), (16, 128000)])
+def test_degenerate_residual_draws_from_p(orc, B, V):
+    """q = 1.001 p at every id (q is not renormalised): the first draft is
+    rejected once u >= 1/1.001, max(p - q, 0) is 0 everywhere, so the token
+    is drawn from p itself and the status says so.  The larger shape fills
+    the draw stream, which then makes the final draw itself; the smaller one
+    leaves it to the final pass."""
+    import speculative_decoding_sampling_gb300 as sv
+    K, T = 2, 1.0
+    rng = np.random.default_rng(21)
+    logits = rng.normal(0.0, 2.0, (B, K + 1, V)).astype(np.float32)
+    z = logits.astype(np.float64) / T
+    p = np.exp(z - z.max(-1, keepdims=True))
+    p /= p.sum(-1, keepdims=True)
+    q = (p[:, :K] * 1.001).astype(np.float32)
+    tok = rng.integers(0, V, (B, K)).astype(np.int32)
+    u = rng.random((B, K + 1)).astype(np.float32)
+    u[:, 0] = 0.9995
+    inp = synth.Inputs(None, logits, q, tok, u, T)
+    cand = G.run_inputs(inp)
+    assert cand["status"] == sv.SV_DEGENERATE_RESIDUAL, cand["status"]
+    assert (cand["num_emitted"] == 1).all()
+    assert (cand["residual_mass"] == 0.0).all()
+    _check(orc, inp, cand)
+
+
 def test_bad_inputs_report_and_emit_nothing(orc):
     """Bad data sets status bits, that sequence emits nothing, others are unaffected."""
     import speculative_decoding_sampling_gb300 as sv
