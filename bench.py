@@ -1,9 +1,10 @@
 #!/usr/bin/env python3
 """Benchmark of the speculative-sampling verification step on GB300.
 
-One step = one spec_verify call over a whole batch: three launches, the row
-pass (rows_kernel), the draw stream (survivor_kernel) and the final draws
-(final_kernel), with inputs resident in HBM.  Prints ONE JSON line on rank 0.
+One step = one spec_verify call over a whole batch: the row pass
+(rows_kernel), the draw stream (survivor_kernel) and, when the draw stream
+does not fill the GPU, the final draws (final_kernel); inputs resident in
+HBM.  Prints ONE JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle, timed on the host
@@ -206,9 +207,9 @@ def run_gpu(args):
     cargs = args_for(d_logits, d_q, d_tok, d_u, out)
 
     def step(s):
-        # one call = the three launches of the path (row pass, draw stream,
-        # final draws), each chained to the one before by programmatic
-        # dependent launch
+        # one call = the launches of the path (row pass, draw stream and,
+        # unless the draw stream makes them, the final draws), each chained
+        # to the one before by programmatic dependent launch
         rc = lib.spec_verify(*cargs[:-1], s.cuda_stream)
         if rc:
             raise RuntimeError(sv.sv_status_string(rc))
@@ -235,6 +236,22 @@ def run_gpu(args):
         step(stream)
     barrier()
 
+    # bytes one step reads: every logit, the surviving rows again, the
+    # rejected rows' draft probabilities.  Below twice the L2 size, the L2 is
+    # flushed before every timed step, outside the timed events, so no step
+    # finds its inputs cached by the step before.
+    touched = algorithmic_bytes(w, out["num_emitted"].cpu().numpy())["total"]
+    flush_l2 = {"auto": touched < 2 * L2_BYTES, "on": True, "off": False}[args.l2_flush]
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev) if flush_l2 else None
+
+    def flush(s):
+        # write a buffer of twice the L2: no input of the step stays cached
+        if flush_buf is not None:
+            with torch.cuda.stream(s):
+                flush_buf.fill_(1)
+    launches_per_step = sv.sv_kernel_launches(
+        torch.bfloat16 if w.dtype == "bf16" else torch.float32, d_q is not None, B, K, V)
+
     # the public call captured in CUDA graphs, GRAPH_STEPS consecutive calls
     # (steps) per graph plus a one-call graph for the remainder: the timed
     # region replays them, so host launch overhead and the gap between graph
@@ -251,22 +268,35 @@ def run_gpu(args):
     graph1.replay()
     barrier()
 
-    # ---- timed region: exactly K steps of the public call (graph replays)
+    # ---- timed region: exactly K steps of the public call (graph replays;
+    # with the L2 flush, eager calls, each between its own events)
     clocks = ClockSampler(local)
     clocks.start()
     barrier()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(gstream):
-        t_start.record(gstream)
-        for _ in range(args.steps // GRAPH_STEPS):
-            graph.replay()
-        for _ in range(args.steps % GRAPH_STEPS):
-            graph1.replay()
-        t_end.record(gstream)
-    barrier()
-    ms_total = t_start.elapsed_time(t_end)
-    ms_step = ms_total / args.steps
+    if flush_l2:
+        tev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        # eager calls: the host enqueues each call while the flush before it
+        # runs, so the events see the call's device time alone
+        for e0, e1 in tev:
+            flush(stream)
+            e0.record(stream)
+            step(stream)
+            e1.record(stream)
+        barrier()
+        ms_step = sum(e0.elapsed_time(e1) for e0, e1 in tev) / args.steps
+    else:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(gstream):
+            t_start.record(gstream)
+            for _ in range(args.steps // GRAPH_STEPS):
+                graph.replay()
+            for _ in range(args.steps % GRAPH_STEPS):
+                graph1.replay()
+            t_end.record(gstream)
+        barrier()
+        ms_step = t_start.elapsed_time(t_end) / args.steps
 
     # the same K steps as eager calls from the host (for reference)
     e_start = torch.cuda.Event(enable_timing=True)
@@ -282,6 +312,7 @@ def run_gpu(args):
     n_k = max(20, min(args.steps, 500))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_k)]
     for i in range(n_k):
+        flush(stream)
         staged_step(evs[i])
     barrier()
     clk = clocks.stop()
@@ -369,16 +400,22 @@ def run_gpu(args):
             "config": {"workload": w.name, "B_per_gpu": B, "K": K, "V": V,
                        "logits_dtype": w.dtype, "draft": "one-hot ids" if w.onehot else "dense q fp32",
                        "temperature": w.T, "top_p": w.top_p or None,
-                       "l2": "inputs larger than L2 (%.0f MB > 129 MB), no flush" %
-                             ((B * (K + 1) * V * (2 if w.dtype == 'bf16' else 4)) / 1e6),
+                       "l2": (f"L2 flushed before every timed step (a {2 * L2_BYTES >> 20} MiB buffer written "
+                              f"outside the timed events): a step reads {touched / 1e6:.0f} MB, "
+                              f"under twice the {L2_BYTES >> 20} MiB L2") if flush_l2 else
+                             (f"no flush: a step reads {touched / 1e6:.0f} MB, "
+                              + ("more than twice" if touched >= 2 * L2_BYTES else "UNDER twice (flush off by flag)")
+                              + f" the {L2_BYTES >> 20} MiB L2"),
                        "parallelism": f"replicas x{world} (shard over sequences)"},
             "tokens_per_s": tokens_per_step * world / (ms_step * 1e-3),
             "hbm_gbs_step": step_gbs,
             "hbm_frac_step": {"of_measured": step_gbs / peak, "of_8tbs_nominal": step_gbs / NOMINAL_HBM_GBS},
             "ms_per_step_eager": ms_step_eager,
-            "timing": f"CUDA-graph replay of the public C-ABI call ({GRAPH_STEPS} consecutive calls per "
-                      "replay, the remainder one call per replay); ms_per_step_eager: the same calls "
-                      "issued from the host",
+            "timing": (("the public C-ABI call issued from the host, each call between its own CUDA "
+                        "events, the L2 flush before each (enqueued while the flush runs)") if flush_l2 else
+                       (f"CUDA-graph replay of the public C-ABI call ({GRAPH_STEPS} consecutive calls per "
+                        "replay, the remainder one call per replay)")) +
+                      "; ms_per_step_eager: the same K calls issued back to back from the host, no flush",
             "kernels_ms": {"rows_kernel": rows_ms, "survivor_kernel+final_kernel": surv_ms,
                            "source": f"{n_k} staged calls with CUDA events between the row pass and the draws"},
             "kernels_gbs": {"rows_kernel": rows_gbs, "survivor_kernel+final_kernel": surv_gbs},
@@ -387,10 +424,11 @@ def run_gpu(args):
                          "achieved": rows_gbs, "peak": peak, "unit": "GB/s",
                          "frac": rows_gbs / peak, "peak_source": peak_kind,
                          "traffic": recorded_traffic(w.name, "rows_kernel")},
-            "e2e": {"value": seqs / (e2e_ms * 1e-3), "unit": "seqs/s",
-                    "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-            "gpu_launches": 3 * args.steps,
+            "e2e": ({"value": seqs / (e2e_ms * 1e-3), "unit": "seqs/s",
+                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
+                     "d2h_bytes_per_step": d2h, "steps": e2e_steps} if e2e_steps else None),
+            "gpu_launches": launches_per_step * args.steps,
+            "gpu_launches_per_step": launches_per_step,
             "clocks": clk,
             "status_bits": st,
             "cpu_baseline": cpu,
@@ -483,6 +521,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     ap.add_argument("--batch", type=int, default=0, help="override B (profiling runs)")
+    ap.add_argument("--l2-flush", default="auto", choices=["auto", "on", "off"],
+                    help="flush L2 before every timed step (auto: when a step reads under 2x L2)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

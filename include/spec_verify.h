@@ -210,6 +210,20 @@ sv_status_t spec_verify_noalloc(const void *target_logits,
                                 float *residual_mass, int32_t *status_dev,
                                 void *stream);
 
+/* Number of kernels one spec_verify (or spec_verify_stats) call with these
+ * arguments launches on the CURRENT device: 2 (the row pass and the draw
+ * stream, which then also makes the final draws) or 3 (plus the final
+ * kernel).  The choice depends on B, K, V, the logits dtype, whether draft
+ * probabilities are passed (dense != 0; ignored when K == 0) and how many
+ * CTAs of each kernel the device holds at once.  *launches is 0 for B == 0.
+ * Returns SV_EINVAL (NULL launches, B < 0, K < 0, V < 1, unknown dtype),
+ * SV_EUNSUPPORTED (sizes spec_verify would reject as unsupported) or
+ * SV_ECUDA (the device could not be queried).  Launches nothing.  The pages
+ * have no counterpart: it serves callers that account for launches. */
+sv_status_t sv_kernel_launches(sv_dtype_t logits_dtype, int32_t dense,
+                               int64_t B, int32_t K, int32_t V,
+                               int32_t *launches);
+
 /* Static, NUL-terminated description of a status code. */
 const char *sv_status_string(sv_status_t status);
 

@@ -29,6 +29,20 @@ def sv_workspace_bytes(B: int, K: int, V: int) -> int:
     return int(N.lib().sv_workspace_bytes(int(B), int(K), int(V)))
 
 
+def sv_kernel_launches(logits_dtype: torch.dtype, dense: bool, B: int, K: int, V: int) -> int:
+    """Kernels one spec_verify call with these arguments launches on the
+    current device (2 or 3; 0 for B == 0)."""
+    import ctypes
+    dt = N.SV_BF16 if logits_dtype == torch.bfloat16 else N.SV_FP32
+    if logits_dtype not in (torch.bfloat16, torch.float32):
+        raise SpecVerifyError(N.SV_EINVAL)
+    n = ctypes.c_int32(-1)
+    rc = N.lib().sv_kernel_launches(dt, 1 if dense else 0, int(B), int(K), int(V), ctypes.byref(n))
+    if rc != N.SV_OK:
+        raise SpecVerifyError(rc)
+    return int(n.value)
+
+
 _ws_lock = threading.Lock()
 _ws_cache: dict[int, torch.Tensor] = {}
 

@@ -116,6 +116,34 @@ cudaError_t resident_ctas(Resident &out)
 
 int64_t clamp_grid(int64_t want, int64_t cap) { return want < 1 ? 1 : (want > cap ? cap : want); }
 
+// CTAs of the draw stream: at least one chunk per warp, at most one wave
+int64_t draw_grid(int64_t NC, const Resident &res) { return clamp_grid(ceil_div(NC, sv::kDrawWarps), res.draw); }
+
+// A stream that fills every SM, with at least as many draw warps as
+// sequences: each sequence has its own warps, and the last of them makes its
+// final draw (no final kernel, whose CTAs would only be placed once the
+// stream's CTAs leave).  A smaller stream leaves SMs free, where the final
+// kernel's CTAs wait for it and draw with block-wide scans, sooner than one
+// warp can.
+bool inline_final(int64_t grid, int64_t B, const Resident &res)
+{
+    return grid == res.draw && grid * sv::kDrawWarps >= B;
+}
+
+// Kernels one whole call launches on the current device: the row pass, the
+// draw stream and, unless the stream makes the final draws, the final kernel.
+template <typename LT, bool DENSE>
+cudaError_t launches_per_call(int64_t B, const Plan &plan, int32_t &n)
+{
+    Resident res;
+    const cudaError_t e = resident_ctas<LT, DENSE>(res);
+    if (e != cudaSuccess)
+        return e;
+    const int64_t grid = draw_grid(B * static_cast<int64_t>(plan.CPS), res);
+    n = inline_final(grid, B, res) ? 2 : 3;
+    return cudaSuccess;
+}
+
 template <typename LT, bool DENSE>
 cudaError_t launch(sv::Params P, const Plan &plan, int stages, cudaStream_t stream)
 {
@@ -154,15 +182,8 @@ cudaError_t launch(sv::Params P, const Plan &plan, int stages, cudaStream_t stre
             return e;
     }
     if (stages & kSurvivors) {
-        // at least one chunk per warp
-        const int64_t grid = clamp_grid(ceil_div(P.NC, sv::kDrawWarps), res.draw);
-        // a stream that fills every SM, with at least as many draw warps as
-        // sequences: each sequence has its own warps, and the last of them
-        // makes its final draw (no final kernel, whose CTAs would only be
-        // placed once the stream's CTAs leave).  A smaller stream leaves SMs
-        // free, where the final kernel's CTAs wait for it and draw with
-        // block-wide scans, sooner than one warp can.
-        P.inline_final = grid == res.draw && grid * sv::kDrawWarps >= P.B ? 1 : 0;
+        const int64_t grid = draw_grid(P.NC, res);
+        P.inline_final = inline_final(grid, P.B, res) ? 1 : 0;
         // programmatic dependent launch: the draw's CTAs may be scheduled
         // while the row pass drains; they wait in griddepcontrol.wait for
         // its completion before reading anything it wrote
@@ -328,6 +349,33 @@ sv_status_t sv_sample_survivors(const void *target_logits, sv_dtype_t logits_dty
     return run(kSurvivors, target_logits, logits_dtype, draft_probs, draft_tokens, uniforms, temperature, B, K,
                V, out_tokens, num_emitted, accept_flags, accept_prob, residual_mass, status_dev, workspace,
                workspace_bytes, stream);
+}
+
+sv_status_t sv_kernel_launches(sv_dtype_t logits_dtype, int32_t dense, int64_t B, int32_t K, int32_t V,
+                               int32_t *launches)
+{
+    if (!launches || B < 0 || K < 0 || V < 1 || (logits_dtype != SV_BF16 && logits_dtype != SV_FP32))
+        return SV_EINVAL;
+    if (V > SV_MAX_V)
+        return SV_EUNSUPPORTED;
+    Plan plan;
+    if (!make_plan(B, K, V, plan))
+        return SV_EUNSUPPORTED;
+    if (B == 0) {
+        *launches = 0;
+        return SV_OK;
+    }
+    const bool d = dense != 0 && K > 0; // K = 0 has no draft probabilities to read
+    int32_t n = 0;
+    cudaError_t e;
+    if (logits_dtype == SV_BF16)
+        e = d ? launches_per_call<uint16_t, true>(B, plan, n) : launches_per_call<uint16_t, false>(B, plan, n);
+    else
+        e = d ? launches_per_call<float, true>(B, plan, n) : launches_per_call<float, false>(B, plan, n);
+    if (e != cudaSuccess)
+        return SV_ECUDA;
+    *launches = n;
+    return SV_OK;
 }
 
 const char *sv_status_string(sv_status_t status)

@@ -83,3 +83,21 @@ def test_unsupported_sizes():
 
 def test_empty_batch_is_a_noop():
     assert _call(B=0, ws_bytes=0) == N.SV_OK
+
+
+def _launches(dtype=N.SV_BF16, dense=1, B=4, K=3, V=1000, out=True):
+    n = ctypes.c_int32(-7)
+    rc = N.lib().sv_kernel_launches(dtype, dense, B, K, V, ctypes.byref(n) if out else None)
+    return rc, n.value
+
+
+@pytest.mark.parametrize("kw", [dict(out=False), dict(B=-1), dict(K=-1), dict(V=0), dict(dtype=7)],
+                         ids=lambda d: ",".join(d))
+def test_kernel_launches_host_checks(kw):
+    # rejected before the device is queried
+    assert _launches(**kw)[0] == N.SV_EINVAL
+
+
+def test_kernel_launches_sizes_and_empty_batch():
+    assert _launches(V=N.SV_MAX_V + 1)[0] == N.SV_EUNSUPPORTED
+    assert _launches(B=0) == (N.SV_OK, 0)

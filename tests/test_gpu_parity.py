@@ -306,3 +306,14 @@ def test_acceptance_statistics_counters(orc):
                       "accept_flags": res.accept_flags.cpu().numpy(),
                       "accept_prob": res.accept_prob.cpu().numpy(),
                       "residual_mass": res.residual_mass.cpu().numpy(), "status": int(status.item())})
+
+
+def test_kernel_launch_count():
+    """sv_kernel_launches: a draw stream that fills the GPU makes its own
+    final draws (2 kernels); a small one leaves them to the final kernel (3)."""
+    import speculative_decoding_sampling_gb300 as sv
+    assert sv.sv_kernel_launches(torch.bfloat16, True, 256, 8, 151936) == 2
+    assert sv.sv_kernel_launches(torch.bfloat16, False, 128, 8, 128256) == 2
+    assert sv.sv_kernel_launches(torch.bfloat16, True, 8, 4, 32000) == 3
+    assert sv.sv_kernel_launches(torch.float32, True, 1, 4, 32000) == 3
+    assert sv.sv_kernel_launches(torch.bfloat16, True, 0, 4, 32000) == 0
