@@ -74,7 +74,30 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         ctypes.c_double, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
         ctypes.c_int32, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_void_p]
+    lib.sv_oracle_filter_logits.restype = ctypes.c_int
+    lib.sv_oracle_filter_logits.argtypes = [
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_double,
+        ctypes.c_int32, ctypes.c_double, ctypes.c_void_p, _c_i32p, _c_i32p, ctypes.c_int]
+    lib.sv_oracle_filter_order.restype = ctypes.c_int32
+    lib.sv_oracle_filter_order.argtypes = [
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_double,
+        ctypes.c_int32, ctypes.c_double, _c_i32p, _c_f64p, _c_i32p, _c_f64p]
     return lib
+
+
+@dataclass
+class FilterResult:
+    logits: np.ndarray   # the filtered rows, same dtype and shape as the input
+    kept: np.ndarray     # int32 [rows]: ids kept (0 for a bad row)
+    status: np.ndarray   # int32 [rows]: ORC_BAD_ROW for a row copied unchanged
+
+
+@dataclass
+class FilterOrder:
+    ids: np.ndarray      # int32 [n]: the finite ids in filter order
+    cum: np.ndarray      # fp64 [n]: cumulative unnormalised mass in that order
+    n_topk: int          # ids the top-k step keeps
+    tau: float           # mass the top-p step must reach
 
 
 _loaded: dict[str, "Oracle"] = {}
@@ -185,6 +208,50 @@ class Oracle:
         if Z < 0:
             raise ValueError("invalid row")
         return p, w, cdf, Z
+
+
+    @staticmethod
+    def _dtype_of(logits: np.ndarray) -> int:
+        if logits.dtype == np.uint16:
+            return 0
+        if logits.dtype == np.float32:
+            return 1
+        raise TypeError("logits must be uint16 (bf16 bits) or float32")
+
+    def filter_logits(self, logits: np.ndarray, T: float, top_k: int = 0,
+                      top_p: float = 1.0, nthreads: int = 1) -> FilterResult:
+        """Top-k / top-p filtering of the rows of `logits` (last axis = V) at
+        temperature T: the ids outside the kept set become -inf."""
+        logits = np.ascontiguousarray(logits)
+        dtype = self._dtype_of(logits)
+        V = logits.shape[-1]
+        rows = logits.size // V if V else 0
+        out = np.empty_like(logits)
+        kept = np.empty(rows, np.int32)
+        status = np.empty(rows, np.int32)
+        rc = self.lib.sv_oracle_filter_logits(
+            logits.ctypes.data, dtype, rows, V, float(T), int(top_k), float(top_p),
+            out.ctypes.data, self._ptr(kept, _c_i32p), self._ptr(status, _c_i32p), int(nthreads))
+        if rc != 0:
+            raise ValueError("sv_oracle_filter_logits rejected its arguments")
+        return FilterResult(out, kept, status)
+
+    def filter_order(self, logits: np.ndarray, row: int, T: float, top_k: int = 0,
+                     top_p: float = 1.0) -> FilterOrder | None:
+        """The filter order of one row (None for a bad row)."""
+        logits = np.ascontiguousarray(logits)
+        dtype = self._dtype_of(logits)
+        V = logits.shape[-1]
+        ids = np.empty(V, np.int32)
+        cum = np.empty(V, np.float64)
+        nk = ctypes.c_int32(0)
+        tau = ctypes.c_double(0.0)
+        n = self.lib.sv_oracle_filter_order(
+            logits.ctypes.data, dtype, int(row), V, float(T), int(top_k), float(top_p),
+            self._ptr(ids, _c_i32p), self._ptr(cum, _c_f64p), ctypes.byref(nk), ctypes.byref(tau))
+        if n < 0:
+            return None
+        return FilterOrder(ids[:n].copy(), cum[:n].copy(), int(nk.value), float(tau.value))
 
 
 def load(path: str | None = None) -> Oracle:

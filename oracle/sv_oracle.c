@@ -492,3 +492,206 @@ out:
     free(qr);
     return Z;
 }
+
+/* ------------------------------------------------ top-k / top-p filtering
+ *
+ * (7) The target distribution p carries the target's own sampling
+ *     processing -- temperature, top-k, top-p -- before any accept test, and
+ *     q must match what the draft actually used ("推测解码：草稿、验证与实际加速",
+ *     section 接受与拒绝怎样保住分布).  The pages name these steps but define
+ *     neither top-k nor top-p; the reading taken here:
+ *       - order the ids by p = softmax(z / T) descending, equal p by
+ *         ascending id (ids with a -inf logit have p = 0 and are never kept);
+ *       - top-k (k >= 1): keep the first min(k, #finite) ids of that order;
+ *         k <= 0 keeps every finite id;
+ *       - top-p (0 < top_p < 1): of those, keep the shortest prefix whose
+ *         mass reaches top_p times the mass of the top-k set (the id that
+ *         crosses the threshold is kept); top_p >= 1 keeps the top-k set
+ *         (top_p <= 0 or NaN is rejected);
+ *       - every other logit becomes -inf and kept logits are copied
+ *         unchanged, so softmax(z' / T) is the renormalised filtered p.
+ *     Masses are fp64 exp(z/T - max) summed sequentially in that order.
+ */
+
+typedef struct {
+    double z;   /* logit (the order of z/T, T > 0) */
+    int32_t id;
+} ranked_t;
+
+static int ranked_cmp(const void *a, const void *b)
+{
+    const ranked_t *x = (const ranked_t *)a, *y = (const ranked_t *)b;
+    if (x->z > y->z)
+        return -1;
+    if (x->z < y->z)
+        return 1;
+    return (x->id > y->id) - (x->id < y->id);
+}
+
+/* One row: the finite ids in filter order (rank[0..n)), their cumulative
+ * masses cum[0..n) (unnormalised, exp(z/T - max)), the top-k count and the
+ * top-p target mass.  Returns the number of finite ids, -1 for a bad row
+ * (NaN, +inf or no finite logit). */
+static int32_t filter_rank_row(const void *logits, int dtype, int64_t off, int32_t V, double T,
+                               int32_t top_k, double top_p, ranked_t *rank, double *cum,
+                               int32_t *n_topk, double *tau)
+{
+    int32_t n = 0;
+    double m = -INFINITY;
+    for (int32_t i = 0; i < V; ++i) {
+        double z = logit_at(logits, dtype, off + i);
+        if (isnan(z) || (isinf(z) && z > 0))
+            return -1;
+        if (isinf(z))
+            continue;
+        rank[n].z = z;
+        rank[n].id = i;
+        ++n;
+        if (z / T > m)
+            m = z / T;
+    }
+    if (n == 0)
+        return -1;
+    qsort(rank, (size_t)n, sizeof(ranked_t), ranked_cmp);
+    double acc = 0.0;
+    for (int32_t r = 0; r < n; ++r) {
+        acc += exp(rank[r].z / T - m);
+        cum[r] = acc;
+    }
+    const int32_t nk = (top_k >= 1 && top_k < n) ? top_k : n;
+    *n_topk = nk;
+    *tau = (top_p > 0.0 && top_p < 1.0) ? top_p * cum[nk - 1] : cum[nk - 1];
+    return n;
+}
+
+/* How many ids of the order are kept: the shortest prefix (within the
+ * top-k count) whose cumulative mass reaches tau. */
+static int32_t filter_kept(const double *cum, int32_t nk, double tau)
+{
+    int32_t r = 0;
+    while (r < nk - 1 && cum[r] < tau)
+        ++r;
+    return r + 1;
+}
+
+typedef struct {
+    const void *logits;
+    int dtype;
+    int32_t V;
+    double T, top_p;
+    int32_t top_k;
+    void *out;
+    int32_t *kept;
+    int32_t *status;
+    int64_t r0, r1;
+    int failed;
+} filter_job_t;
+
+static void *filter_job(void *arg)
+{
+    filter_job_t *J = (filter_job_t *)arg;
+    const int32_t V = J->V;
+    ranked_t *rank = (ranked_t *)malloc((size_t)V * sizeof(ranked_t));
+    double *cum = (double *)malloc((size_t)V * sizeof(double));
+    if (!rank || !cum) {
+        J->failed = 1;
+        free(rank);
+        free(cum);
+        return NULL;
+    }
+    for (int64_t row = J->r0; row < J->r1; ++row) {
+        const int64_t off = row * (int64_t)V;
+        int32_t nk = 0;
+        double tau = 0.0;
+        const int32_t n = filter_rank_row(J->logits, J->dtype, off, V, J->T, J->top_k, J->top_p,
+                                          rank, cum, &nk, &tau);
+        /* copy the row; then mask what is not kept */
+        if (J->dtype == 0)
+            memcpy((uint16_t *)J->out + off, (const uint16_t *)J->logits + off, (size_t)V * 2);
+        else
+            memcpy((float *)J->out + off, (const float *)J->logits + off, (size_t)V * 4);
+        if (n < 0) {
+            J->kept[row] = 0;
+            J->status[row] = ORC_BAD_ROW;
+            continue;
+        }
+        const int32_t kept = (J->top_p < 1.0) ? filter_kept(cum, nk, tau) : nk;
+        for (int32_t r = kept; r < n; ++r) {
+            const int32_t i = rank[r].id;
+            if (J->dtype == 0)
+                ((uint16_t *)J->out)[off + i] = 0xFF80u; /* bf16 -inf */
+            else
+                ((float *)J->out)[off + i] = -INFINITY;
+        }
+        J->kept[row] = kept;
+        J->status[row] = 0;
+    }
+    free(rank);
+    free(cum);
+    return NULL;
+}
+
+/* Filter `rows` logit rows of V entries (dtype 0 = bf16 bits, 1 = fp32) at
+ * temperature T with top_k / top_p as in (7).  out: the filtered rows, same
+ * dtype; kept[row]: ids kept (0 for a bad row); status[row]: ORC_BAD_ROW for
+ * a row with NaN, +inf or no finite logit (copied unchanged).  Returns 0. */
+int sv_oracle_filter_logits(const void *logits, int dtype, int64_t rows, int32_t V, double T,
+                            int32_t top_k, double top_p, void *out, int32_t *kept,
+                            int32_t *status, int nthreads)
+{
+    if (!logits || !out || !kept || !status || rows < 0 || V < 1 || !(T > 0.0) || !(top_p > 0.0))
+        return -1;
+    if (nthreads < 1)
+        nthreads = 1;
+    if ((int64_t)nthreads > rows)
+        nthreads = (int)(rows > 0 ? rows : 1);
+    filter_job_t *jobs = (filter_job_t *)calloc((size_t)nthreads, sizeof(filter_job_t));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !th) {
+        free(jobs);
+        free(th);
+        return -1;
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        filter_job_t J = {logits, dtype, V, T, top_p, top_k, out, kept, status,
+                          rows * t / nthreads, rows * (t + 1) / nthreads, 0};
+        jobs[t] = J;
+    }
+    for (int t = 1; t < nthreads; ++t)
+        if (pthread_create(&th[t], NULL, filter_job, &jobs[t]) != 0)
+            jobs[t].failed = 2;
+    filter_job(&jobs[0]);
+    int rc = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (jobs[t].failed == 2) {
+            jobs[t].failed = 0;
+            filter_job(&jobs[t]);
+        } else {
+            pthread_join(th[t], NULL);
+        }
+    }
+    for (int t = 0; t < nthreads; ++t)
+        if (jobs[t].failed)
+            rc = -1;
+    free(jobs);
+    free(th);
+    return rc;
+}
+
+/* One row's filter order for parity checks: the finite ids in order
+ * (ids[0..n)), the cumulative masses of that order (cum[0..n)), the top-k
+ * count and the top-p target mass.  Returns n, or -1 for a bad row. */
+int32_t sv_oracle_filter_order(const void *logits, int dtype, int64_t row, int32_t V, double T,
+                               int32_t top_k, double top_p, int32_t *ids, double *cum,
+                               int32_t *n_topk, double *tau)
+{
+    ranked_t *rank = (ranked_t *)malloc((size_t)V * sizeof(ranked_t));
+    if (!rank)
+        return -1;
+    const int32_t n = filter_rank_row(logits, dtype, row * (int64_t)V, V, T, top_k, top_p, rank, cum,
+                                      n_topk, tau);
+    for (int32_t r = 0; r < n; ++r)
+        ids[r] = rank[r].id;
+    free(rank);
+    return n;
+}

@@ -496,6 +496,146 @@ def pin_bruteforce_tiny(orc):
                 assert got == want, (K, p_rows, q_rows, draft, us[b], got, want)
 
 
+
+# ------------------------------------------------ top-k / top-p filtering
+# The target's p carries its own temperature, top-k and top-p ("推测解码：
+# 草稿、验证与实际加速", section 接受与拒绝怎样保住分布); the pages do not define
+# the two filters, so these pins fix the reading taken (ids ordered by p
+# descending, ties by lower id; top-k keeps the first k; top-p keeps the
+# shortest prefix of the top-k set reaching top_p of its mass).
+
+def _filter_kept(orc, z, T=1.0, top_k=0, top_p=1.0):
+    z = np.asarray(z, np.float32)[None, :]
+    r = orc.filter_logits(z, T, top_k, top_p)
+    kept = [int(i) for i in np.nonzero(np.isfinite(r.logits[0]))[0]]
+    assert int(r.kept[0]) == len(kept) and int(r.status[0]) == 0
+    # kept logits are copied bit for bit
+    assert np.array_equal(r.logits[0][kept].view(np.uint32), z[0][kept].view(np.uint32))
+    return kept
+
+
+def pin_filter_closed_forms(orc):
+    z = np.log([0.4, 0.3, 0.2, 0.1])
+    assert _filter_kept(orc, z, top_p=0.35) == [0]
+    assert _filter_kept(orc, z, top_p=0.5) == [0, 1]
+    assert _filter_kept(orc, z, top_p=0.75) == [0, 1, 2]
+    assert _filter_kept(orc, z, top_p=0.95) == [0, 1, 2, 3]
+    assert _filter_kept(orc, z, top_k=2) == [0, 1]
+    assert _filter_kept(orc, z, top_k=1) == [0]
+    assert _filter_kept(orc, z, top_k=9) == [0, 1, 2, 3]
+    # top-p measured against the top-k set's mass: 0.4 / 0.7 >= 0.5
+    assert _filter_kept(orc, z, top_k=2, top_p=0.5) == [0]
+    assert _filter_kept(orc, z, top_k=2, top_p=0.6) == [0, 1]
+    # top-3 mass 0.9: 0.77 of it is 0.693, reached by 0.4 + 0.3
+    assert _filter_kept(orc, z, top_k=3, top_p=0.77) == [0, 1]
+    assert _filter_kept(orc, z, top_p=0.77) == [0, 1, 2]
+    # order of the ids in the row does not matter
+    assert _filter_kept(orc, z[::-1].copy(), top_p=0.5) == [2, 3]
+
+
+def pin_filter_ties_by_id(orc):
+    z = [1.0, 2.0, 2.0, 0.0, 2.0]
+    assert _filter_kept(orc, z, top_k=1) == [1]
+    assert _filter_kept(orc, z, top_k=2) == [1, 2]
+    assert _filter_kept(orc, z, top_k=3) == [1, 2, 4]
+    assert _filter_kept(orc, z, top_p=1e-9) == [1]
+    # equal logits have exact unit masses: 0.5 of four is reached exactly by
+    # the second id, which is kept (reaching the mass is enough)
+    assert _filter_kept(orc, [0.0, 0.0, 0.0, 0.0], top_p=0.5) == [0, 1]
+    assert _filter_kept(orc, [0.0, 0.0, 0.0, 0.0], top_p=0.75) == [0, 1, 2]
+
+
+def pin_filter_temperature(orc):
+    z = np.log([0.6, 0.4])
+    # T = 1: p = (0.6, 0.4)
+    assert _filter_kept(orc, z, T=1.0, top_p=0.55) == [0]
+    assert _filter_kept(orc, z, T=1.0, top_p=0.8) == [0, 1]
+    # T = 4: p0 = 0.6^(1/4) / (0.6^(1/4) + 0.4^(1/4)) = 0.5253
+    assert _filter_kept(orc, z, T=4.0, top_p=0.55) == [0, 1]
+    assert _filter_kept(orc, z, T=4.0, top_p=0.52) == [0]
+    # T = 1/4: p0 = 0.6^4 / (0.6^4 + 0.4^4) = 0.8351
+    assert _filter_kept(orc, z, T=0.25, top_p=0.8) == [0]
+
+
+def pin_filter_masked_and_bad_rows(orc):
+    ninf = -np.inf
+    # -inf ids have p = 0: never kept, not counted
+    assert _filter_kept(orc, [ninf, 1.0, ninf, 0.5], top_k=3) == [1, 3]
+    assert _filter_kept(orc, [ninf, 1.0, ninf, 0.5], top_p=0.999999) == [1, 3]
+    bad = np.array([[0.0, np.nan, 1.0], [0.0, np.inf, 1.0], [ninf, ninf, ninf], [0.0, 1.0, 2.0]],
+                   np.float32)
+    r = orc.filter_logits(bad, 1.0, 1, 0.5)
+    assert list(r.status) == [8, 8, 8, 0] and list(r.kept) == [0, 0, 0, 1]
+    assert np.array_equal(r.logits[:3].view(np.uint32), bad[:3].view(np.uint32))
+    # bf16 rows: the masked ids become the bf16 -inf pattern
+    zb = np.array([[0x3F80, 0x4000, 0xBF80]], np.uint16)   # 1.0, 2.0, -1.0
+    rb = orc.filter_logits(zb, 1.0, 1, 1.0)
+    assert list(rb.logits[0]) == [0xFF80, 0x4000, 0xFF80] and int(rb.kept[0]) == 1
+
+
+def _bruteforce_kept(z, T, top_k, top_p):
+    """The smallest order-closed set of finite ids (no id outside it ranks
+    before an id inside it) within the top-k set whose mass reaches top_p
+    of the top-k set's, by enumerating all subsets."""
+    V = len(z)
+    fin = [i for i in range(V) if np.isfinite(z[i])]
+    m = max(z[i] / T for i in fin)
+    e = {i: float(np.exp(z[i] / T - m)) for i in fin}
+
+    def before(j, i):   # j ranks before i
+        return z[j] > z[i] or (z[j] == z[i] and j < i)
+
+    closed = []
+    for mask in range(1, 1 << V):
+        S = [i for i in range(V) if mask >> i & 1]
+        if any(not np.isfinite(z[i]) for i in S):
+            continue
+        if all(j in S for i in S for j in fin if before(j, i)):
+            closed.append(S)
+    nk = len(fin) if top_k < 1 else min(top_k, len(fin))
+    topk = [S for S in closed if len(S) == nk][0]
+    if top_p >= 1.0:
+        return sorted(topk), False
+    tau = top_p * sum(e[i] for i in topk)
+    ok = [S for S in closed if len(S) <= nk and sum(e[i] for i in S) >= tau]
+    best = min(ok, key=len)
+    near = any(abs(sum(e[i] for i in S) - tau) < 1e-12 for S in closed)
+    return sorted(best), near
+
+
+def pin_filter_bruteforce_tiny(orc):
+    rng = np.random.default_rng(7)
+    checked = 0
+    for trial in range(60):
+        V = int(rng.integers(1, 7))
+        z = rng.choice([-2.0, -1.0, -0.5, 0.0, 0.5, 1.0, 2.0, -np.inf], size=V).astype(np.float32)
+        if not np.isfinite(z).any():
+            z[0] = 0.0
+        for top_k in (0, 1, 2, 3, 6):
+            for top_p in (0.3, 0.5, 0.8, 0.95, 1.0):
+                for T in (0.5, 1.0, 2.0):
+                    want, near = _bruteforce_kept(z.astype(np.float64), T, top_k, top_p)
+                    if near:
+                        continue
+                    assert _filter_kept(orc, z, T=T, top_k=top_k, top_p=top_p) == want, \
+                        (z, top_k, top_p, T)
+                    checked += 1
+    assert checked > 2000
+
+
+def pin_filter_matches_generator_nucleus(orc):
+    """The input generator marks the top-p nucleus of the 64-sequence workload
+    with its own sort (synth.c); the oracle's filter must mask the same ids."""
+    import synth
+    w = synth.WORKLOADS["b64_k5_v128256_bf16_topp"].with_(B=2, V=6000)
+    masked = synth.generate(w).logits
+    raw = synth.generate(w.with_(top_p=0.0)).logits
+    kept = masked != 0xFF80
+    assert np.array_equal(masked[kept], raw[kept])
+    r = orc.filter_logits(raw, w.T, 0, w.top_p)
+    assert np.array_equal(r.logits, masked)
+    assert (r.status == 0).all() and int(r.kept.min()) >= 1
+
 ALL_PINS = [
     # cheap first: mutants should fail fast
     pin_worked_example,
@@ -516,6 +656,12 @@ ALL_PINS = [
     pin_batch_consistency,
     pin_pointwise_identity,
     pin_bruteforce_tiny,
+    pin_filter_closed_forms,
+    pin_filter_ties_by_id,
+    pin_filter_temperature,
+    pin_filter_masked_and_bad_rows,
+    pin_filter_bruteforce_tiny,
+    pin_filter_matches_generator_nucleus,
     pin_output_distribution,
     pin_expected_tokens,
 ]

@@ -15,7 +15,7 @@ MUTANTS = [
     ("residual_no_clamp", "w[i] = d > 0.0 ? d : 0.0;", "w[i] = d;", 1),
     ("ratio_inverted", "double a = px / qx;", "double a = qx / px;", 1),
     ("accept_no_min", "o.accept_prob[k] = a < 1.0 ? a : 1.0;", "o.accept_prob[k] = a;", 1),
-    ("temperature_times", "/ T;", "* T;", 2),
+    ("temperature_times", "/ T;", "* T;", 3),
     ("cdf_le", "if (t < C)", "if (t <= C)", 1),
     ("correction_uses_rejecting_draw", "inverse_cdf(w_scratch, V, u[K], &Z)",
      "inverse_cdf(w_scratch, V, u[jstar], &Z)", 1),
@@ -34,6 +34,15 @@ MUTANTS = [
     ("u_upper_inclusive", "u[k] < 1.0)", "u[k] <= 1.0)", 1),
     ("p_of_draft_from_next_row", "double px = P[(int64_t)k * V + tok[k]];",
      "double px = P[(int64_t)(k + 1) * V + tok[k]];", 1),
+    # top-k / top-p filtering
+    ("filter_ties_high_id", "return (x->id > y->id) - (x->id < y->id);\n}\n\n/* One row",
+     "return (x->id < y->id) - (x->id > y->id);\n}\n\n/* One row", 1),
+    ("filter_topp_of_total_mass", "top_p * cum[nk - 1]", "top_p * cum[n - 1]", 1),
+    ("filter_drops_crossing_id", "    return r + 1;\n}", "    return r > 0 ? r : 1;\n}", 1),
+    ("filter_reach_strict", "cum[r] < tau", "cum[r] <= tau", 1),
+    ("filter_topk_one_more", "top_k < n) ? top_k : n", "top_k < n) ? top_k + 1 : n", 1),
+    ("filter_mass_without_temperature", "acc += exp(rank[r].z / T - m);",
+     "acc += exp(rank[r].z - m);", 1),
 ]
 
 
