@@ -210,6 +210,37 @@ sv_status_t spec_verify_noalloc(const void *target_logits,
                                 float *residual_mass, int32_t *status_dev,
                                 void *stream);
 
+/* Top-k / top-p filtering of target logit rows, for targets that sample
+ * with those filters: the accept test and the final draw must see the
+ * target's processed distribution -- temperature, top-k, top-p -- and q must
+ * be what the draft actually used ("推测解码：草稿、验证与实际加速", section
+ * 接受与拒绝怎样保住分布).  The pages name the filters without defining them;
+ * this library's reading: the ids of a row are ordered by
+ * p = softmax(z / T) descending, equal p by ascending id; top-k keeps the
+ * first min(top_k, #finite) ids (top_k <= 0: no top-k); top-p keeps the
+ * shortest prefix of that set whose mass reaches top_p times the set's mass,
+ * the crossing id included (top_p >= 1: no top-p).  Kept logits are copied
+ * unchanged and every other entry becomes -inf, so passing out_logits to
+ * spec_verify with the same temperature verifies against the filtered p.
+ *   logits      [rows, V] bf16 or fp32 (logits_dtype), device.
+ *   out_logits  [rows, V], same dtype; may be the same pointer as logits (in
+ *               place); other overlaps are not allowed.
+ *   kept        [rows] int32: ids kept per row (0 for a bad row).  May be NULL.
+ *   status_dev  SV_BAD_ROW is OR-ed in for a row with NaN, +inf or no finite
+ *               logit; such a row is copied unchanged.  May be NULL.
+ * Masses are formed as the verification forms them (exp2 on the
+ * special-function unit, summed exactly in fixed point), so a row whose
+ * cumulative mass crosses top_p within ~1e-6 of an id's boundary may keep
+ * one id more or less than an fp64 computation would.
+ * Returns SV_EINVAL (NULL or misaligned pointer, rows < 0, V < 1, T not
+ * finite or <= 0, top_p <= 0 or NaN, unknown dtype), SV_EUNSUPPORTED
+ * (V > SV_MAX_V) or SV_ECUDA.  rows == 0 is a no-op.  One launch on
+ * `stream`; allocates nothing. */
+sv_status_t sv_filter_logits(const void *logits, sv_dtype_t logits_dtype,
+                             int64_t rows, int32_t V, float temperature,
+                             int32_t top_k, float top_p, void *out_logits,
+                             int32_t *kept, int32_t *status_dev, void *stream);
+
 /* Number of kernels one spec_verify (or spec_verify_stats) call with these
  * arguments launches on the CURRENT device: 2 (the row pass and the draw
  * stream, which then also makes the final draws) or 3 (plus the final

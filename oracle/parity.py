@@ -185,3 +185,65 @@ def _check_sequence(orc, logits, q, tokens, u, T, cand, b, ores, oi, rep, depth,
         rep.excused += 1
     else:
         rep.failures.append((b, "final token", g, o, uk, float(worst)))
+
+
+# ------------------------------------------------ top-k / top-p filtering
+
+FILTER_WINDOW = 1e-5
+
+
+@dataclass
+class FilterReport:
+    rows: int = 0
+    excused: list = field(default_factory=list)    # (row, oracle kept, candidate kept)
+    failures: list = field(default_factory=list)   # (row, reason)
+
+    def ok(self, max_excused_fraction: float = 1e-3) -> bool:
+        return not self.failures and len(self.excused) <= max(1, max_excused_fraction * self.rows)
+
+    def summary(self) -> str:
+        return (f"{self.rows} rows, {len(self.excused)} excused, {len(self.failures)} failures"
+                + (f"; first failure {self.failures[0]}" if self.failures else ""))
+
+
+def compare_filter(orc, logits, T, top_k, top_p, cand_out, cand_kept) -> FilterReport:
+    """Filtered rows of a candidate against the oracle's.  A row must match
+    the oracle bit for bit, except when the two keep different numbers of
+    ids and every cumulative mass between the two cuts lies within
+    FILTER_WINDOW (relative) of the top-p target: then the candidate's row
+    must still be exactly the oracle's order cut at the candidate's count,
+    and the row is counted as excused.  Top-k counts are never excused."""
+    logits = np.ascontiguousarray(logits)
+    V = logits.shape[-1]
+    flat_in = logits.reshape(-1, V)
+    ref = orc.filter_logits(flat_in, T, top_k, top_p)
+    flat_c = np.ascontiguousarray(cand_out).reshape(-1, V)
+    kept_c = np.asarray(cand_kept).reshape(-1)
+    rep = FilterReport(rows=flat_in.shape[0])
+    neg = np.uint16(0xFF80) if flat_in.dtype == np.uint16 else np.float32(-np.inf)
+    for r in range(flat_in.shape[0]):
+        a = ref.logits[r].view(np.uint16 if flat_in.dtype == np.uint16 else np.uint32)
+        b = flat_c[r].view(a.dtype)
+        if np.array_equal(a, b) and int(kept_c[r]) == int(ref.kept[r]):
+            continue
+        order = orc.filter_order(flat_in, r, T, top_k, top_p)
+        if order is None or ref.status[r] != 0:
+            rep.failures.append((r, "bad row not copied unchanged"))
+            continue
+        ng, no = int(kept_c[r]), int(ref.kept[r])
+        if not (1 <= ng <= order.n_topk):
+            rep.failures.append((r, f"kept {ng} outside [1, {order.n_topk}]"))
+            continue
+        want = flat_in[r].copy()
+        drop = order.ids[ng:]
+        want[drop] = neg
+        if not np.array_equal(want.view(a.dtype), b):
+            rep.failures.append((r, f"row is not the order cut at {ng}"))
+            continue
+        lo, hi = min(ng, no), max(ng, no)
+        tau = order.tau
+        if all(abs(order.cum[n - 1] - tau) <= FILTER_WINDOW * tau for n in range(lo, hi)):
+            rep.excused.append((r, no, ng))
+        else:
+            rep.failures.append((r, f"kept {ng} vs oracle {no} outside the window"))
+    return rep

@@ -14,7 +14,7 @@ SV_MAX_V = 1 << 21
 
 # every function the header declares, in declaration order
 EXPORTS = ["sv_workspace_bytes", "spec_verify", "spec_verify_stats", "sv_verify_rows",
-           "sv_sample_survivors", "sv_kernel_launches", "sv_status_string"]
+           "sv_sample_survivors", "sv_filter_logits", "sv_kernel_launches", "sv_status_string"]
 
 
 def stats_words(K: int) -> int:
@@ -53,6 +53,10 @@ def lib() -> ctypes.CDLL:
             fn.argtypes = _VERIFY_ARGTYPES
         L.spec_verify_stats.restype = ctypes.c_int
         L.spec_verify_stats.argtypes = _VERIFY_ARGTYPES[:-1] + [ctypes.c_void_p, ctypes.c_void_p]
+        L.sv_filter_logits.restype = ctypes.c_int
+        L.sv_filter_logits.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int32,
+                                       ctypes.c_float, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         L.sv_kernel_launches.restype = ctypes.c_int
         L.sv_kernel_launches.argtypes = [ctypes.c_int, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
                                          ctypes.c_int32, ctypes.c_void_p]

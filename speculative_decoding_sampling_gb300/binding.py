@@ -43,6 +43,37 @@ def sv_kernel_launches(logits_dtype: torch.dtype, dense: bool, B: int, K: int, V
     return int(n.value)
 
 
+def sv_filter_logits(logits: torch.Tensor, temperature: float, top_k: int = 0, top_p: float = 1.0, *,
+                     out: torch.Tensor | None = None, kept: torch.Tensor | None = None,
+                     status: torch.Tensor | None = None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Top-k / top-p filtering of logit rows (last axis = V) at `temperature`:
+    every id outside the kept set becomes -inf.  `out` may be `logits`
+    itself (in place).  Returns (filtered logits, kept ids per row)."""
+    if logits.dtype not in (torch.bfloat16, torch.float32):
+        raise SpecVerifyError(N.SV_EINVAL)
+    if not logits.is_cuda or not logits.is_contiguous() or logits.dim() < 1:
+        raise ValueError("logits must be a contiguous CUDA tensor")
+    V = logits.shape[-1]
+    rows = logits.numel() // V if V else 0
+    if out is None:
+        out = torch.empty_like(logits)
+    if out.shape != logits.shape or out.dtype != logits.dtype or not out.is_contiguous() \
+            or out.device != logits.device:
+        raise ValueError("out must match logits")
+    if kept is None:
+        kept = torch.empty(logits.shape[:-1], dtype=torch.int32, device=logits.device)
+    if kept.numel() != rows or kept.dtype != torch.int32 or not kept.is_contiguous():
+        raise ValueError("kept must be int32 with one entry per row")
+    dt = N.SV_BF16 if logits.dtype == torch.bfloat16 else N.SV_FP32
+    stream = torch.cuda.current_stream(logits.device).cuda_stream
+    rc = N.lib().sv_filter_logits(logits.data_ptr(), dt, rows, V, float(temperature), int(top_k),
+                                  float(top_p), out.data_ptr(), kept.data_ptr(),
+                                  None if status is None else status.data_ptr(), stream)
+    if rc != N.SV_OK:
+        raise SpecVerifyError(rc)
+    return out, kept
+
+
 _ws_lock = threading.Lock()
 _ws_cache: dict[int, torch.Tensor] = {}
 

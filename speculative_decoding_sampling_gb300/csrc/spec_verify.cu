@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 #include <mutex>
 
+#include "sv_filter.cuh"
 #include "sv_final.cuh"
 #include "sv_rows.cuh"
 
@@ -376,6 +377,65 @@ sv_status_t sv_kernel_launches(sv_dtype_t logits_dtype, int32_t dense, int64_t B
         return SV_ECUDA;
     *launches = n;
     return SV_OK;
+}
+
+sv_status_t sv_filter_logits(const void *logits, sv_dtype_t logits_dtype, int64_t rows, int32_t V,
+                             float temperature, int32_t top_k, float top_p, void *out_logits, int32_t *kept,
+                             int32_t *status_dev, void *stream)
+{
+    if (rows < 0 || V < 1 || (logits_dtype != SV_BF16 && logits_dtype != SV_FP32))
+        return SV_EINVAL;
+    if (V > SV_MAX_V)
+        return SV_EUNSUPPORTED;
+    if (!std::isfinite(temperature) || !(temperature > 0.0f) || !(top_p > 0.0f))
+        return SV_EINVAL;
+    const float c = static_cast<float>(1.4426950408889634074 / static_cast<double>(temperature));
+    if (!std::isfinite(c) || !(c > 0.0f))
+        return SV_EINVAL;
+    const size_t esize = logits_dtype == SV_BF16 ? 2 : 4;
+    if (rows > 0 && (!logits || !out_logits))
+        return SV_EINVAL;
+    if (!aligned(logits, esize) || !aligned(out_logits, esize) || (kept && !aligned(kept, 4)) ||
+        (status_dev && !aligned(status_dev, 4)))
+        return SV_EINVAL;
+    if (rows > 0 && static_cast<int64_t>(V) > INT64_MAX / rows)
+        return SV_EUNSUPPORTED;
+    if (rows == 0)
+        return SV_OK;
+    sv::FilterParams F;
+    F.in = logits;
+    F.out = out_logits;
+    F.rows = rows;
+    F.V = V;
+    F.c = c;
+    F.top_k = top_k;
+    F.top_p = top_p;
+    const int fb = 62 - ceil_log2_u64(static_cast<uint64_t>(V) + 1);
+    F.fb = fb < 40 ? fb : 40;
+    F.yscale = static_cast<float>(sv::kYBins) / static_cast<float>(F.fb + 2);
+    F.vec = aligned(logits, 16) && aligned(out_logits, 16) && (static_cast<size_t>(V) * esize) % 16 == 0 ? 1 : 0;
+    F.kept = kept;
+    F.status = status_dev;
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = logits_dtype == SV_BF16
+                ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sv::filter_kernel<uint16_t>,
+                                                                sv::kFilterThreads, 0)
+                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sv::filter_kernel<float>,
+                                                                sv::kFilterThreads, 0);
+    if (e != cudaSuccess)
+        return SV_ECUDA;
+    const int64_t resident = static_cast<int64_t>(sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
+    const int64_t grid = rows < resident ? rows : resident;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (logits_dtype == SV_BF16)
+        sv::filter_kernel<uint16_t><<<static_cast<unsigned>(grid), sv::kFilterThreads, 0, s>>>(F);
+    else
+        sv::filter_kernel<float><<<static_cast<unsigned>(grid), sv::kFilterThreads, 0, s>>>(F);
+    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 
 const char *sv_status_string(sv_status_t status)

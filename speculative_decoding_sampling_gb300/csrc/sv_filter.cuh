@@ -1,0 +1,495 @@
+// sv_filter.cuh -- top-k / top-p filtering of target logit rows.
+//
+// The target distribution the accept test uses already carries the
+// target's own sampling processing: temperature, top-k and top-p
+// ("推测解码：草稿、验证与实际加速", section 接受与拒绝怎样保住分布).  The pages
+// name these steps without defining them; the reading implemented here:
+// the ids of a row are ordered by p = softmax(z / T) descending, equal p by
+// ascending id; top-k keeps the first min(k, #finite) ids; top-p keeps the
+// shortest prefix of that set whose mass reaches top_p times the set's mass
+// (the crossing id is kept); every other logit becomes -inf, kept logits
+// are copied unchanged, so softmax(z' / T) is the renormalised filtered p.
+//
+// One CTA per row (a persistent grid over the rows).  Masses are the
+// verification's own: e_i = exp2(z_i c - fl(m c)) as an integer multiple of
+// 2^-fb, so every sum is exact and order-independent.  Per row:
+//   1. one pass: the maximum, the finite count, NaN / +inf detection (the
+//      only pass that has to come from HBM; the rest find the row in L2);
+//   2. one pass: counts and masses in kYBins bins of y = z c - fl(m c)
+//      (bin 0 holds the largest values; the last bin everything whose mass
+//      rounds to zero), and the bin where the top-k count / top-p mass is
+//      reached, by a scan from bin 0;
+//   3. inside that bin, the exact element: the order key of z (an unsigned
+//      integer that sorts like z) is narrowed radix digit by radix digit
+//      (8 bits per pass, starting below the bits all of the bin's keys
+//      share) to one value, and among the ids holding that value the j-th in
+//      id order is found by an ordered block scan;
+//   4. one pass writes the row: z where (z, id) ranks at or before the cut,
+//      -inf elsewhere.
+// With both filters, top-k is resolved first (its cut bounds the elements
+// top-p may keep, and its exact mass sets the top-p target).
+#pragma once
+
+#include "sv_device.cuh"
+
+namespace sv {
+
+constexpr int kFilterThreads = 512;
+constexpr int kFilterWarps = kFilterThreads / 32;
+constexpr int kYBins = 512;       // coarse bins of y
+constexpr int kTieIds = 8;        // consecutive ids a thread owns in the ordered scan
+
+struct FilterParams {
+    const void *in;
+    void *out;
+    int64_t rows;
+    int32_t V;
+    float c;          // log2(e) / T
+    int32_t top_k;    // <= 0: off
+    float top_p;      // >= 1: off
+    int fb;           // fractional bits of the masses
+    float yscale;     // bins per unit of -y: kYBins / (fb + 2), so the last
+                      // bin only holds ids whose mass rounds to zero
+    int vec;          // rows are 16-byte aligned groups: vector loads
+    int32_t *kept;    // [rows] or nullptr
+    int32_t *status;  // or nullptr
+};
+
+// The element type's raw bits, value, order key and -inf pattern.
+template <typename LT> struct FilterElem;
+template <> struct FilterElem<uint16_t> {
+    static constexpr int kPerVec = 8;
+    __device__ static float value(uint32_t h) { return __uint_as_float(h << 16); }
+    __device__ static bool finite(uint32_t h) { return (h & 0x7F80u) != 0x7F80u; }
+    __device__ static bool nan_or_pinf(uint32_t h) { return (h & 0x7F80u) == 0x7F80u && h != 0xFF80u; }
+    // -0 sorts as +0: they are the same logit
+    __device__ static uint32_t key(uint32_t h)
+    {
+        h = h == 0x8000u ? 0u : h;
+        return (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
+    }
+    __device__ static uint32_t bits_of_key(uint32_t k) { return (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu); }
+    static constexpr uint32_t kNegInf = 0xFF80u;
+};
+template <> struct FilterElem<float> {
+    static constexpr int kPerVec = 4;
+    __device__ static float value(uint32_t u) { return __uint_as_float(u); }
+    __device__ static bool finite(uint32_t u) { return (u & 0x7F800000u) != 0x7F800000u; }
+    __device__ static bool nan_or_pinf(uint32_t u) { return (u & 0x7F800000u) == 0x7F800000u && u != 0xFF800000u; }
+    __device__ static uint32_t key(uint32_t u)
+    {
+        u = u == 0x80000000u ? 0u : u;
+        return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    }
+    __device__ static uint32_t bits_of_key(uint32_t k) { return (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k; }
+    static constexpr uint32_t kNegInf = 0xFF800000u;
+};
+
+// Raw bits of element i (plain loads: the output may be the input).
+template <typename LT>
+__device__ __forceinline__ uint32_t filter_bits(const LT *row, int64_t i)
+{
+    if constexpr (sizeof(LT) == 2)
+        return reinterpret_cast<const unsigned short *>(row)[i];
+    else
+        return __float_as_uint(row[i]);
+}
+
+// Visit every element (id, raw bits) of a row; thread t takes vectors (or
+// elements) t, t + blockDim, ...
+template <typename LT, typename F>
+__device__ __forceinline__ void filter_visit(const LT *row, int32_t V, bool vec, F &&f)
+{
+    if (vec) {
+        constexpr int PV = FilterElem<LT>::kPerVec;
+        const int32_t nv = V / PV;
+        const uint4 *rv = reinterpret_cast<const uint4 *>(row);
+        for (int32_t v = threadIdx.x; v < nv; v += kFilterThreads) {
+            const uint4 w = rv[v];
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+            if constexpr (PV == 8) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    f(v * 8 + 2 * k, u[k] & 0xFFFFu);
+                    f(v * 8 + 2 * k + 1, u[k] >> 16);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    f(v * 4 + k, u[k]);
+            }
+        }
+    } else {
+        for (int32_t i = threadIdx.x; i < V; i += kFilterThreads)
+            f(i, filter_bits<LT>(row, i));
+    }
+}
+
+struct FilterShared {
+    unsigned int cnt[kYBins];
+    unsigned long long mass[kYBins];
+    unsigned int dcnt[256];
+    unsigned long long dmass[256];
+    float redf[kFilterWarps];
+    long long redl[kFilterWarps];
+    unsigned int kmin, kmax;
+    int bad;
+    int found;
+    int32_t found_id;
+};
+
+__device__ __forceinline__ float block_max_f(float v, FilterShared &S)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    __syncthreads();
+    if (lane == 0)
+        S.redf[warp] = v;
+    __syncthreads();
+    float r = S.redf[0];
+#pragma unroll
+    for (int w = 1; w < kFilterWarps; ++w)
+        r = fmaxf(r, S.redf[w]);
+    return r;
+}
+
+__device__ __forceinline__ long long block_sum_l(long long v, FilterShared &S)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_sum_ll(v);
+    __syncthreads();
+    if (lane == 0)
+        S.redl[warp] = v;
+    __syncthreads();
+    long long r = 0;
+#pragma unroll
+    for (int w = 0; w < kFilterWarps; ++w)
+        r += S.redl[w];
+    return r;
+}
+
+// The per-row constants every pass forms masses and bins with.
+struct FilterRow {
+    float c, mc, yscale;
+    int fb;
+    __device__ float y(float z) const { return __fmaf_rn(z, c, -mc); }
+    __device__ long long w(float yv) const { return to_fixed(ex2(yv), fb); }
+    __device__ int bin(float yv) const
+    {
+        const float t = fmaxf(__fmul_rn(-yv, yscale), 0.0f);
+        return t < static_cast<float>(kYBins - 1) ? static_cast<int>(t) : kYBins - 1;
+    }
+};
+
+// k >> s, 0 for s >= 32 (a bin's keys may differ in all 32 bits)
+__device__ __forceinline__ uint32_t shr32(uint32_t k, int s) { return s >= 32 ? 0u : k >> s; }
+
+// A cut in the order: (key, id).  Element (k, i) ranks at or before it iff
+// k > key or (k == key and i <= id).
+struct Cut {
+    uint32_t key;
+    int32_t id;
+    __device__ bool covers(uint32_t k, int32_t i) const { return k > key || (k == key && i <= id); }
+};
+
+// Inside coarse bin `b`, among the finite elements at or before `bound`
+// (when `bounded`), the element at which the running count reaches
+// `target` (MASS = false) or the running mass reaches `target` (MASS = true),
+// in the filter order.  Returns the cut at that element and adds the mass
+// of the elements up to and including it to *mass_upto.
+template <typename LT, bool MASS>
+__device__ Cut filter_resolve(const LT *row, int32_t V, bool vec, const FilterRow &R, int b, bool bounded,
+                              Cut bound, long long target, long long *mass_upto, FilterShared &S)
+{
+    using E = FilterElem<LT>;
+    auto considered = [&](int32_t i, uint32_t bits, uint32_t &k, long long &w) {
+        if (!E::finite(bits))
+            return false;
+        k = E::key(bits);
+        if (bounded && !bound.covers(k, i))
+            return false;
+        const float yv = R.y(E::value(bits));
+        if (R.bin(yv) != b)
+            return false;
+        w = R.w(yv);
+        return true;
+    };
+    // the key bits every considered element shares
+    if (threadIdx.x == 0) {
+        S.kmin = 0xFFFFFFFFu;
+        S.kmax = 0u;
+    }
+    __syncthreads();
+    filter_visit<LT>(row, V, vec, [&](int32_t i, uint32_t bits) {
+        uint32_t k;
+        long long w;
+        if (considered(i, bits, k, w)) {
+            atomicMin(&S.kmin, k);
+            atomicMax(&S.kmax, k);
+        }
+    });
+    __syncthreads();
+    const uint32_t kx = S.kmin ^ S.kmax;
+    int hi = kx ? 32 - __clz(kx) : 0; // the low `hi` bits still differ
+    uint32_t prefix = shr32(S.kmax, hi);
+    long long rem = target;
+    long long acc_mass = 0;
+    while (hi > 0) {
+        const int lo = hi > 8 ? hi - 8 : 0;
+        const int nd = 1 << (hi - lo);
+        __syncthreads();
+        for (int d = threadIdx.x; d < nd; d += kFilterThreads) {
+            S.dcnt[d] = 0u;
+            S.dmass[d] = 0ull;
+        }
+        __syncthreads();
+        filter_visit<LT>(row, V, vec, [&](int32_t i, uint32_t bits) {
+            uint32_t k;
+            long long w;
+            if (considered(i, bits, k, w) && shr32(k, hi) == prefix) {
+                const uint32_t d = (k >> lo) & static_cast<uint32_t>(nd - 1);
+                atomicAdd(&S.dcnt[d], 1u);
+                if (w)
+                    atomicAdd(&S.dmass[d], static_cast<unsigned long long>(w));
+            }
+        });
+        __syncthreads();
+        // every thread scans the (at most 256) digits from the top: the same
+        // answer everywhere, no broadcast needed
+        int d = nd - 1;
+        for (; d > 0; --d) {
+            const long long have = MASS ? static_cast<long long>(S.dmass[d]) : static_cast<long long>(S.dcnt[d]);
+            if (have >= rem)
+                break;
+            rem -= have;
+            acc_mass += static_cast<long long>(S.dmass[d]);
+        }
+        prefix = (prefix << (hi - lo)) | static_cast<uint32_t>(d);
+        hi = lo;
+    }
+    // one value left: its ids in id order, the j-th of them is the cut
+    const uint32_t kcut = prefix;
+    const float ycut = R.y(E::value(E::bits_of_key(kcut)));
+    const long long wcut = R.w(ycut);
+    long long j = rem; // count target
+    if (MASS)
+        j = wcut > 0 ? (rem + wcut - 1) / wcut : 1;
+    if (j < 1)
+        j = 1;
+    *mass_upto += acc_mass + j * wcut;
+    // ordered scan: thread t owns ids [t0 + t * kTieIds, t0 + (t+1) * kTieIds)
+    if (threadIdx.x == 0) {
+        S.found = 0;
+        S.found_id = -1;
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int64_t t0 = 0; t0 < V; t0 += static_cast<int64_t>(kFilterThreads) * kTieIds) {
+        const int64_t i0 = t0 + static_cast<int64_t>(threadIdx.x) * kTieIds;
+        uint32_t hits = 0; // bit m: id i0 + m holds the value (and is considered)
+#pragma unroll
+        for (int m = 0; m < kTieIds; ++m) {
+            const int64_t i = i0 + m;
+            if (i < V) {
+                const uint32_t bits = filter_bits<LT>(row, i);
+                if (E::finite(bits) && E::key(bits) == kcut &&
+                    (!bounded || bound.covers(kcut, static_cast<int32_t>(i))))
+                    hits |= 1u << m;
+            }
+        }
+        const long long n = __popc(hits);
+        // block exclusive scan of n in thread (= id) order
+        long long incl = warp_incl_scan_ll(n, lane);
+        __syncthreads();
+        if (lane == 31)
+            S.redl[warp] = incl;
+        __syncthreads();
+        long long before = incl - n;
+        long long total = 0;
+#pragma unroll
+        for (int w = 0; w < kFilterWarps; ++w) {
+            const long long s = S.redl[w];
+            if (w < warp)
+                before += s;
+            total += s;
+        }
+        if (before < j && j <= before + n) {
+            uint32_t h = hits;
+            for (long long r = j - before; r > 1; --r)
+                h &= h - 1; // drop the lowest set bit
+            S.found_id = static_cast<int32_t>(i0 + (__ffs(h) - 1));
+            S.found = 1;
+        }
+        __syncthreads();
+        if (S.found)
+            break;
+        j -= total;
+    }
+    __syncthreads();
+    const Cut cut = {kcut, S.found_id};
+    __syncthreads();
+    return cut;
+}
+
+template <typename LT>
+__global__ void __launch_bounds__(kFilterThreads, 1) filter_kernel(const FilterParams P)
+{
+    using E = FilterElem<LT>;
+    __shared__ FilterShared S;
+    const int32_t V = P.V;
+    for (int64_t r = blockIdx.x; r < P.rows; r += gridDim.x) {
+        const LT *row = static_cast<const LT *>(P.in) + r * V;
+        LT *orow = static_cast<LT *>(P.out) + r * V;
+        // 1. maximum, finite count, bad entries
+        float m = -INFINITY;
+        long long nfin = 0;
+        int bad = 0;
+        filter_visit<LT>(row, V, P.vec, [&](int32_t, uint32_t bits) {
+            if (E::finite(bits)) {
+                m = fmaxf(m, E::value(bits));
+                ++nfin;
+            } else if (E::nan_or_pinf(bits)) {
+                bad = 1;
+            }
+        });
+        if (threadIdx.x == 0)
+            S.bad = 0;
+        __syncthreads();
+        if (bad)
+            S.bad = 1;
+        m = block_max_f(m, S);
+        nfin = block_sum_l(nfin, S);
+        if (S.bad || nfin == 0) {
+            // a row the verification rejects anyway: copied unchanged
+            if (P.out != P.in)
+                for (int32_t i = threadIdx.x; i < V; i += kFilterThreads)
+                    orow[i] = row[i];
+            if (threadIdx.x == 0) {
+                if (P.kept)
+                    P.kept[r] = 0;
+                if (P.status)
+                    atomicOr(P.status, kBadRow);
+            }
+            __syncthreads();
+            continue;
+        }
+        const FilterRow R = {P.c, mc_of(m, P.c), P.yscale, P.fb};
+
+        // 2. coarse bins of y
+        for (int i = threadIdx.x; i < kYBins; i += kFilterThreads) {
+            S.cnt[i] = 0u;
+            S.mass[i] = 0ull;
+        }
+        __syncthreads();
+        filter_visit<LT>(row, V, P.vec, [&](int32_t, uint32_t bits) {
+            const bool fin = E::finite(bits);
+            const float yv = fin ? R.y(E::value(bits)) : 0.0f;
+            const int b = fin ? R.bin(yv) : -1;
+            // the last bin (zero mass) is the crowded one: one add per warp
+            const unsigned am = __activemask();
+            const unsigned under = __ballot_sync(am, b == kYBins - 1);
+            if (b == kYBins - 1) {
+                if ((threadIdx.x & 31) == __ffs(under) - 1)
+                    atomicAdd(&S.cnt[kYBins - 1], static_cast<unsigned>(__popc(under)));
+            } else if (b >= 0) {
+                atomicAdd(&S.cnt[b], 1u);
+                const long long w = R.w(yv);
+                if (w)
+                    atomicAdd(&S.mass[b], static_cast<unsigned long long>(w));
+            }
+        });
+        __syncthreads();
+
+        // 3. the cuts
+        const bool use_k = P.top_k >= 1 && static_cast<long long>(P.top_k) < nfin;
+        const bool use_p = P.top_p < 1.0f;
+        bool have_cut = false;
+        Cut cut = {0u, -1};
+        long long Sk = 0; // mass of the top-k set
+        int bk = kYBins - 1;
+        if (use_k) {
+            long long acc = 0, accm = 0;
+            int b = 0;
+            for (; b < kYBins - 1; ++b) {
+                if (acc + static_cast<long long>(S.cnt[b]) >= P.top_k)
+                    break;
+                acc += S.cnt[b];
+                accm += static_cast<long long>(S.mass[b]);
+            }
+            bk = b;
+            Sk = accm;
+            cut = filter_resolve<LT, false>(row, V, P.vec, R, b, false, cut, P.top_k - acc, &Sk, S);
+            have_cut = true;
+        } else {
+            for (int b = 0; b < kYBins; ++b)
+                Sk += static_cast<long long>(S.mass[b]);
+        }
+        if (use_p) {
+            long long tau = static_cast<long long>(ceil(static_cast<double>(P.top_p) * static_cast<double>(Sk)));
+            if (tau < 1)
+                tau = 1;
+            long long accm = 0;
+            int b = 0;
+            for (; b < bk; ++b) {
+                if (accm + static_cast<long long>(S.mass[b]) >= tau)
+                    break;
+                accm += static_cast<long long>(S.mass[b]);
+            }
+            long long upto = accm;
+            cut = filter_resolve<LT, true>(row, V, P.vec, R, b, have_cut && b == bk, cut, tau - accm, &upto, S);
+            have_cut = true;
+        }
+
+        // 4. write the row
+        long long kept = 0;
+        const bool vec = P.vec;
+        auto keep_of = [&](int32_t i, uint32_t bits) {
+            return E::finite(bits) && (!have_cut || cut.covers(E::key(bits), i));
+        };
+        if (vec) {
+            constexpr int PV = E::kPerVec;
+            const int32_t nv = V / PV;
+            const uint4 *rv = reinterpret_cast<const uint4 *>(row);
+            uint4 *ov = reinterpret_cast<uint4 *>(orow);
+            for (int32_t v = threadIdx.x; v < nv; v += kFilterThreads) {
+                const uint4 w = rv[v];
+                uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if constexpr (PV == 8) {
+                        uint32_t lo = u[k] & 0xFFFFu, hi = u[k] >> 16;
+                        const bool kl = keep_of(v * 8 + 2 * k, lo), kh = keep_of(v * 8 + 2 * k + 1, hi);
+                        kept += kl + kh;
+                        lo = kl ? lo : E::kNegInf;
+                        hi = kh ? hi : E::kNegInf;
+                        u[k] = lo | (hi << 16);
+                    } else {
+                        const bool kk = keep_of(v * 4 + k, u[k]);
+                        kept += kk;
+                        u[k] = kk ? u[k] : E::kNegInf;
+                    }
+                }
+                ov[v] = make_uint4(u[0], u[1], u[2], u[3]);
+            }
+        } else {
+            for (int32_t i = threadIdx.x; i < V; i += kFilterThreads) {
+                const uint32_t bits = filter_bits<LT>(row, i);
+                const bool kk = keep_of(i, bits);
+                kept += kk;
+                const uint32_t o = kk ? bits : E::kNegInf;
+                if constexpr (sizeof(LT) == 2)
+                    reinterpret_cast<unsigned short *>(orow)[i] = static_cast<unsigned short>(o);
+                else
+                    reinterpret_cast<uint32_t *>(orow)[i] = o;
+            }
+        }
+        kept = block_sum_l(kept, S);
+        if (threadIdx.x == 0 && P.kept)
+            P.kept[r] = static_cast<int32_t>(kept);
+        __syncthreads();
+    }
+}
+
+} // namespace sv

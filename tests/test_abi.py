@@ -101,3 +101,29 @@ def test_kernel_launches_host_checks(kw):
 def test_kernel_launches_sizes_and_empty_batch():
     assert _launches(V=N.SV_MAX_V + 1)[0] == N.SV_EUNSUPPORTED
     assert _launches(B=0) == (N.SV_OK, 0)
+
+
+def _filter(**kw):
+    fake = 1 << 40
+    a = dict(logits=fake, dtype=N.SV_BF16, rows=4, V=1000, T=1.0, k=0, p=0.9, out=fake, kept=None,
+             status=None, stream=None)
+    a.update(kw)
+    return N.lib().sv_filter_logits(a["logits"], a["dtype"], a["rows"], a["V"], ctypes.c_float(a["T"]),
+                                    a["k"], ctypes.c_float(a["p"]), a["out"], a["kept"], a["status"],
+                                    a["stream"])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(logits=None), dict(out=None), dict(rows=-1), dict(V=0), dict(dtype=5), dict(T=0.0),
+    dict(T=float("nan")), dict(T=float("inf")), dict(p=0.0), dict(p=-0.5), dict(p=float("nan")),
+    dict(logits=(1 << 40) + 1), dict(out=(1 << 40) + 1), dict(kept=(1 << 40) + 2),
+], ids=lambda d: ",".join(d))
+def test_filter_host_checks(kw):
+    # rejected before any CUDA call
+    assert _filter(**kw) == N.SV_EINVAL
+
+
+def test_filter_sizes_and_empty():
+    assert _filter(V=N.SV_MAX_V + 1) == N.SV_EUNSUPPORTED
+    assert _filter(rows=0) == N.SV_OK
+    assert _filter(rows=0, logits=None, out=None) == N.SV_OK
