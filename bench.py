@@ -176,6 +176,13 @@ def run_gpu(args):
 
     # this rank's shard of the global batch: sequences [rank*B, (rank+1)*B)
     inp = synth.generate(w, b0=rank * B, nb=B)
+    filt = bool(args.filter_top_p)
+    if filt:
+        # the target's top-p applied on the GPU: raw logits in, the draft's
+        # processed q, tokens and uniforms as generated
+        if not w.top_p:
+            raise SystemExit("--filter-top-p needs a workload with top-p")
+        inp.logits = synth.generate(w.with_(top_p=0.0), b0=rank * B, nb=B).logits
     host = {"logits": torch.from_numpy(inp.logits.view(np.int16) if w.dtype == "bf16" else inp.logits),
             "q": None if inp.q is None else torch.from_numpy(inp.q),
             "tokens": torch.from_numpy(inp.tokens), "u": torch.from_numpy(inp.u)}
@@ -204,20 +211,37 @@ def run_gpu(args):
                 o["accept_prob"].data_ptr(), o["residual_mass"].data_ptr(), status.data_ptr(),
                 ws.data_ptr(), need, stream.cuda_stream)
 
-    cargs = args_for(d_logits, d_q, d_tok, d_u, out)
+    d_filt = torch.empty_like(d_logits) if filt else None
+    d_kept = torch.empty(B * (K + 1), dtype=torch.int32, device=dev) if filt else None
+    top_p32 = float(np.float32(w.top_p)) if filt else 1.0
+    cargs = args_for(d_filt if filt else d_logits, d_q, d_tok, d_u, out)
+
+    def filter_call(s):
+        rc = lib.sv_filter_logits(d_logits.data_ptr(), dt, B * (K + 1), V, ctypes.c_float(w.T), 0,
+                                  ctypes.c_float(top_p32), d_filt.data_ptr(), d_kept.data_ptr(),
+                                  status.data_ptr(), s.cuda_stream)
+        if rc:
+            raise RuntimeError(sv.sv_status_string(rc))
 
     def step(s):
         # one call = the launches of the path (row pass, draw stream and,
         # unless the draw stream makes them, the final draws), each chained
-        # to the one before by programmatic dependent launch
+        # to the one before by programmatic dependent launch; with
+        # --filter-top-p the filter launch comes first
+        if filt:
+            filter_call(s)
         rc = lib.spec_verify(*cargs[:-1], s.cuda_stream)
         if rc:
             raise RuntimeError(sv.sv_status_string(rc))
 
-    def staged_step(evs):
+    def staged_step(evs, fev=None):
         # the same launches through the per-stage entry points, with events
         # between the row pass and the draws (this breaks the launch chaining
         # there, so it is used for per-kernel durations only)
+        if fev is not None:
+            fev[0].record(stream)
+            filter_call(stream)
+            fev[1].record(stream)
         evs[0].record(stream)
         rc = lib.sv_verify_rows(*cargs)
         evs[1].record(stream)
@@ -250,7 +274,7 @@ def run_gpu(args):
             with torch.cuda.stream(s):
                 flush_buf.fill_(1)
     launches_per_step = sv.sv_kernel_launches(
-        torch.bfloat16 if w.dtype == "bf16" else torch.float32, d_q is not None, B, K, V)
+        torch.bfloat16 if w.dtype == "bf16" else torch.float32, d_q is not None, B, K, V) + (1 if filt else 0)
 
     # the public call captured in CUDA graphs, GRAPH_STEPS consecutive calls
     # (steps) per graph plus a one-call graph for the remainder: the timed
@@ -311,13 +335,15 @@ def run_gpu(args):
     # ---- per-kernel durations: the same launches, events between them
     n_k = max(20, min(args.steps, 500))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_k)]
+    fevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_k)] if filt else None
     for i in range(n_k):
         flush(stream)
-        staged_step(evs[i])
+        staged_step(evs[i], fevs[i] if filt else None)
     barrier()
     clk = clocks.stop()
     rows_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / n_k
     surv_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / n_k
+    filt_ms = sum(e[0].elapsed_time(e[1]) for e in fevs) / n_k if filt else None
     if world > 1:
         t = torch.tensor([ms_step], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -327,6 +353,9 @@ def run_gpu(args):
     st = int(status.item())
     tokens_per_step = int(num_emitted.sum())
     nbytes = algorithmic_bytes(w, num_emitted)
+    if filt:   # the filter reads every logit once and writes every logit once
+        nbytes["filter_kernel"] = 2 * B * (K + 1) * V * (2 if w.dtype == "bf16" else 4)
+        nbytes["total"] += nbytes["filter_kernel"]
     peak, peak_kind = peaks()
     rows_gbs = nbytes["rows_kernel"] / (rows_ms * 1e-3) / 1e9
     surv_gbs = nbytes["draw_kernels"] / (surv_ms * 1e-3) / 1e9
@@ -354,6 +383,8 @@ def run_gpu(args):
         e_tok.copy_(pin["tokens"], non_blocking=True)
         e_u.copy_(pin["u"], non_blocking=True)
         lg = e_logits.view(torch.bfloat16) if w.dtype == "bf16" else e_logits
+        if filt:
+            sv.sv_filter_logits(lg, w.T, 0, top_p32, out=lg, kept=d_kept, status=status)
         res = sv.spec_verify(lg, pin.get("q"), e_tok, e_u, w.T, out=out, workspace=ws, status=status)
         h_out["out_tokens"].copy_(res.out_tokens, non_blocking=True)
         h_out["num_emitted"].copy_(res.num_emitted, non_blocking=True)
@@ -382,7 +413,13 @@ def run_gpu(args):
         cpu = None
         parity_note = None
         if not args.no_cpu_baseline:
-            cpu, parity_note = cpu_baseline_and_check(w, inp, out, args.cpu_seconds)
+            fl = None
+            if filt:
+                f = d_filt.cpu()
+                f = f.view(torch.int16).numpy().view(np.uint16) if w.dtype == "bf16" else f.numpy()
+                fl = (f, d_kept.cpu().numpy())
+            cpu, parity_note = cpu_baseline_and_check(w, inp, out, args.cpu_seconds,
+                                                      top_p=top_p32 if filt else None, filtered=fl)
         result = {
             "metric": METRIC,
             "value": seqs / (ms_step * 1e-3),
@@ -400,6 +437,8 @@ def run_gpu(args):
             "config": {"workload": w.name, "B_per_gpu": B, "K": K, "V": V,
                        "logits_dtype": w.dtype, "draft": "one-hot ids" if w.onehot else "dense q fp32",
                        "temperature": w.T, "top_p": w.top_p or None,
+                       "top_p_applied": ("on the GPU (sv_filter_logits, raw logits in)" if filt else
+                                         ("by the input generator (masked logits in)" if w.top_p else None)),
                        "l2": (f"L2 flushed before every timed step (a {2 * L2_BYTES >> 20} MiB buffer written "
                               f"outside the timed events): a step reads {touched / 1e6:.0f} MB, "
                               f"under twice the {L2_BYTES >> 20} MiB L2") if flush_l2 else
@@ -419,6 +458,11 @@ def run_gpu(args):
             "kernels_ms": {"rows_kernel": rows_ms, "survivor_kernel+final_kernel": surv_ms,
                            "source": f"{n_k} staged calls with CUDA events between the row pass and the draws"},
             "kernels_gbs": {"rows_kernel": rows_gbs, "survivor_kernel+final_kernel": surv_gbs},
+            "filter": ({"kernel": "filter_kernel", "top_p": top_p32, "top_k": 0, "ms": filt_ms,
+                        "algorithmic_bytes": nbytes["filter_kernel"],
+                        "achieved": nbytes["filter_kernel"] / (filt_ms * 1e-3) / 1e9, "peak": peak,
+                        "unit": "GB/s", "frac": nbytes["filter_kernel"] / (filt_ms * 1e-3) / 1e9 / peak,
+                        "kept_mean": float(d_kept.float().mean().item())} if filt else None),
             "algorithmic_bytes": nbytes,
             "roofline": {"bound": "hbm", "kernel": "rows_kernel",
                          "achieved": rows_gbs, "peak": peak, "unit": "GB/s",
@@ -440,9 +484,11 @@ def run_gpu(args):
     return result
 
 
-def cpu_baseline_and_check(w, inp, out, seconds):
+def cpu_baseline_and_check(w, inp, out, seconds, top_p=None, filtered=None):
     """Time the oracle as it stands on this host's cores over the whole batch
-    (repeated until `seconds` elapse) and check the GPU outputs against it."""
+    (repeated until `seconds` elapse) and check the GPU outputs against it.
+    With `top_p`, the oracle filters the raw logits first (part of the timed
+    step) and the GPU's filtered logits `filtered` are checked too."""
     import oracle
     from oracle import parity
     orc = oracle.load()
@@ -450,17 +496,29 @@ def cpu_baseline_and_check(w, inp, out, seconds):
     t0 = time.perf_counter()
     passes = 0
     ref = None
+    logits = inp.logits
     while True:
-        ref = orc.verify(inp.logits, inp.q, inp.tokens, inp.u, inp.T, nthreads=cores)
+        if top_p is not None:
+            logits = orc.filter_logits(inp.logits, inp.T, 0, top_p, nthreads=cores).logits
+        ref = orc.verify(logits, inp.q, inp.tokens, inp.u, inp.T, nthreads=cores)
         passes += 1
         if time.perf_counter() - t0 >= seconds:
             break
     el = time.perf_counter() - t0
     cand = {k: out[k].cpu().numpy() for k in out}
-    rep = parity.compare(orc, inp.logits, inp.q, inp.tokens, inp.u, inp.T, cand, oracle_res=ref)
+    note = {}
+    if top_p is not None:
+        frep = parity.compare_filter(orc, inp.logits, inp.T, 0, top_p, filtered[0], filtered[1])
+        note["filter"] = {"ok": frep.ok(), "summary": frep.summary()}
+        if frep.excused:   # verify what the GPU actually filtered
+            logits = filtered[0].reshape(logits.shape)
+            ref = None
+    rep = parity.compare(orc, logits, inp.q, inp.tokens, inp.u, inp.T, cand, oracle_res=ref)
     cpu = {"value": passes * inp.B / el, "unit": "seqs/s", "cores": cores, "kind": "oracle",
-           "sample": f"all {inp.B} sequences of the workload, {passes} passes, {el:.1f} s wall"}
-    return cpu, {"ok": rep.ok(), "summary": rep.summary()}
+           "sample": f"all {inp.B} sequences of the workload, {passes} passes, {el:.1f} s wall"
+                     + (" (top-p filter included)" if top_p is not None else "")}
+    ok = rep.ok() and all(v["ok"] for v in note.values())
+    return cpu, dict(ok=ok, summary=rep.summary(), **note)
 
 
 # ------------------------------------------------------------ reference arm
@@ -521,6 +579,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     ap.add_argument("--batch", type=int, default=0, help="override B (profiling runs)")
+    ap.add_argument("--filter-top-p", action="store_true",
+                    help="top-p workloads: raw logits, the target's top-p applied by sv_filter_logits in the step")
     ap.add_argument("--l2-flush", default="auto", choices=["auto", "on", "off"],
                     help="flush L2 before every timed step (auto: when a step reads under 2x L2)")
     args = ap.parse_args()

@@ -19,11 +19,14 @@
 //      (bin 0 holds the largest values; the last bin everything whose mass
 //      rounds to zero), and the bin where the top-k count / top-p mass is
 //      reached, by a scan from bin 0;
-//   3. inside that bin, the exact element: the order key of z (an unsigned
-//      integer that sorts like z) is narrowed radix digit by radix digit
-//      (8 bits per pass, starting below the bits all of the bin's keys
-//      share) to one value, and among the ids holding that value the j-th in
-//      id order is found by an ordered block scan;
+//   3. inside that bin, the exact element.  A bin is a contiguous range of
+//      the order key of z (an unsigned integer that sorts like z).  A bin of
+//      at most kCollect ids is collected into shared memory in one pass,
+//      sorted (bitonic, by key then id) and walked with a block scan.  A
+//      larger bin is narrowed radix digit by radix digit (8 bits per pass,
+//      starting below the bits all its keys share) to one value, and among
+//      the ids holding that value the j-th in id order is found by an
+//      ordered block scan;
 //   4. one pass writes the row: z where (z, id) ranks at or before the cut,
 //      -inf elsewhere.
 // With both filters, top-k is resolved first (its cut bounds the elements
@@ -38,6 +41,7 @@ constexpr int kFilterThreads = 512;
 constexpr int kFilterWarps = kFilterThreads / 32;
 constexpr int kYBins = 512;       // coarse bins of y
 constexpr int kTieIds = 8;        // consecutive ids a thread owns in the ordered scan
+constexpr int kCollect = 2048;    // ids of a bin resolved by a sort in shared memory
 
 struct FilterParams {
     const void *in;
@@ -70,6 +74,7 @@ template <> struct FilterElem<uint16_t> {
     }
     __device__ static uint32_t bits_of_key(uint32_t k) { return (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu); }
     static constexpr uint32_t kNegInf = 0xFF80u;
+    static constexpr uint32_t kKeyMin = 0x0080u, kKeyMax = 0xFF7Fu; // keys of the finite values
 };
 template <> struct FilterElem<float> {
     static constexpr int kPerVec = 4;
@@ -83,6 +88,7 @@ template <> struct FilterElem<float> {
     }
     __device__ static uint32_t bits_of_key(uint32_t k) { return (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k; }
     static constexpr uint32_t kNegInf = 0xFF800000u;
+    static constexpr uint32_t kKeyMin = 0x00800000u, kKeyMax = 0xFF7FFFFFu;
 };
 
 // Raw bits of element i (plain loads: the output may be the input).
@@ -102,10 +108,10 @@ __device__ __forceinline__ void filter_visit(const LT *row, int32_t V, bool vec,
 {
     if (vec) {
         constexpr int PV = FilterElem<LT>::kPerVec;
+        constexpr int U = 4; // vectors a thread has in flight
         const int32_t nv = V / PV;
         const uint4 *rv = reinterpret_cast<const uint4 *>(row);
-        for (int32_t v = threadIdx.x; v < nv; v += kFilterThreads) {
-            const uint4 w = rv[v];
+        auto visit_vec = [&](int32_t v, const uint4 w) {
             const uint32_t u[4] = {w.x, w.y, w.z, w.w};
             if constexpr (PV == 8) {
 #pragma unroll
@@ -118,7 +124,19 @@ __device__ __forceinline__ void filter_visit(const LT *row, int32_t V, bool vec,
                 for (int k = 0; k < 4; ++k)
                     f(v * 4 + k, u[k]);
             }
+        };
+        int32_t v = threadIdx.x;
+        for (; v + (U - 1) * kFilterThreads < nv; v += U * kFilterThreads) {
+            uint4 w[U];
+#pragma unroll
+            for (int t = 0; t < U; ++t)
+                w[t] = rv[v + t * kFilterThreads];
+#pragma unroll
+            for (int t = 0; t < U; ++t)
+                visit_vec(v + t * kFilterThreads, w[t]);
         }
+        for (; v < nv; v += kFilterThreads)
+            visit_vec(v, rv[v]);
     } else {
         for (int32_t i = threadIdx.x; i < V; i += kFilterThreads)
             f(i, filter_bits<LT>(row, i));
@@ -132,6 +150,9 @@ struct FilterShared {
     unsigned long long dmass[256];
     float redf[kFilterWarps];
     long long redl[kFilterWarps];
+    uint32_t ckey[kCollect]; // a bin's collected ids: keys, then sorted with them
+    int32_t cid[kCollect];
+    unsigned int ncol;
     unsigned int kmin, kmax;
     int bad;
     int found;
@@ -183,6 +204,35 @@ struct FilterRow {
     }
 };
 
+// The keys of coarse bin b: [klo, khi].  The bin of a value never grows
+// with its key (y is a rounded fma of z with c > 0, the bin a rounded
+// scaling of -y), so a bin is a contiguous range of keys, found by binary
+// search over the finite keys (every thread computes the same range).
+template <typename LT>
+__device__ __forceinline__ void bin_keys(const FilterRow &R, int b, uint32_t &klo, uint32_t &khi)
+{
+    using E = FilterElem<LT>;
+    auto first_at_most = [&](int bb) { // smallest finite key whose bin is <= bb
+        uint64_t lo = E::kKeyMin, hi = static_cast<uint64_t>(E::kKeyMax) + 1;
+        while (lo < hi) {
+            const uint64_t mid = (lo + hi) >> 1;
+            if (R.bin(R.y(E::value(E::bits_of_key(static_cast<uint32_t>(mid))))) <= bb)
+                hi = mid;
+            else
+                lo = mid + 1;
+        }
+        return lo;
+    };
+    klo = static_cast<uint32_t>(first_at_most(b));
+    khi = b == 0 ? E::kKeyMax : static_cast<uint32_t>(first_at_most(b - 1) - 1);
+}
+
+// Ranks first in the filter order: the larger key, then the smaller id.
+__device__ __forceinline__ bool ranks_first(uint32_t ka, int32_t ia, uint32_t kb, int32_t ib)
+{
+    return ka > kb || (ka == kb && ia < ib);
+}
+
 // k >> s, 0 for s >= 32 (a bin's keys may differ in all 32 bits)
 __device__ __forceinline__ uint32_t shr32(uint32_t k, int s) { return s >= 32 ? 0u : k >> s; }
 
@@ -204,18 +254,103 @@ __device__ Cut filter_resolve(const LT *row, int32_t V, bool vec, const FilterRo
                               Cut bound, long long target, long long *mass_upto, FilterShared &S)
 {
     using E = FilterElem<LT>;
+    uint32_t klo, khi;
+    bin_keys<LT>(R, b, klo, khi);
+    auto member = [&](int32_t i, uint32_t bits, uint32_t &k) {
+        k = E::key(bits); // non-finite keys lie outside every bin's range
+        return k >= klo && k <= khi && (!bounded || bound.covers(k, i));
+    };
     auto considered = [&](int32_t i, uint32_t bits, uint32_t &k, long long &w) {
-        if (!E::finite(bits))
+        if (!member(i, bits, k))
             return false;
-        k = E::key(bits);
-        if (bounded && !bound.covers(k, i))
-            return false;
-        const float yv = R.y(E::value(bits));
-        if (R.bin(yv) != b)
-            return false;
-        w = R.w(yv);
+        w = R.w(R.y(E::value(bits)));
         return true;
     };
+    if (S.cnt[b] <= static_cast<unsigned>(kCollect)) {
+        // the bin fits in shared memory: collect it, sort it, walk it
+        if (threadIdx.x == 0)
+            S.ncol = 0u;
+        __syncthreads();
+        filter_visit<LT>(row, V, vec, [&](int32_t i, uint32_t bits) {
+            uint32_t k;
+            if (member(i, bits, k)) {
+                const unsigned slot = atomicAdd(&S.ncol, 1u);
+                if (slot < static_cast<unsigned>(kCollect)) { // the bin's count bounds it; kept in bounds regardless
+                    S.ckey[slot] = k;
+                    S.cid[slot] = i;
+                }
+            }
+        });
+        __syncthreads();
+        const int n = S.ncol < static_cast<unsigned>(kCollect) ? static_cast<int>(S.ncol) : kCollect;
+        int n2 = 1;
+        while (n2 < n)
+            n2 <<= 1;
+        for (int i = n + threadIdx.x; i < n2; i += kFilterThreads) { // padding ranks last
+            S.ckey[i] = 0u;
+            S.cid[i] = 0x7FFFFFFF;
+        }
+        __syncthreads();
+        for (int k = 2; k <= n2; k <<= 1) { // bitonic sort into the filter order
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                for (int i = threadIdx.x; i < n2; i += kFilterThreads) {
+                    const int l = i ^ j;
+                    if (l > i) {
+                        const bool first = (i & k) == 0; // this pair sorts into filter order
+                        const bool swap = first ? ranks_first(S.ckey[l], S.cid[l], S.ckey[i], S.cid[i])
+                                                : ranks_first(S.ckey[i], S.cid[i], S.ckey[l], S.cid[l]);
+                        if (swap) {
+                            const uint32_t tk = S.ckey[i];
+                            const int32_t ti = S.cid[i];
+                            S.ckey[i] = S.ckey[l];
+                            S.cid[i] = S.cid[l];
+                            S.ckey[l] = tk;
+                            S.cid[l] = ti;
+                        }
+                    }
+                }
+                __syncthreads();
+            }
+        }
+        // running masses in that order: thread t owns entries 4t .. 4t+3
+        constexpr int PT = kCollect / kFilterThreads;
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        long long pre[PT];
+        long long run = 0;
+#pragma unroll
+        for (int e = 0; e < PT; ++e) {
+            const int i = threadIdx.x * PT + e;
+            run += i < n ? R.w(R.y(E::value(E::bits_of_key(S.ckey[i])))) : 0;
+            pre[e] = run;
+        }
+        const long long incl = warp_incl_scan_ll(run, lane);
+        __syncthreads();
+        if (lane == 31)
+            S.redl[warp] = incl;
+        if (threadIdx.x == 0)
+            S.found_id = 0x7FFFFFFF;
+        __syncthreads();
+        long long off = incl - run;
+        for (int w = 0; w < warp; ++w)
+            off += S.redl[w];
+#pragma unroll
+        for (int e = 0; e < PT; ++e) {
+            const int i = threadIdx.x * PT + e;
+            pre[e] += off;
+            const bool hit = MASS ? (i < n && pre[e] >= target) : (i == target - 1);
+            if (hit)
+                atomicMin(&S.found_id, i);
+        }
+        __syncthreads();
+        const int ci = S.found_id < n ? S.found_id : n - 1;
+        if (ci >= threadIdx.x * PT && ci < threadIdx.x * PT + PT)
+            S.redl[0] = pre[ci - threadIdx.x * PT]; // running mass through the cut
+        __syncthreads();
+        const Cut cut = {S.ckey[ci], S.cid[ci]};
+        *mass_upto += S.redl[0];
+        __syncthreads();
+        return cut;
+    }
     // the key bits every considered element shares
     if (threadIdx.x == 0) {
         S.kmin = 0xFFFFFFFFu;
@@ -334,7 +469,7 @@ __device__ Cut filter_resolve(const LT *row, int32_t V, bool vec, const FilterRo
 }
 
 template <typename LT>
-__global__ void __launch_bounds__(kFilterThreads, 1) filter_kernel(const FilterParams P)
+__global__ void __launch_bounds__(kFilterThreads, 2) filter_kernel(const FilterParams P)
 {
     using E = FilterElem<LT>;
     __shared__ FilterShared S;
