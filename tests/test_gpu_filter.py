@@ -45,6 +45,17 @@ def test_filter_parity(orc, V, n, dtype):
                 _check(orc, z, T, top_k, top_p)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_filter_wide_nucleus(orc, dtype):
+    """Nearly flat rows: the top-p set holds thousands of ids, more than the
+    fast path's shared-memory list, so the exact fallback decides."""
+    z = filter_rows.rows(11, 4, 32000, dtype, sigma=0.2)
+    for top_p in (0.5, 0.9):
+        _, kept, _ = _check(orc, z, 1.0, 0, top_p)
+        assert kept.max() > 2048
+        _check(orc, z, 1.0, 3000, top_p)   # top-k set larger than the list as well
+
+
 def test_filter_ties_flat_rows(orc):
     # every id the same value: the cuts fall among ties, decided by id
     z = np.zeros((3, 100000), np.float32)
