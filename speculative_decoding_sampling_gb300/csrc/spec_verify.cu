@@ -1,7 +1,9 @@
 // spec_verify.cu -- C ABI of the verification library: argument checks,
-// workspace layout, and the three launches (row pass, draw stream, final
-// draws) on the caller's stream, each chained to the one before by
-// programmatic dependent launch.  The operation itself is documented in spec_verify.h.
+// workspace layout, and the launches on the caller's stream -- the row
+// pass, the draw stream and, when the draw stream does not fill the GPU,
+// the final draws -- each chained to the one before by programmatic
+// dependent launch; and the top-k / top-p filter.  The operations
+// themselves are documented in spec_verify.h.
 #include "spec_verify.h"
 
 #include <cmath>
@@ -460,7 +462,7 @@ const char *sv_status_string(sv_status_t status)
 // workspace: a server whose device memory is reserved up front by its own
 // pool and that forbids cudaMalloc on the request path, or a plugin interface
 // that passes a plugin its input and output buffers but no allocator.  For
-// them, spec_verify_noalloc runs the same three kernels with their scratch in a
+// them, spec_verify_noalloc runs the same kernels with their scratch in a
 // fixed-size array that lives in the library's device image.  The array is
 // shared by every call on a device and keeps the last call's contents, so
 // each call clears the bytes it needs before launching; calls that overlap on
