@@ -28,9 +28,11 @@
  *   draft_probs = NULL; then a_k = min(1, p_k(x_k)) and r is p without x.
  *
  * Conventions for every entry point below:
- *   - All tensor pointers are DEVICE pointers, row-major and contiguous, owned
- *     by the caller.  The library allocates nothing and keeps no state beyond
- *     the caller's workspace; calls on distinct workspaces are independent.
+ *   - All tensor pointers are DEVICE pointers (inputs may also be mapped
+ *     page-locked host memory, see spec_verify), row-major and contiguous,
+ *     owned by the caller.  The library allocates nothing; its only state is
+ *     per-device cached occupancy figures and, for spec_verify_noalloc, one
+ *     static scratch array.  Calls on distinct workspaces are independent.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  A return of SV_OK means the work was enqueued.
  *   - Host-side checks run before anything is launched and return SV_EINVAL
