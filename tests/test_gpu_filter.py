@@ -109,3 +109,23 @@ def test_filter_then_verify(orc):
     assert np.array_equal(got, ref.logits)
     rep = parity.compare(orc, ref.logits, inp.q, inp.tokens, inp.u, inp.T, cand)
     assert rep.ok(), rep.summary()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_filter_in_place_scalar_path(orc, dtype):
+    # V odd: rows are not 16-byte groups, element loads; in place
+    z = filter_rows.rows(21, 6, 5001, dtype)
+    top_p = float(np.float32(0.9))
+    out_a, kept_a, _ = _gpu_filter(z.copy(), 0.8, 17, top_p)
+    out_b, kept_b, _ = _gpu_filter(z.copy(), 0.8, 17, top_p, in_place=True)
+    assert np.array_equal(out_a.view(np.uint8), out_b.view(np.uint8)) and np.array_equal(kept_a, kept_b)
+    rep = parity.compare_filter(orc, z, 0.8, 17, top_p, out_b, kept_b)
+    assert rep.ok(), rep.summary()
+
+
+def test_filter_largest_vocabulary(orc):
+    import speculative_decoding_sampling_gb300 as sv
+    V = sv.SV_MAX_V
+    z = filter_rows.rows(5, 2, V, "bf16")
+    _check(orc, z, 1.0, 0, 0.9)
+    _check(orc, z, 0.7, 1000, 0.95)
