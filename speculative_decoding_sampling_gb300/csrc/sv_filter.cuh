@@ -37,7 +37,8 @@
 
 namespace sv {
 
-constexpr int kFilterThreads = 512;
+constexpr int kFilterThreads = 256; // 4 CTAs per SM: rows spread over more CTA slots (384 rows of the
+                                      // top-p workload: 608 slots instead of 304, so no partial second wave)
 constexpr int kFilterWarps = kFilterThreads / 32;
 constexpr int kYBins = 512;       // coarse bins of y
 constexpr int kTieIds = 8;        // consecutive ids a thread owns in the ordered scan
@@ -469,7 +470,7 @@ __device__ Cut filter_resolve(const LT *row, int32_t V, bool vec, const FilterRo
 }
 
 template <typename LT>
-__global__ void __launch_bounds__(kFilterThreads, 2) filter_kernel(const FilterParams P)
+__global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const FilterParams P)
 {
     using E = FilterElem<LT>;
     __shared__ FilterShared S;
