@@ -26,6 +26,14 @@
  *     section 算完三个 token 的全部概率, the replay's sampler and final draw).
  *   A deterministic draft (n-gram, prompt lookup) is q = one-hot on x: pass
  *   draft_probs = NULL; then a_k = min(1, p_k(x_k)) and r is p without x.
+ *   A target that samples with top-k / top-p runs its raw logits through
+ *   sv_filter_logits first (same temperature); p is then the filtered,
+ *   renormalised distribution.
+ *
+ * Entry points: spec_verify (the whole step), spec_verify_stats (plus
+ * acceptance counters), sv_verify_rows / sv_sample_survivors (its two
+ * stages), spec_verify_noalloc (no workspace argument), sv_filter_logits
+ * (top-k / top-p), sv_workspace_bytes, sv_kernel_launches, sv_status_string.
  *
  * Conventions for every entry point below:
  *   - All tensor pointers are DEVICE pointers (inputs may also be mapped
