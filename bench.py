@@ -73,10 +73,12 @@ def algorithmic_bytes(w, num_emitted: np.ndarray) -> dict:
 
 
 def kernel_source_hash() -> str:
+    """Hash of the sources the verification kernels and their launches are
+    built from (every .cu/.cuh file but the top-k / top-p filter's)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_sampling_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
+        if f.endswith((".cu", ".cuh")) and f != "sv_filter.cuh":
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
