@@ -62,8 +62,11 @@ def sv_filter_logits(logits: torch.Tensor, temperature: float, top_k: int = 0, t
         raise ValueError("out must match logits")
     if kept is None:
         kept = torch.empty(logits.shape[:-1], dtype=torch.int32, device=logits.device)
-    if kept.numel() != rows or kept.dtype != torch.int32 or not kept.is_contiguous():
-        raise ValueError("kept must be int32 with one entry per row")
+    if kept.numel() != rows or kept.dtype != torch.int32 or not kept.is_contiguous() \
+            or kept.device != logits.device:
+        raise ValueError("kept must be a contiguous int32 tensor with one entry per row on the logits' device")
+    if status is not None:
+        _check(status, "status", torch.int32, (1,), logits.device)
     dt = N.SV_BF16 if logits.dtype == torch.bfloat16 else N.SV_FP32
     stream = torch.cuda.current_stream(logits.device).cuda_stream
     rc = N.lib().sv_filter_logits(logits.data_ptr(), dt, rows, V, float(temperature), int(top_k),

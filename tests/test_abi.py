@@ -127,3 +127,13 @@ def test_filter_sizes_and_empty():
     assert _filter(V=N.SV_MAX_V + 1) == N.SV_EUNSUPPORTED
     assert _filter(rows=0) == N.SV_OK
     assert _filter(rows=0, logits=None, out=None) == N.SV_OK
+
+
+def test_filter_binding_rejects_bad_tensors():
+    # checked in Python before the library is called: no GPU needed
+    import torch
+    x = torch.zeros(2, 8)                       # not a CUDA tensor
+    with pytest.raises(ValueError):
+        sv.sv_filter_logits(x, 1.0, 0, 0.9)
+    with pytest.raises(sv.SpecVerifyError):
+        sv.sv_filter_logits(torch.zeros(2, 8, dtype=torch.float16), 1.0, 0, 0.9)
