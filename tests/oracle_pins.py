@@ -623,6 +623,23 @@ def pin_filter_bruteforce_tiny(orc):
     assert checked > 2000
 
 
+def pin_filter_topk_matches_library_sort(orc):
+    """Top-k on rows of 5000 ids with many ties (values on a coarse grid):
+    the kept ids are the first k of numpy's stable sort by value descending
+    (equal values keep ascending id order)."""
+    rng = np.random.default_rng(23)
+    z = (np.round(rng.standard_normal((6, 5000)) * 4.0) / 2.0).astype(np.float32)
+    z[2, rng.random(5000) < 0.4] = -np.inf
+    for k in (1, 7, 100, 2999):
+        r = orc.filter_logits(z, 0.9, k, 1.0)
+        for row in range(z.shape[0]):
+            order = np.argsort(-z[row].astype(np.float64), kind="stable")
+            finite = order[np.isfinite(z[row][order])]
+            want = np.sort(finite[:k])
+            got = np.nonzero(np.isfinite(r.logits[row]))[0]
+            assert np.array_equal(got, want), (k, row)
+
+
 def pin_filter_matches_generator_nucleus(orc):
     """The input generator marks the top-p nucleus of the 64-sequence workload
     with its own sort (synth.c); the oracle's filter must mask the same ids."""
@@ -661,6 +678,7 @@ ALL_PINS = [
     pin_filter_temperature,
     pin_filter_masked_and_bad_rows,
     pin_filter_bruteforce_tiny,
+    pin_filter_topk_matches_library_sort,
     pin_filter_matches_generator_nucleus,
     pin_output_distribution,
     pin_expected_tokens,
