@@ -64,7 +64,7 @@ struct Params {
     // a completed call leaves the whole workspace zero-filled
     float2 *row_part;     // [R * PM]  (max of z, normaliser relative to it) per CTA a row falls in
     float4 *row_side;     // [R]       the row's draft token (int bits), z(x), q(x), u
-    int4 *seq_info;       // [B]       the verdict for the final kernel: j* (-1 = bad sequence), bits of the
+    int4 *seq_info;       // [B]       the verdict for the final draw: j* (-1 = bad sequence), bits of the
                           //           surviving row's max m and normaliser s, the rejected draft x (one-hot) or -1
     long long *seq_E;     // [B]       exact sum of pt over the surviving row (dense), 2^-fix_bits units
     uint32_t *seq_cnt;    // [B]       draw-stream chunks of the sequence folded so far (inline final draws)

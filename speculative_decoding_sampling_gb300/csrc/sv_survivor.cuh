@@ -398,7 +398,7 @@ __device__ __forceinline__ void draw_range(const Params &P, int64_t c0, int64_t 
     unsigned long long Ehi = E0, Elo = 0ull; // see fold_group
     auto flush = [&]() {
         // the dense rejection's share of its normaliser E = sum pt, in 2^-fb
-        // units; read by the final kernel
+        // units; read by the final draw
         if (DENSE) {
             float h0, h1, l0, l1;
             unpack2(Ehi, h0, h1);

@@ -24,7 +24,7 @@ struct Verdict {
 // time).  Deterministic: every warp that computes it gets the same answer.
 // With `write`, the warp also writes the sequence's accepted prefix, flags,
 // accept probabilities, count, status bits, and the surviving row's
-// statistics for the final kernel (exactly one warp per sequence does).
+// statistics for the final draw (exactly one warp per sequence does).
 template <typename LT, bool DENSE>
 __device__ Verdict seq_verdict(const Params &P, int64_t b, int lane, bool write)
 {
