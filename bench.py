@@ -75,13 +75,15 @@ def algorithmic_bytes(w, num_emitted: np.ndarray) -> dict:
 def kernel_source_hash() -> str:
     """Hash of the code the verification kernels and their launches are
     built from: every .cu/.cuh file but the top-k / top-p filter's, with
-    // comments and trailing blanks removed (they do not change a kernel)."""
+    // comments, trailing blanks and empty lines removed (they do not change
+    a kernel)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_sampling_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh")) and f != "sv_filter.cuh":
             with open(os.path.join(csrc, f), encoding="utf-8") as fh:
-                code = "\n".join(line.split("//", 1)[0].rstrip() for line in fh.read().splitlines())
+                lines = (line.split("//", 1)[0].rstrip() for line in fh.read().splitlines())
+                code = "\n".join(line for line in lines if line)
             h.update(f.encode() + b"\0" + code.encode())
     return h.hexdigest()[:16]
 
