@@ -73,14 +73,14 @@ def algorithmic_bytes(w, num_emitted: np.ndarray) -> dict:
 
 
 def kernel_source_hash() -> str:
-    """Hash of the code the verification kernels and their launches are
-    built from: every .cu/.cuh file but the top-k / top-p filter's, with
-    // comments, trailing blanks and empty lines removed (they do not change
-    a kernel)."""
+    """Hash of the device code of the verification kernels: every .cuh file
+    but the top-k / top-p filter's (the C ABI's host code in spec_verify.cu
+    is left out), with // comments, trailing blanks and empty lines removed
+    (they do not change a kernel)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_sampling_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")) and f != "sv_filter.cuh":
+        if f.endswith(".cuh") and f != "sv_filter.cuh":
             with open(os.path.join(csrc, f), encoding="utf-8") as fh:
                 lines = (line.split("//", 1)[0].rstrip() for line in fh.read().splitlines())
                 code = "\n".join(line for line in lines if line)
@@ -160,13 +160,169 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- GPU arm
 
+def config_of(w, world: int, filt: bool) -> dict:
+    """The `config` object of a bench line: what the workload is.  Both arms
+    print it from here, so the same workload gives the same dict."""
+    return {"workload": w.name, "B_per_gpu": w.B, "K": w.K, "V": w.V,
+            "logits_dtype": w.dtype, "draft": "one-hot ids" if w.onehot else "dense q fp32",
+            "temperature": w.T, "top_p": w.top_p or None,
+            "top_p_applied": ("on the GPU (sv_filter_logits, raw logits in)" if filt else
+                              ("by the input generator (masked logits in)" if w.top_p else None)),
+            "parallelism": f"replicas x{world} (shard over sequences)"}
+
+
+ROTATE_BYTES = 4 * L2_BYTES   # rotating copies: the bytes the steps between two uses of a copy read
+FLUSH_BELOW = 16 << 20        # steps reading less than this: L2 flush between eager calls instead
+
+
+class Rig:
+    """Device inputs of one workload (one or several copies), the outputs,
+    status, workspace and the public C-ABI call on a given copy."""
+
+    def __init__(self, torch, w, inp, dev, copies: int, logits_override=None):
+        import speculative_decoding_sampling_gb300 as sv
+        from speculative_decoding_sampling_gb300 import _native as N
+        self.torch, self.w, self.dev = torch, w, dev
+        self.lib = N.lib()
+        self.dt = N.SV_BF16 if w.dtype == "bf16" else N.SV_FP32
+        B, K, V = w.B, w.K, w.V
+        lg_host = inp.logits if logits_override is None else logits_override
+        host_lg = torch.from_numpy(lg_host.view(np.int16) if w.dtype == "bf16" else lg_host)
+        self.copies = []
+        for _ in range(copies):
+            lg = host_lg.to(dev)
+            if w.dtype == "bf16":
+                lg = lg.view(torch.bfloat16)
+            q = None if inp.q is None else torch.from_numpy(inp.q).to(dev)
+            self.copies.append((lg, q, torch.from_numpy(inp.tokens).to(dev), torch.from_numpy(inp.u).to(dev)))
+        self.out = {"out_tokens": torch.empty((B, K + 1), dtype=torch.int32, device=dev),
+                    "num_emitted": torch.empty((B,), dtype=torch.int32, device=dev),
+                    "accept_flags": torch.empty((B, K), dtype=torch.int8, device=dev),
+                    "accept_prob": torch.empty((B, K), dtype=torch.float32, device=dev),
+                    "residual_mass": torch.empty((B,), dtype=torch.float32, device=dev)}
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.need = sv.sv_workspace_bytes(B, K, V)
+        self.ws = torch.zeros(self.need, dtype=torch.uint8, device=dev)
+        self.sv = sv
+
+    def args(self, i, stream, logits=None):
+        lg, q, tok, u = self.copies[i]
+        lg = lg if logits is None else logits
+        w, o = self.w, self.out
+        return (lg.data_ptr(), self.dt, None if q is None else q.data_ptr(), tok.data_ptr(),
+                u.data_ptr(), ctypes.c_float(w.T), w.B, w.K, w.V, o["out_tokens"].data_ptr(),
+                o["num_emitted"].data_ptr(), o["accept_flags"].data_ptr(), o["accept_prob"].data_ptr(),
+                o["residual_mass"].data_ptr(), self.status.data_ptr(), self.ws.data_ptr(), self.need,
+                stream.cuda_stream)
+
+    def call(self, i, stream, logits=None):
+        rc = self.lib.spec_verify(*self.args(i, stream, logits))
+        if rc:
+            raise RuntimeError(self.sv.sv_status_string(rc))
+
+    def host_outputs(self):
+        return {k: v.cpu().numpy() for k, v in self.out.items()}
+
+
+def l2_rule(touched: int, flushed: bool, copies: int) -> str:
+    if flushed:
+        return (f"L2 flushed before every timed step (a {2 * L2_BYTES >> 20} MiB buffer written outside the "
+                f"timed events; eager calls): a step reads {touched / 1e6:.1f} MB")
+    if copies > 1:
+        return (f"{copies} rotating input copies, step i reads copy i mod {copies}: {copies} x "
+                f"{touched / 1e6:.0f} MB between two reads of a copy, over 4x the {L2_BYTES >> 20} MiB L2; "
+                "no flush")
+    return f"no flush: a step reads {touched / 1e6:.0f} MB, more than twice the {L2_BYTES >> 20} MiB L2"
+
+
+def time_steps(torch, rig, steps: int, step_fn, flushed: bool, dev):
+    """Device ms per step of `step_fn(i, stream)` (i = step number): CUDA
+    graphs of whole rotations replayed back to back, or, with the flush,
+    eager calls each between its own events."""
+    stream = torch.cuda.current_stream(dev)
+    n = len(rig.copies)
+    if flushed:
+        buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+        tev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i, (e0, e1) in enumerate(tev):
+            buf.fill_(1)
+            e0.record(stream)
+            step_fn(i % n, stream)
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return sum(e0.elapsed_time(e1) for e0, e1 in tev) / steps
+    per = n if n > 1 else GRAPH_STEPS
+    gstream = torch.cuda.Stream(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gstream):
+        for i in range(per):
+            step_fn(i % n, gstream)
+    rem = steps % per
+    graph_r = None
+    if rem:
+        graph_r = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_r, stream=gstream):
+            for i in range(rem):
+                step_fn(i % n, gstream)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(gstream):
+        t0.record(gstream)
+        for _ in range(steps // per):
+            graph.replay()
+        if graph_r is not None:
+            graph_r.replay()
+        t1.record(gstream)
+    torch.cuda.synchronize(dev)
+    return t0.elapsed_time(t1) / steps
+
+
+def measure_workload(torch, dev, name: str, steps: int, cpu_threads: int) -> dict:
+    """One of the five configurations: step time, algorithmic bytes, GB/s,
+    roofline fractions, the L2 rule, and parity of the outputs against the
+    fp64 oracle on the same inputs."""
+    import synth
+    import oracle
+    from oracle import parity
+    w = synth.WORKLOADS[name]
+    inp = synth.generate(w)
+    rig = Rig(torch, w, inp, dev, 1)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        rig.call(0, stream)
+    torch.cuda.synchronize(dev)
+    cand = rig.host_outputs()
+    nb = algorithmic_bytes(w, cand["num_emitted"])
+    touched = nb["total"]
+    flushed = touched < FLUSH_BELOW
+    copies = 1 if (flushed or touched >= 2 * L2_BYTES) else int(-(-ROTATE_BYTES // touched))
+    if copies > 1:
+        rig = Rig(torch, w, inp, dev, copies)
+    for i in range(3 * len(rig.copies)):
+        rig.call(i % len(rig.copies), stream)
+    ms = time_steps(torch, rig, steps, rig.call, flushed, dev)
+    orc = oracle.load()
+    rep = parity.compare(orc, inp.logits, inp.q, inp.tokens, inp.u, inp.T, rig.host_outputs(),
+                         oracle_res=orc.verify(inp.logits, inp.q, inp.tokens, inp.u, inp.T, nthreads=cpu_threads))
+    peak, _ = peaks()
+    gbs = touched / (ms * 1e-3) / 1e9
+    return {"step_us": ms * 1e3, "algorithmic_MB": touched / 1e6, "GB_per_s": gbs,
+            "frac_of_measured": gbs / peak, "frac_of_8TBs": gbs / NOMINAL_HBM_GBS,
+            "seqs_per_s": w.B / (ms * 1e-3), "launches_per_step": rig.sv.sv_kernel_launches(
+                torch.bfloat16 if w.dtype == "bf16" else torch.float32, inp.q is not None, w.B, w.K, w.V),
+            "l2": l2_rule(touched, flushed, len(rig.copies)), "steps": steps,
+            "status_bits": int(rig.status.item()),
+            "parity": {"ok": rep.ok(), "summary": rep.summary()}}
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
 
     import synth
     import speculative_decoding_sampling_gb300 as sv
-    from speculative_decoding_sampling_gb300 import _native as N
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -183,168 +339,98 @@ def run_gpu(args):
     # this rank's shard of the global batch: sequences [rank*B, (rank+1)*B)
     inp = synth.generate(w, b0=rank * B, nb=B)
     filt = bool(args.filter_top_p)
+    raw = None
     if filt:
         # the target's top-p applied on the GPU: raw logits in, the draft's
         # processed q, tokens and uniforms as generated
         if not w.top_p:
             raise SystemExit("--filter-top-p needs a workload with top-p")
-        inp.logits = synth.generate(w.with_(top_p=0.0), b0=rank * B, nb=B).logits
-    host = {"logits": torch.from_numpy(inp.logits.view(np.int16) if w.dtype == "bf16" else inp.logits),
-            "q": None if inp.q is None else torch.from_numpy(inp.q),
-            "tokens": torch.from_numpy(inp.tokens), "u": torch.from_numpy(inp.u)}
-    d_logits = host["logits"].to(dev)
-    if w.dtype == "bf16":
-        d_logits = d_logits.view(torch.bfloat16)
-    d_q = None if host["q"] is None else host["q"].to(dev)
-    d_tok = host["tokens"].to(dev)
-    d_u = host["u"].to(dev)
-    out = {"out_tokens": torch.empty((B, K + 1), dtype=torch.int32, device=dev),
-           "num_emitted": torch.empty((B,), dtype=torch.int32, device=dev),
-           "accept_flags": torch.empty((B, K), dtype=torch.int8, device=dev),
-           "accept_prob": torch.empty((B, K), dtype=torch.float32, device=dev),
-           "residual_mass": torch.empty((B,), dtype=torch.float32, device=dev)}
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    need = sv.sv_workspace_bytes(B, K, V)
-    ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+        raw = synth.generate(w.with_(top_p=0.0), b0=rank * B, nb=B).logits
+    rig = Rig(torch, w, inp, dev, 1, logits_override=raw)
     stream = torch.cuda.current_stream(dev)
-    lib = N.lib()
-    dt = N.SV_BF16 if w.dtype == "bf16" else N.SV_FP32
-
-    def args_for(logits, q, tok, u, o):
-        return (logits.data_ptr(), dt, None if q is None else q.data_ptr(), tok.data_ptr(),
-                u.data_ptr(), ctypes.c_float(w.T), B, K, V, o["out_tokens"].data_ptr(),
-                o["num_emitted"].data_ptr(), o["accept_flags"].data_ptr(),
-                o["accept_prob"].data_ptr(), o["residual_mass"].data_ptr(), status.data_ptr(),
-                ws.data_ptr(), need, stream.cuda_stream)
-
-    d_filt = torch.empty_like(d_logits) if filt else None
-    d_kept = torch.empty(B * (K + 1), dtype=torch.int32, device=dev) if filt else None
     top_p32 = float(np.float32(w.top_p)) if filt else 1.0
-    cargs = args_for(d_filt if filt else d_logits, d_q, d_tok, d_u, out)
+    d_filt = torch.empty_like(rig.copies[0][0]) if filt else None
+    d_kept = torch.empty(B * (K + 1), dtype=torch.int32, device=dev) if filt else None
 
-    def filter_call(s):
-        rc = lib.sv_filter_logits(d_logits.data_ptr(), dt, B * (K + 1), V, ctypes.c_float(w.T), 0,
-                                  ctypes.c_float(top_p32), d_filt.data_ptr(), d_kept.data_ptr(),
-                                  status.data_ptr(), s.cuda_stream)
+    def filter_call(i, s):
+        rc = rig.lib.sv_filter_logits(rig.copies[i][0].data_ptr(), rig.dt, B * (K + 1), V, ctypes.c_float(w.T), 0,
+                                      ctypes.c_float(top_p32), d_filt.data_ptr(), d_kept.data_ptr(),
+                                      rig.status.data_ptr(), s.cuda_stream)
         if rc:
             raise RuntimeError(sv.sv_status_string(rc))
 
-    def step(s):
-        # one call = the launches of the path (row pass, draw stream and,
-        # unless the draw stream makes them, the final draws), each chained
-        # to the one before by programmatic dependent launch; with
-        # --filter-top-p the filter launch comes first
+    def step(i, s):
+        # one step = the public call: the row pass, the draw stream and, unless
+        # the draw stream makes them, the final draws, each chained to the one
+        # before by programmatic dependent launch; with --filter-top-p the
+        # filter launch comes first
         if filt:
-            filter_call(s)
-        rc = lib.spec_verify(*cargs[:-1], s.cuda_stream)
-        if rc:
-            raise RuntimeError(sv.sv_status_string(rc))
-
-    def staged_step(evs, fev=None):
-        # the same launches through the per-stage entry points, with events
-        # between the row pass and the draws (this breaks the launch chaining
-        # there, so it is used for per-kernel durations only)
-        if fev is not None:
-            fev[0].record(stream)
-            filter_call(stream)
-            fev[1].record(stream)
-        evs[0].record(stream)
-        rc = lib.sv_verify_rows(*cargs)
-        evs[1].record(stream)
-        rc |= lib.sv_sample_survivors(*cargs)
-        evs[2].record(stream)
-        if rc:
-            raise RuntimeError(sv.sv_status_string(rc))
+            filter_call(i, s)
+            rig.call(i, s, logits=d_filt)
+        else:
+            rig.call(i, s)
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    # warm-up
     for _ in range(max(args.warmup, 3)):
-        step(stream)
+        step(0, stream)
     barrier()
 
     # bytes one step reads: every logit, the surviving rows again, the
-    # rejected rows' draft probabilities.  Below twice the L2 size, the L2 is
-    # flushed before every timed step, outside the timed events, so no step
-    # finds its inputs cached by the step before.
-    touched = algorithmic_bytes(w, out["num_emitted"].cpu().numpy())["total"]
-    flush_l2 = {"auto": touched < 2 * L2_BYTES, "on": True, "off": False}[args.l2_flush]
-    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev) if flush_l2 else None
-
-    def flush(s):
-        # write a buffer of twice the L2: no input of the step stays cached
-        if flush_buf is not None:
-            with torch.cuda.stream(s):
-                flush_buf.fill_(1)
+    # rejected rows' draft probabilities (and the filter's read and write)
+    touched = algorithmic_bytes(w, rig.out["num_emitted"].cpu().numpy())["total"]
+    if filt:
+        touched += 2 * B * (K + 1) * V * (2 if w.dtype == "bf16" else 4)
+    flushed = {"auto": touched < FLUSH_BELOW, "on": True, "off": False}[args.l2_flush]
+    copies = 1 if (flushed or touched >= 2 * L2_BYTES or args.l2_flush == "off") else int(-(-ROTATE_BYTES // touched))
+    if copies > 1:
+        rig = Rig(torch, w, inp, dev, copies, logits_override=raw)
+        for i in range(3 * copies):
+            step(i, stream)
     launches_per_step = sv.sv_kernel_launches(
-        torch.bfloat16 if w.dtype == "bf16" else torch.float32, d_q is not None, B, K, V) + (1 if filt else 0)
-
-    # the public call captured in CUDA graphs, GRAPH_STEPS consecutive calls
-    # (steps) per graph plus a one-call graph for the remainder: the timed
-    # region replays them, so host launch overhead and the gap between graph
-    # launches stay out of the device timing
-    gstream = torch.cuda.Stream(dev)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=gstream):
-        for _ in range(GRAPH_STEPS):
-            step(gstream)
-    graph1 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph1, stream=gstream):
-        step(gstream)
-    graph.replay()
-    graph1.replay()
+        torch.bfloat16 if w.dtype == "bf16" else torch.float32, inp.q is not None, B, K, V) + (1 if filt else 0)
     barrier()
 
-    # ---- timed region: exactly K steps of the public call (graph replays;
-    # with the L2 flush, eager calls, each between its own events)
+    # ---- timed region: exactly K steps of the public call
     clocks = ClockSampler(local)
     clocks.start()
     barrier()
-    if flush_l2:
-        tev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        # eager calls: the host enqueues each call while the flush before it
-        # runs, so the events see the call's device time alone
-        for e0, e1 in tev:
-            flush(stream)
-            e0.record(stream)
-            step(stream)
-            e1.record(stream)
-        barrier()
-        ms_step = sum(e0.elapsed_time(e1) for e0, e1 in tev) / args.steps
-    else:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(gstream):
-            t_start.record(gstream)
-            for _ in range(args.steps // GRAPH_STEPS):
-                graph.replay()
-            for _ in range(args.steps % GRAPH_STEPS):
-                graph1.replay()
-            t_end.record(gstream)
-        barrier()
-        ms_step = t_start.elapsed_time(t_end) / args.steps
+    ms_step = time_steps(torch, rig, args.steps, step, flushed, dev)
+    barrier()
 
     # the same K steps as eager calls from the host (for reference)
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
-    for _ in range(args.steps):
-        step(stream)
+    for i in range(args.steps):
+        step(i % copies, stream)
     e_end.record(stream)
     barrier()
     ms_step_eager = e_start.elapsed_time(e_end) / args.steps
 
-    # ---- per-kernel durations: the same launches, events between them
+    # ---- per-kernel durations: the stages through their own entry points,
+    # events between them (this breaks the launch chaining there, so it is
+    # used for per-kernel durations only)
     n_k = max(20, min(args.steps, 500))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_k)]
     fevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_k)] if filt else None
     for i in range(n_k):
-        flush(stream)
-        staged_step(evs[i], fevs[i] if filt else None)
+        c = i % copies
+        if filt:
+            fevs[i][0].record(stream)
+            filter_call(c, stream)
+            fevs[i][1].record(stream)
+        a = rig.args(c, stream, logits=d_filt if filt else None)
+        evs[i][0].record(stream)
+        rc = rig.lib.sv_verify_rows(*a)
+        evs[i][1].record(stream)
+        rc |= rig.lib.sv_sample_survivors(*a)
+        evs[i][2].record(stream)
+        if rc:
+            raise RuntimeError(sv.sv_status_string(rc))
     barrier()
     clk = clocks.stop()
     rows_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / n_k
@@ -355,8 +441,8 @@ def run_gpu(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_step = float(t.item())
 
-    num_emitted = out["num_emitted"].cpu().numpy()
-    st = int(status.item())
+    num_emitted = rig.out["num_emitted"].cpu().numpy()
+    st = int(rig.status.item())
     tokens_per_step = int(num_emitted.sum())
     nbytes = algorithmic_bytes(w, num_emitted)
     if filt:   # the filter reads every logit once and writes every logit once
@@ -367,65 +453,30 @@ def run_gpu(args):
     surv_gbs = nbytes["draw_kernels"] / (surv_ms * 1e-3) / 1e9
     step_gbs = nbytes["total"] / (ms_step * 1e-3) / 1e9
 
-    # ---- end to end through the public call with pinned host buffers: the
-    # logits (every one is read), tokens and uniforms are copied to the device
-    # each step; the draft probabilities stay in page-locked host memory and
-    # the kernels read them in place, so only the rejected rows and the
-    # drafted entries cross the host link
-    e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 20))
-    pin = {k: (v.pin_memory() if (v is not None and e2e_steps) else v) for k, v in host.items()}
-    h_out = {"out_tokens": torch.empty((B, K + 1), dtype=torch.int32).pin_memory(),
-             "num_emitted": torch.empty((B,), dtype=torch.int32).pin_memory()}
-    h2d = sum(pin[k].numel() * pin[k].element_size() for k in ("logits", "tokens", "u"))
-    if pin.get("q") is not None:   # q bytes read in place: rejected rows, one sector per drafted entry
-        h2d += rejected_rows_now(out, K) * V * 4 + B * K * 32
-    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
-    e_logits = torch.empty_like(host["logits"], device=dev) if e2e_steps else None
-    e_tok = torch.empty_like(d_tok)
-    e_u = torch.empty_like(d_u)
-
-    def e2e_step():
-        e_logits.copy_(pin["logits"], non_blocking=True)
-        e_tok.copy_(pin["tokens"], non_blocking=True)
-        e_u.copy_(pin["u"], non_blocking=True)
-        lg = e_logits.view(torch.bfloat16) if w.dtype == "bf16" else e_logits
-        if filt:
-            sv.sv_filter_logits(lg, w.T, 0, top_p32, out=lg, kept=d_kept, status=status)
-        res = sv.spec_verify(lg, pin.get("q"), e_tok, e_u, w.T, out=out, workspace=ws, status=status)
-        h_out["out_tokens"].copy_(res.out_tokens, non_blocking=True)
-        h_out["num_emitted"].copy_(res.num_emitted, non_blocking=True)
-
-    e2e_ms = float("nan")
-    if e2e_steps:
-        for _ in range(3):   # the host pages read in place get their device mappings on first touch
-            e2e_step()
-        barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
-        barrier()
-        e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e = None if args.no_e2e else run_e2e(torch, w, inp, rig, raw, filt, top_p32, d_kept, dev, args, world)
 
     result = None
     if rank == 0:
         seqs = B * world
         cpu = None
         parity_note = None
+        out_host = rig.host_outputs()
         if not args.no_cpu_baseline:
             fl = None
             if filt:
                 f = d_filt.cpu()
                 f = f.view(torch.int16).numpy().view(np.uint16) if w.dtype == "bf16" else f.numpy()
                 fl = (f, d_kept.cpu().numpy())
-            cpu, parity_note = cpu_baseline_and_check(w, inp, out, args.cpu_seconds,
-                                                      top_p=top_p32 if filt else None, filtered=fl)
+            cpu, parity_note = cpu_baseline_and_check(w, inp, out_host, args.cpu_seconds,
+                                                      top_p=top_p32 if filt else None, filtered=fl,
+                                                      raw_logits=raw)
+        workloads = None
+        if args.workloads:
+            cores = os.cpu_count() or 1
+            workloads = {}
+            for name in synth.WORKLOADS:
+                workloads[name] = measure_workload(torch, dev, name, min(args.steps, 300), cores)
+        config = config_of(w, world, filt)
         result = {
             "metric": METRIC,
             "value": seqs / (ms_step * 1e-3),
@@ -440,27 +491,17 @@ def run_gpu(args):
             "dtype": "f32",
             "data": "synthetic (seeded Philox4x32-10 generator; shapes and value "
                     "distributions of the workload; no model weights or datasets)",
-            "config": {"workload": w.name, "B_per_gpu": B, "K": K, "V": V,
-                       "logits_dtype": w.dtype, "draft": "one-hot ids" if w.onehot else "dense q fp32",
-                       "temperature": w.T, "top_p": w.top_p or None,
-                       "top_p_applied": ("on the GPU (sv_filter_logits, raw logits in)" if filt else
-                                         ("by the input generator (masked logits in)" if w.top_p else None)),
-                       "l2": (f"L2 flushed before every timed step (a {2 * L2_BYTES >> 20} MiB buffer written "
-                              f"outside the timed events): a step reads {touched / 1e6:.0f} MB, "
-                              f"under twice the {L2_BYTES >> 20} MiB L2") if flush_l2 else
-                             (f"no flush: a step reads {touched / 1e6:.0f} MB, "
-                              + ("more than twice" if touched >= 2 * L2_BYTES else "UNDER twice (flush off by flag)")
-                              + f" the {L2_BYTES >> 20} MiB L2"),
-                       "parallelism": f"replicas x{world} (shard over sequences)"},
+            "config": config,
+            "l2": l2_rule(touched, flushed, copies),
             "tokens_per_s": tokens_per_step * world / (ms_step * 1e-3),
             "hbm_gbs_step": step_gbs,
             "hbm_frac_step": {"of_measured": step_gbs / peak, "of_8tbs_nominal": step_gbs / NOMINAL_HBM_GBS},
             "ms_per_step_eager": ms_step_eager,
             "timing": (("the public C-ABI call issued from the host, each call between its own CUDA "
-                        "events, the L2 flush before each (enqueued while the flush runs)") if flush_l2 else
-                       (f"CUDA-graph replay of the public C-ABI call ({GRAPH_STEPS} consecutive calls per "
-                        "replay, the remainder one call per replay)")) +
-                      "; ms_per_step_eager: the same K calls issued back to back from the host, no flush",
+                        "events, the L2 flush before each (enqueued while the flush runs)") if flushed else
+                       ("CUDA-graph replay of the public C-ABI call, back to back (one graph holds a whole "
+                        "rotation of input copies, or %d calls)" % GRAPH_STEPS)) +
+                      "; ms_per_step_eager: the same K calls issued back to back from the host",
             "kernels_ms": {"rows_kernel": rows_ms, "survivor_kernel+final_kernel": surv_ms,
                            "source": f"{n_k} staged calls with CUDA events between the row pass and the draws"},
             "kernels_gbs": {"rows_kernel": rows_gbs, "survivor_kernel+final_kernel": surv_gbs},
@@ -474,15 +515,14 @@ def run_gpu(args):
                          "achieved": rows_gbs, "peak": peak, "unit": "GB/s",
                          "frac": rows_gbs / peak, "peak_source": peak_kind,
                          "traffic": recorded_traffic(w.name, "rows_kernel")},
-            "e2e": ({"value": seqs / (e2e_ms * 1e-3), "unit": "seqs/s",
-                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
-                     "d2h_bytes_per_step": d2h, "steps": e2e_steps} if e2e_steps else None),
+            "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "gpu_launches_per_step": launches_per_step,
             "clocks": clk,
             "status_bits": st,
             "cpu_baseline": cpu,
             "parity": parity_note,
+            "workloads": workloads,
         }
     if world > 1:
         dist.barrier()
@@ -490,7 +530,91 @@ def run_gpu(args):
     return result
 
 
-def cpu_baseline_and_check(w, inp, out, seconds, top_p=None, filtered=None):
+def run_e2e(torch, w, inp, rig, raw, filt, top_p32, d_kept, dev, args, world):
+    """The same metric end to end through the Python API from pinned host
+    buffers: every step copies its logits, tokens and uniforms host -> device
+    and its results device -> host; q stays in page-locked memory and the
+    kernels read it in place (only the rejected rows and the drafted entries
+    cross the link).  Two device input buffers alternate, so step i+1's
+    copy (on a copy stream) overlaps step i's verification and result copy."""
+    import speculative_decoding_sampling_gb300 as sv
+    B, K = w.B, w.K
+    steps = max(3, min(args.steps, 20))
+    lg_np = inp.logits if raw is None else raw
+    host_lg = torch.from_numpy(lg_np.view(np.int16) if w.dtype == "bf16" else lg_np).pin_memory()
+    pin = {"logits": host_lg, "tokens": torch.from_numpy(inp.tokens).pin_memory(),
+           "u": torch.from_numpy(inp.u).pin_memory(),
+           "q": None if inp.q is None else torch.from_numpy(inp.q).pin_memory()}
+    h_out = [{"out_tokens": torch.empty((B, K + 1), dtype=torch.int32).pin_memory(),
+              "num_emitted": torch.empty((B,), dtype=torch.int32).pin_memory()} for _ in range(2)]
+    h2d = sum(pin[k].numel() * pin[k].element_size() for k in ("logits", "tokens", "u"))
+    if pin["q"] is not None:   # q bytes read in place: rejected rows, one sector per drafted entry
+        h2d += int((rig.out["num_emitted"] <= K).sum().item()) * w.V * 4 + B * K * 32
+    d2h = sum(v.numel() * v.element_size() for v in h_out[0].values())
+    bufs = [{"logits": torch.empty_like(host_lg, device=dev), "tokens": torch.empty_like(pin["tokens"], device=dev),
+             "u": torch.empty_like(pin["u"], device=dev)} for _ in range(2)]
+    outs = [{k: torch.empty_like(v) for k, v in rig.out.items()} for _ in range(2)]
+    ws = [rig.ws, torch.zeros_like(rig.ws)]
+    comp = torch.cuda.current_stream(dev)
+    cps = torch.cuda.Stream(dev)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_step(i):
+        sl = i % 2
+        cps.wait_event(consumed[sl])           # the verification two steps back is done with this buffer
+        with torch.cuda.stream(cps):
+            for k in ("logits", "tokens", "u"):
+                bufs[sl][k].copy_(pin[k], non_blocking=True)
+            copied[sl].record(cps)
+        comp.wait_event(copied[sl])
+        lg = bufs[sl]["logits"].view(torch.bfloat16) if w.dtype == "bf16" else bufs[sl]["logits"]
+        if filt:
+            sv.sv_filter_logits(lg, w.T, 0, top_p32, out=lg, kept=d_kept, status=rig.status)
+        o = outs[sl]
+        sv.spec_verify(lg, pin["q"], bufs[sl]["tokens"], bufs[sl]["u"], w.T, workspace=ws[sl],
+                       status=rig.status, out=o)
+        h_out[sl]["out_tokens"].copy_(o["out_tokens"], non_blocking=True)
+        h_out[sl]["num_emitted"].copy_(o["num_emitted"], non_blocking=True)
+        consumed[sl].record(comp)
+
+    for i in range(4):   # the host pages read in place get their device mappings on first touch
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(comp)
+    cps.wait_event(e0)
+    for i in range(steps):
+        e2e_step(i)
+    e1.record(comp)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    # the link on its own: the step's logits copied host -> device, pinned
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(cps):
+        c0.record(cps)
+        for _ in range(3):
+            bufs[0]["logits"].copy_(pin["logits"], non_blocking=True)
+        c1.record(cps)
+    torch.cuda.synchronize(dev)
+    link_peak = 3 * pin["logits"].numel() * pin["logits"].element_size() / (c0.elapsed_time(c1) * 1e-3) / 1e9
+    link = h2d / (ms * 1e-3) / 1e9
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": B * world / (ms * 1e-3), "unit": "seqs/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "link_gbs": link, "link_peak_gbs": link_peak, "link_frac": link / link_peak,
+            "how": "two alternating device input buffers: step i+1's host->device copy on a copy stream "
+                   "overlaps step i's verification and result copy; link_peak_gbs = the same logits "
+                   "copied host->device alone"}
+
+
+def cpu_baseline_and_check(w, inp, out, seconds, top_p=None, filtered=None, raw_logits=None):
     """Time the oracle as it stands on this host's cores over the whole batch
     (repeated until `seconds` elapse) and check the GPU outputs against it.
     With `top_p`, the oracle filters the raw logits first (part of the timed
@@ -503,9 +627,10 @@ def cpu_baseline_and_check(w, inp, out, seconds, top_p=None, filtered=None):
     passes = 0
     ref = None
     logits = inp.logits
+    raw = inp.logits if raw_logits is None else raw_logits
     while True:
         if top_p is not None:
-            logits = orc.filter_logits(inp.logits, inp.T, 0, top_p, nthreads=cores).logits
+            logits = orc.filter_logits(raw, inp.T, 0, top_p, nthreads=cores).logits
         ref = orc.verify(logits, inp.q, inp.tokens, inp.u, inp.T, nthreads=cores)
         passes += 1
         if time.perf_counter() - t0 >= seconds:
@@ -517,7 +642,7 @@ def cpu_baseline_and_check(w, inp, out, seconds, top_p=None, filtered=None):
     while True:
         lg1 = inp.logits
         if top_p is not None:
-            lg1 = orc.filter_logits(inp.logits, inp.T, 0, top_p, nthreads=1).logits
+            lg1 = orc.filter_logits(raw, inp.T, 0, top_p, nthreads=1).logits
         orc.verify(lg1, inp.q, inp.tokens, inp.u, inp.T, nthreads=1)
         passes1 += 1
         if time.perf_counter() - t1 >= seconds / 2:
@@ -526,7 +651,7 @@ def cpu_baseline_and_check(w, inp, out, seconds, top_p=None, filtered=None):
     cand = {k: (out[k].cpu().numpy() if hasattr(out[k], "cpu") else np.asarray(out[k])) for k in out}
     note = {}
     if top_p is not None:
-        frep = parity.compare_filter(orc, inp.logits, inp.T, 0, top_p, filtered[0], filtered[1])
+        frep = parity.compare_filter(orc, raw, inp.T, 0, top_p, filtered[0], filtered[1])
         note["filter"] = {"ok": frep.ok(), "summary": frep.summary()}
         if frep.excused:   # verify what the GPU actually filtered
             logits = filtered[0].reshape(logits.shape)
@@ -578,8 +703,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B_per_gpu": w.B, "K": w.K, "V": w.V,
-                   "logits_dtype": w.dtype, "draft": "one-hot ids" if w.onehot else "dense q fp32"},
+        "config": config_of(w, world, bool(args.filter_top_p)),
         "cpu_baseline": {"value": value, "unit": "seqs/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "seqs/s", "h2d_bytes_per_step": 0,
@@ -602,7 +726,11 @@ def main():
     ap.add_argument("--filter-top-p", action="store_true",
                     help="top-p workloads: raw logits, the target's top-p applied by sv_filter_logits in the step")
     ap.add_argument("--l2-flush", default="auto", choices=["auto", "on", "off"],
-                    help="flush L2 before every timed step (auto: when a step reads under 2x L2)")
+                    help="auto: steps reading under 16 MB flush L2 between eager calls, steps reading under "
+                         "2x L2 rotate input copies (4x L2 between two reads of a copy), larger steps neither; "
+                         "on: always flush; off: neither")
+    ap.add_argument("--no-workloads", dest="workloads", action="store_false",
+                    help="skip the per-configuration `workloads` object (all five configs, parity included)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -200,9 +200,11 @@ sv_status_t sv_sample_survivors(
  *   - Returns SV_EUNSUPPORTED when sv_workspace_bytes(B, K, V) exceeds
  *     SV_NOALLOC_SCRATCH_BYTES (4 MiB holds, e.g., B = 256, K = 8 at V = 151936).
  *   - Calls no cudaMalloc / cudaFree and no allocating library routine.
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *   - Every call looks up the array's device address in the current
+ *     context (cudaGetSymbolAddress, host-side and cheap), so the address
+ *     stays right after a context is destroyed and made again.  The first
+ *     call on a device may also load the library's device code into the
+ *     context; make that first call before any stream capture.
  *   - Every call on a device shares the one array: each call clears the
  *     bytes it uses (an asynchronous memset on `stream`) and then launches.
  *     Calls whose work may overlap on the GPU (different streams or host

@@ -174,12 +174,18 @@ def _call(fn_name: str, target_logits, draft_probs, draft_tokens, uniforms,
     need = sv_workspace_bytes(B, K, V)
     if need == 0 and B > 0:
         raise SpecVerifyError(N.SV_EUNSUPPORTED)
-    if workspace is None:
-        workspace = default_workspace(dev, need)
-    elif workspace.device != dev or workspace.numel() * workspace.element_size() < need:
-        raise ValueError(f"workspace must hold {need} bytes on {dev}")
     if stream is None:
         stream = torch.cuda.current_stream(dev)
+    if workspace is None:
+        workspace = default_workspace(dev, need)
+        # the shared workspace was allocated on the stream current at the time;
+        # when this call runs on another one, the caching allocator must not
+        # hand the memory out again (after a larger workspace replaces it)
+        # before this call's kernels are done with it
+        if stream != torch.cuda.current_stream(dev):
+            workspace.record_stream(stream)
+    elif workspace.device != dev or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must hold {need} bytes on {dev}")
     args = [target_logits.data_ptr(), dt, _ptr(draft_probs), _ptr(draft_tokens),
             uniforms.data_ptr(), float(temperature), B, K, V, _ptr(out_tokens),
             _ptr(num_emitted), _ptr(accept_flags), _ptr(accept_prob),

@@ -8,6 +8,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <mutex>
 
@@ -75,10 +76,46 @@ enum Stage { kRows = 1, kSurvivors = 2, kBoth = 3 };
 
 constexpr int kMaxDevices = 64;
 
+// The current context's process-unique id, or 0 when none can be had (no
+// context current yet, or a driver without the query).  The driver calls
+// are reached through the runtime's entry-point lookup, so the library does
+// not link the driver library itself.
+unsigned long long current_context_id()
+{
+    using GetCurrent = CUresult (*)(CUcontext *);
+    using GetId = CUresult (*)(CUcontext, unsigned long long *);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(f);
+        (void)cudaGetLastError();
+    });
+    if (!get_current || !get_id)
+        return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
 // Per device and kernel instantiation: how many CTAs of each kernel fit on
-// the device at once (the grids of the persistent kernels).
+// the device at once (the grids of the persistent kernels).  Cached per
+// device for the context the figures were taken in: a context created anew
+// (after cudaDeviceReset, or a caller's own context) has forgotten the draw
+// kernel's shared-memory attribute, so the figures are taken again there.
 struct Resident {
     int rows, draw;
+    unsigned long long ctx; // context id the entry was made in (0: none)
 };
 
 template <typename LT, bool DENSE>
@@ -92,8 +129,9 @@ cudaError_t resident_ctas(Resident &out)
         return e;
     if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(mu);
-    if (cache[dev].rows == 0) {
+    if (cache[dev].rows == 0 || cache[dev].ctx == 0 || cache[dev].ctx != ctx) {
         int sms = 0, rows = 0, draw = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess)
@@ -112,6 +150,7 @@ cudaError_t resident_ctas(Resident &out)
         sms = sms > 0 ? sms : 1;
         cache[dev].rows = (rows > 0 ? rows : 1) * sms;
         cache[dev].draw = (draw > 0 ? draw : 1) * sms;
+        cache[dev].ctx = current_context_id(); // taken after the calls above made the context current
     }
     out = cache[dev];
     return cudaSuccess;
@@ -471,33 +510,25 @@ const char *sv_status_string(sv_status_t status)
 
 namespace {
 constexpr size_t kNoallocScratchBytes = SV_NOALLOC_SCRATCH_BYTES;
-constexpr int kNoallocMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[kNoallocMaxDevices] = {};
 } // namespace
 
 // Every GPU that loads this library holds this array until the process exits.
 static __device__ __align__(256) unsigned char g_sv_noalloc_scratch[kNoallocScratchBytes];
 
 namespace {
-// The device address of the scratch array on the current device.  The host
-// symbol is only a stand-in for the array, so the address is looked up once
-// per device (with that device current) and cached.
+// The device address of the scratch array in the current context.  In host
+// code the array's name is only a stand-in, so the address is looked up
+// with the device current, on every call: the lookup is host-side and
+// cheap, and a kept address would go stale when the context is destroyed
+// and made again (cudaDeviceReset), which places the module anew.
 sv_status_t noalloc_scratch(void **out)
 {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_sv_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        (void)cudaGetLastError();
         return SV_ECUDA;
-    if (dev < 0 || dev >= kNoallocMaxDevices)
-        return SV_EUNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (g_noalloc_ptr[dev] == nullptr) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_sv_noalloc_scratch) != cudaSuccess || p == nullptr)
-            return SV_ECUDA;
-        g_noalloc_ptr[dev] = p;
     }
-    *out = g_noalloc_ptr[dev];
+    *out = p;
     return SV_OK;
 }
 } // namespace

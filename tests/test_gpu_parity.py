@@ -280,7 +280,8 @@ def test_pinned_host_inputs_read_in_place(orc, where):
 
 def test_acceptance_statistics_counters(orc):
     """spec_verify_stats: the verdicts' counters equal those counted from the
-    outputs, add up over calls, and leave out sequences with bad data."""
+    fp64 oracle's outputs on the same inputs, add up over calls, and leave
+    out sequences with bad data."""
     import speculative_decoding_sampling_gb300 as sv
     from speculative_decoding_sampling_gb300.adaptive import RoundStats, stats_buffer
     w = synth.WORKLOADS["b8_k4_v32000_bf16"].with_(B=40, V=3000)
@@ -293,7 +294,14 @@ def test_acceptance_statistics_counters(orc):
     res = sv.spec_verify(lg, q, tok, u, inp.T, status=status, stats=stats)
     sv.spec_verify(lg, q, tok, u, inp.T, status=status, stats=stats)
     torch.cuda.synchronize()
-    n = res.num_emitted.cpu().numpy()
+    ref = orc.verify(inp.logits, inp.q, inp.tokens, inp.u, inp.T)
+    rep = parity.compare(orc, inp.logits, inp.q, inp.tokens, inp.u, inp.T,
+                         {"out_tokens": res.out_tokens.cpu().numpy(), "num_emitted": res.num_emitted.cpu().numpy(),
+                          "accept_flags": res.accept_flags.cpu().numpy(),
+                          "accept_prob": res.accept_prob.cpu().numpy(),
+                          "residual_mass": res.residual_mass.cpu().numpy()}, oracle_res=ref)
+    assert rep.ok() and rep.excused == 0, rep.summary()   # every accept test decided as the oracle did
+    n = ref.num_emitted.astype(np.int64)                  # the counts come from the oracle's outputs
     ok = n > 0
     assert not ok[3] and ok.sum() == B - 1
     s = RoundStats.from_counters(stats.cpu())
@@ -317,3 +325,58 @@ def test_kernel_launch_count():
     assert sv.sv_kernel_launches(torch.bfloat16, True, 8, 4, 32000) == 3
     assert sv.sv_kernel_launches(torch.float32, True, 1, 4, 32000) == 3
     assert sv.sv_kernel_launches(torch.bfloat16, True, 0, 4, 32000) == 0
+
+
+def test_worked_example_on_the_gpu(orc):
+    """The pages' worked example ("推测解码：草稿、验证与实际加速", section
+    算完三个 token 的全部概率) through the CUDA path: logits = ln p at T = 1,
+    p = (1/2, 3/10, 1/5) and q = (3/5, 1/10, 3/10) at every position, drafts
+    A, C, B, draws 7/10, 9/10, 1/5 and final draw 1/5: A passes at 5/6, C fails
+    at 2/3, B is never reached, and the correction from the residual (0, 1, 0)
+    is B -- [A, B] emitted (tests/golden/worked_example.txt)."""
+    from fractions import Fraction as F
+    from oracle_pins import read_golden
+    g = read_golden("worked_example.txt")
+    ids = {name: i for i, name in enumerate(g["tokens"])}
+    p = np.array([float(F(x)) for x in g["p"]])
+    q = np.array([float(F(x)) for x in g["q"]], np.float32)
+    draft = [ids[x] for x in g["draft"]]
+    K = len(draft)
+    u = np.array([[float(F(x)) for x in g["draws"]] + [float(F(g["final_draw"][0]))]], np.float32)
+    logits = np.log(p).astype(np.float32)[None, None].repeat(K + 1, 1)
+    inp = synth.Inputs(None, logits, q[None, None].repeat(K, 1).copy(), np.array([draft], np.int32), u, 1.0)
+    cand = G.run_inputs(inp)
+    emit = [ids[x] for x in g["emit"]]
+    assert cand["status"] == 0
+    assert cand["num_emitted"][0] == len(emit)
+    assert list(cand["out_tokens"][0]) == emit + [-1] * (K + 1 - len(emit))
+    assert list(cand["accept_flags"][0]) == [1, 0, -1]
+    a = [float(F(x)) for x in g["accept_prob_per_token"]]   # per token A, B, C
+    assert abs(cand["accept_prob"][0, 0] - a[ids["A"]]) < 1e-5
+    assert abs(cand["accept_prob"][0, 1] - a[ids["C"]]) < 1e-5
+    assert abs(cand["residual_mass"][0] - (1 - float(F(g["acceptance"][0])))) < 1e-5
+    _check(orc, inp, cand)
+
+
+def test_p_equals_q_on_random_rows(orc):
+    """q = fp32 of the fp64 softmax of the target row at every drafted
+    position (p = q up to rounding): every draft is accepted in at least
+    99.999 % of the sequences, and the outputs match the oracle."""
+    B, K, V, T = 20000, 4, 256, 1.0
+    rng = np.random.default_rng(77)
+    z = rng.normal(0.0, 2.0, (B, K + 1, V)).astype(np.float32)
+    p = np.exp(z.astype(np.float64) - z.max(-1, keepdims=True))
+    p /= p.sum(-1, keepdims=True)
+    q = p[:, :K].astype(np.float32)
+    tok = np.empty((B, K), np.int32)
+    for k in range(K):   # drafts drawn from q by the inverse CDF of seeded uniforms
+        c = np.cumsum(q[:, k].astype(np.float64), -1)
+        r = rng.random(B) * c[:, -1]
+        tok[:, k] = np.minimum((c < r[:, None]).sum(-1), V - 1)
+    u = rng.random((B, K + 1)).astype(np.float32)
+    inp = synth.Inputs(None, z, q, tok, u, T)
+    cand = G.run_inputs(inp)
+    assert cand["status"] == 0
+    full = (cand["num_emitted"] == K + 1).mean()
+    assert full >= 1 - 1e-5, full
+    _check(orc, inp, cand)
