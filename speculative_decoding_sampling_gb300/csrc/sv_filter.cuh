@@ -10,15 +10,21 @@
 // (the crossing id is kept); every other logit becomes -inf, kept logits
 // are copied unchanged, so softmax(z' / T) is the renormalised filtered p.
 //
-// One CTA per row (a persistent grid over the rows).  Masses are the
+// One CTA per row (a persistent grid over the rows).  The first pass reads
+// the row with an L2 evict-last hint and the output is stored evict-first,
+// so the later passes find the rows in L2.  Masses are the
 // verification's own: e_i = exp2(z_i c - fl(m c)) as an integer multiple of
 // 2^-fb, so every sum is exact and order-independent.  Per row:
 //   1. one pass: the maximum, the finite count, NaN / +inf detection (the
 //      only pass that has to come from HBM; the rest find the row in L2);
-//   2. one pass: counts and masses in kYBins bins of y = z c - fl(m c)
-//      (bin 0 holds the largest values; the last bin everything whose mass
-//      rounds to zero), and the bin where the top-k count / top-p mass is
-//      reached, by a scan from bin 0;
+//   2. one pass: counts in kYBins bins of y = z c - fl(m c) (bin 0 holds
+//      the largest values; the last bin everything whose mass rounds to
+//      zero), the exact masses of the top kTopBins bins, and the exact total
+//      mass, summed in registers; the bin where the top-k count / top-p mass
+//      is reached, by a scan from bin 0 (when the cut lies below the top
+//      bins -- a large top-k, a flat row -- one more pass forms the masses
+//      of the bins down to a limit that counts times each bin's smallest
+//      mass sets);
 //   3. inside that bin, the exact element.  A bin is a contiguous range of
 //      the order key of z (an unsigned integer that sorts like z).  A bin of
 //      at most kCollect ids is collected into shared memory in one pass,
@@ -43,6 +49,7 @@ constexpr int kFilterWarps = kFilterThreads / 32;
 constexpr int kYBins = 512;       // coarse bins of y
 constexpr int kTieIds = 8;        // consecutive ids a thread owns in the ordered scan
 constexpr int kCollect = 2048;    // ids of a bin resolved by a sort in shared memory
+constexpr int kTopBins = 200;     // bins whose exact masses the binning pass forms (y >= -200/yscale)
 
 struct FilterParams {
     const void *in;
@@ -102,9 +109,43 @@ __device__ __forceinline__ uint32_t filter_bits(const LT *row, int64_t i)
         return __float_as_uint(row[i]);
 }
 
+// 16-byte load keeping the line in L2 with priority (the later passes over
+// the row find it there)
+__device__ __forceinline__ uint4 ld_v4_keep(const void *p, uint64_t pol)
+{
+    uint4 r;
+    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p), "l"(pol));
+    return r;
+}
+
+// 16-byte store evicted from L2 first (the output is not read again here)
+__device__ __forceinline__ void st_v4_stream(void *p, uint4 v, uint64_t pol)
+{
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // Visit every element (id, raw bits) of a row; thread t takes vectors (or
-// elements) t, t + blockDim, ...
-template <typename LT, typename F>
+// elements) t, t + blockDim, ...; the next U vectors are requested before
+// the current ones are visited.  KEEP: loads carry an L2 evict-last hint.
+template <typename LT, bool KEEP = false, typename F>
 __device__ __forceinline__ void filter_visit(const LT *row, int32_t V, bool vec, F &&f)
 {
     if (vec) {
@@ -112,6 +153,8 @@ __device__ __forceinline__ void filter_visit(const LT *row, int32_t V, bool vec,
         constexpr int U = 4; // vectors a thread has in flight
         const int32_t nv = V / PV;
         const uint4 *rv = reinterpret_cast<const uint4 *>(row);
+        const uint64_t pol = KEEP ? l2_policy_evict_last() : 0ull;
+        auto load = [&](int32_t v) { return KEEP ? ld_v4_keep(rv + v, pol) : rv[v]; };
         auto visit_vec = [&](int32_t v, const uint4 w) {
             const uint32_t u[4] = {w.x, w.y, w.z, w.w};
             if constexpr (PV == 8) {
@@ -126,18 +169,29 @@ __device__ __forceinline__ void filter_visit(const LT *row, int32_t V, bool vec,
                     f(v * 4 + k, u[k]);
             }
         };
+        constexpr int32_t STEP = U * kFilterThreads;
+        const int32_t nfull = nv / STEP * STEP; // vectors in whole steps
         int32_t v = threadIdx.x;
-        for (; v + (U - 1) * kFilterThreads < nv; v += U * kFilterThreads) {
-            uint4 w[U];
+        if (nfull > 0) {
+            uint4 w[U], nx[U];
 #pragma unroll
             for (int t = 0; t < U; ++t)
-                w[t] = rv[v + t * kFilterThreads];
+                w[t] = load(v + t * kFilterThreads);
+            for (; v < nfull; v += STEP) {
+                const bool more = v + STEP < nfull;
 #pragma unroll
-            for (int t = 0; t < U; ++t)
-                visit_vec(v + t * kFilterThreads, w[t]);
+                for (int t = 0; t < U; ++t)
+                    nx[t] = more ? load(v + STEP + t * kFilterThreads) : w[t];
+#pragma unroll
+                for (int t = 0; t < U; ++t)
+                    visit_vec(v + t * kFilterThreads, w[t]);
+#pragma unroll
+                for (int t = 0; t < U; ++t)
+                    w[t] = nx[t];
+            }
         }
         for (; v < nv; v += kFilterThreads)
-            visit_vec(v, rv[v]);
+            visit_vec(v, load(v));
     } else {
         for (int32_t i = threadIdx.x; i < V; i += kFilterThreads)
             f(i, filter_bits<LT>(row, i));
@@ -482,7 +536,7 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const FilterP
         float m = -INFINITY;
         long long nfin = 0;
         int bad = 0;
-        filter_visit<LT>(row, V, P.vec, [&](int32_t, uint32_t bits) {
+        filter_visit<LT, true>(row, V, P.vec, [&](int32_t, uint32_t bits) {
             if (E::finite(bits)) {
                 m = fmaxf(m, E::value(bits));
                 ++nfin;
@@ -513,12 +567,14 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const FilterP
         }
         const FilterRow R = {P.c, mc_of(m, P.c), P.yscale, P.fb};
 
-        // 2. coarse bins of y
+        // 2. coarse bins of y: counts only, and the exact total mass in
+        // registers (the last bin's ids have zero mass and are only counted)
         for (int i = threadIdx.x; i < kYBins; i += kFilterThreads) {
             S.cnt[i] = 0u;
             S.mass[i] = 0ull;
         }
         __syncthreads();
+        long long Stot = 0;
         filter_visit<LT>(row, V, P.vec, [&](int32_t, uint32_t bits) {
             const bool fin = E::finite(bits);
             const float yv = fin ? R.y(E::value(bits)) : 0.0f;
@@ -532,35 +588,88 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const FilterP
             } else if (b >= 0) {
                 atomicAdd(&S.cnt[b], 1u);
                 const long long w = R.w(yv);
-                if (w)
+                Stot += w;
+                if (b < kTopBins && w) // the top bins' exact masses: the cuts lie there for most rows
                     atomicAdd(&S.mass[b], static_cast<unsigned long long>(w));
             }
         });
+        Stot = block_sum_l(Stot, S);
         __syncthreads();
 
-        // 3. the cuts
+        // 3. the cuts.  Exact bin masses are needed only above the cut: for
+        // the bins before the top-k bin, or, for top-p alone, down to the
+        // first bin where a lower bound of the running mass (counts times the
+        // smallest mass a bin holds) reaches the target; they are formed in
+        // one more pass over the ids of those bins only.
         const bool use_k = P.top_k >= 1 && static_cast<long long>(P.top_k) < nfin;
         const bool use_p = P.top_p < 1.0f;
         bool have_cut = false;
         Cut cut = {0u, -1};
-        long long Sk = 0; // mass of the top-k set
+        long long Sk = Stot; // mass of the top-k set
         int bk = kYBins - 1;
+        long long acck = 0;
         if (use_k) {
-            long long acc = 0, accm = 0;
-            int b = 0;
-            for (; b < kYBins - 1; ++b) {
-                if (acc + static_cast<long long>(S.cnt[b]) >= P.top_k)
+            for (bk = 0; bk < kYBins - 1; ++bk) {
+                if (acck + static_cast<long long>(S.cnt[bk]) >= P.top_k)
                     break;
-                acc += S.cnt[b];
-                accm += static_cast<long long>(S.mass[b]);
+                acck += S.cnt[bk];
             }
-            bk = b;
+        }
+        int b3 = -1; // exact masses of bins 0 .. b3
+        if (use_p) {
+            if (use_k) {
+                b3 = bk - 1;
+            } else {
+                // below the top bins, a lower bound of the running mass
+                // (counts times each bin's smallest mass) limits the bins
+                // the threshold may lie in
+                long long tau0 = static_cast<long long>(ceil(static_cast<double>(P.top_p) * static_cast<double>(Stot)));
+                tau0 = tau0 < 1 ? 1 : tau0;
+                long long top = 0; // the top bins' exact masses first: usually they reach the target
+                for (b3 = 0; b3 < kTopBins; ++b3) {
+                    top += static_cast<long long>(S.mass[b3]);
+                    if (top >= tau0)
+                        break;
+                }
+                long long lower = 0;
+                if (b3 == kTopBins)
+                    b3 = 0;
+                else
+                    lower = tau0; // found: the loop below stops at once
+                for (; b3 < kYBins - 1; ++b3) {
+                    if (lower >= tau0)
+                        break;
+                    // the smallest mass an id of bin b3 can have, taken a
+                    // little below the bin's edge in y (an id's bin comes
+                    // from a rounded product): a lower bound
+                    const long long wlo = R.w(-(static_cast<float>(b3) + 1.01f) / R.yscale) - 1;
+                    lower += static_cast<long long>(S.cnt[b3]) * (wlo > 0 ? wlo : 0);
+                    if (lower >= tau0)
+                        break;
+                }
+            }
+            if (b3 >= kTopBins) { // masses below the top bins: one more pass, rarely needed
+                filter_visit<LT>(row, V, P.vec, [&](int32_t, uint32_t bits) {
+                    if (E::finite(bits)) {
+                        const float yv = R.y(E::value(bits));
+                        const int b = R.bin(yv);
+                        if (b >= kTopBins && b <= b3) {
+                            const long long w = R.w(yv);
+                            if (w)
+                                atomicAdd(&S.mass[b], static_cast<unsigned long long>(w));
+                        }
+                    }
+                });
+                __syncthreads();
+            }
+        }
+        if (use_k) {
+            long long accm = 0;
+            for (int b = 0; b < bk; ++b)
+                accm += static_cast<long long>(S.mass[b]); // exact when top-p needs them, unused otherwise
             Sk = accm;
-            cut = filter_resolve<LT, false>(row, V, P.vec, R, b, false, cut, P.top_k - acc, &Sk, S);
+            cut = filter_resolve<LT, false>(row, V, P.vec, R, bk, false, cut, P.top_k - acck, &Sk, S);
             have_cut = true;
-        } else {
-            for (int b = 0; b < kYBins; ++b)
-                Sk += static_cast<long long>(S.mass[b]);
         }
         if (use_p) {
             long long tau = static_cast<long long>(ceil(static_cast<double>(P.top_p) * static_cast<double>(Sk)));
@@ -568,7 +677,8 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const FilterP
                 tau = 1;
             long long accm = 0;
             int b = 0;
-            for (; b < bk; ++b) {
+            const int blim = use_k ? bk : b3;
+            for (; b < blim; ++b) {
                 if (accm + static_cast<long long>(S.mass[b]) >= tau)
                     break;
                 accm += static_cast<long long>(S.mass[b]);
@@ -589,6 +699,7 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const FilterP
             const int32_t nv = V / PV;
             const uint4 *rv = reinterpret_cast<const uint4 *>(row);
             uint4 *ov = reinterpret_cast<uint4 *>(orow);
+            const uint64_t wpol = l2_policy_evict_first();
             for (int32_t v = threadIdx.x; v < nv; v += kFilterThreads) {
                 const uint4 w = rv[v];
                 uint32_t u[4] = {w.x, w.y, w.z, w.w};
@@ -607,7 +718,7 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const FilterP
                         u[k] = kk ? u[k] : E::kNegInf;
                     }
                 }
-                ov[v] = make_uint4(u[0], u[1], u[2], u[3]);
+                st_v4_stream(ov + v, make_uint4(u[0], u[1], u[2], u[3]), wpol);
             }
         } else {
             for (int32_t i = threadIdx.x; i < V; i += kFilterThreads) {
