@@ -72,15 +72,20 @@ def algorithmic_bytes(w, num_emitted: np.ndarray) -> dict:
     return {"rows_kernel": rows, "draw_kernels": surv, "total": rows + surv, "rejected": rejected}
 
 
-def kernel_source_hash() -> str:
-    """Hash of the device code of the verification kernels: every .cuh file
-    but the top-k / top-p filter's (the C ABI's host code in spec_verify.cu
-    is left out), with // comments, trailing blanks and empty lines removed
-    (they do not change a kernel)."""
+OWN_KERNEL_FILES = ("sv_filter.cuh", "sv_lmhead.cuh")  # kernels of their own, hashed apart
+
+
+def kernel_source_hash(only: str | None = None) -> str:
+    """Hash of device code, with // comments, trailing blanks and empty lines
+    removed (they do not change a kernel).  Default: the verification
+    kernels, i.e. every .cuh file but those of the top-k / top-p filter and
+    the LM head (the C ABI's host code in spec_verify.cu is left out).
+    only="sv_lmhead.cuh": that file and the verification kernels it
+    includes."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_sampling_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith(".cuh") and f != "sv_filter.cuh":
+        if f.endswith(".cuh") and (f not in OWN_KERNEL_FILES or f == only):
             with open(os.path.join(csrc, f), encoding="utf-8") as fh:
                 lines = (line.split("//", 1)[0].rstrip() for line in fh.read().splitlines())
                 code = "\n".join(line for line in lines if line)

@@ -33,7 +33,10 @@
  * Entry points: spec_verify (the whole step), spec_verify_stats (plus
  * acceptance counters), sv_verify_rows / sv_sample_survivors (its two
  * stages), spec_verify_noalloc (no workspace argument), sv_filter_logits
- * (top-k / top-p), sv_workspace_bytes, sv_kernel_launches, sv_status_string.
+ * (top-k / top-p), spec_verify_lm_head / sv_lm_head_logits (the target's LM
+ * head on the tensor cores, fused with the row statistics),
+ * sv_workspace_bytes, sv_lm_head_workspace_bytes, sv_kernel_launches,
+ * sv_status_string.
  *
  * Conventions for every entry point below:
  *   - All tensor pointers are DEVICE pointers (inputs may also be mapped
@@ -78,8 +81,8 @@ typedef enum { SV_BF16 = 0, SV_FP32 = 1 } sv_dtype_t;
 #define SV_BAD_ROW 8             /* a logit row with NaN / +inf / no finite  */
 #define SV_DEGENERATE_RESIDUAL 16 /* residual mass 0 after a rejection: the  */
                                   /* token was drawn from p instead          */
-#define SV_INTERNAL_TIMEOUT 32   /* reserved: no kernel of this version     */
-                                  /* waits on a flag, so it is never set     */
+#define SV_INTERNAL_TIMEOUT 32   /* a kernel's bounded wait ran out (the LM */
+                                  /* head's pipeline); outputs undefined     */
 
 /* Largest vocabulary supported. */
 #define SV_MAX_V (1 << 21)
@@ -252,6 +255,49 @@ sv_status_t sv_filter_logits(const void *logits, sv_dtype_t logits_dtype,
                              int64_t rows, int32_t V, float temperature,
                              int32_t top_k, float top_p, void *out_logits,
                              int32_t *kept, int32_t *status_dev, void *stream);
+
+/* The target's LM head fused with the verification ("推测解码采样验证优化策略 ——
+ * 深度调研报告", part 1 section 6, 扩展性与安全性: operator fusion of the
+ * verification into the target's last layer).
+ *
+ * sv_lm_head_logits: logits = hidden * lm_head^T on the tensor cores (fp32
+ * accumulation, result rounded to bf16 round-to-nearest-even).
+ *   hidden   [M, d] bf16, 16-byte aligned, row-major;
+ *   lm_head  [V, d] bf16 (the output embedding), 16-byte aligned;
+ *   logits   [M, V] bf16 out (2-byte aligned; 16-byte aligned with V % 8 == 0
+ *            for the fast stores).
+ *   status_dev: optional device int32; SV_INTERNAL_TIMEOUT is OR-ed into it
+ *   if one of the kernel's bounded waits ran out (the logits are then
+ *   incomplete); the caller zeroes it.
+ *   d must be a multiple of 8 (the rows' 16-byte stride) and at least 8;
+ *   M <= 2^30, V <= SV_MAX_V.  Returns SV_EINVAL / SV_EUNSUPPORTED on bad
+ *   sizes or pointers, SV_ECUDA when a launch (or the tensor-map set-up)
+ *   fails.  One launch on `stream`; allocates nothing.
+ *
+ * spec_verify_lm_head: spec_verify on logits the LM head computes in the same
+ * step: hidden [B, K+1, d] bf16 (the target's last hidden states of the K+1
+ * verified positions), lm_head [V, d] bf16; the logits are written to
+ * logits_out [B, K+1, V] bf16 (the surviving rows are read again by the
+ * draws) and each row's softmax statistics are formed by the GEMM's
+ * epilogue from those bf16 values, so no separate pass over the logits is
+ * made.  Every other argument as spec_verify; the workspace must hold
+ * sv_lm_head_workspace_bytes(B, K, V) bytes, zero-filled before first use
+ * (calls return the part spec_verify uses to zero; the GEMM's per-tile
+ * statistics are rewritten by every call). */
+size_t sv_lm_head_workspace_bytes(int64_t B, int32_t K, int32_t V);
+sv_status_t sv_lm_head_logits(const void *hidden, const void *lm_head,
+                              int64_t M, int32_t d, int32_t V, void *logits,
+                              int32_t *status_dev, void *stream);
+sv_status_t spec_verify_lm_head(const void *hidden, const void *lm_head,
+                                int32_t d, const float *draft_probs,
+                                const int32_t *draft_tokens,
+                                const float *uniforms, float temperature,
+                                int64_t B, int32_t K, int32_t V,
+                                void *logits_out, int32_t *out_tokens,
+                                int32_t *num_emitted, int8_t *accept_flags,
+                                float *accept_prob, float *residual_mass,
+                                int32_t *status_dev, void *workspace,
+                                size_t workspace_bytes, void *stream);
 
 /* Number of kernels one spec_verify (or spec_verify_stats) call with these
  * arguments launches on the CURRENT device: 2 (the row pass and the draw

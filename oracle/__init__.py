@@ -78,6 +78,14 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.sv_oracle_filter_logits.argtypes = [
         ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_double,
         ctypes.c_int32, ctypes.c_double, ctypes.c_void_p, _c_i32p, _c_i32p, ctypes.c_int]
+    lib.sv_oracle_lm_head_entry.restype = ctypes.c_double
+    lib.sv_oracle_lm_head_entry.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                            ctypes.c_int64]
+    lib.sv_oracle_lm_head.restype = ctypes.c_int
+    lib.sv_oracle_lm_head.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                                      ctypes.c_int32, ctypes.c_void_p]
+    lib.sv_oracle_bf16_round.restype = None
+    lib.sv_oracle_bf16_round.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
     lib.sv_oracle_filter_order.restype = ctypes.c_int32
     lib.sv_oracle_filter_order.argtypes = [
         ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_double,
@@ -252,6 +260,46 @@ class Oracle:
         if n < 0:
             return None
         return FilterOrder(ids[:n].copy(), cum[:n].copy(), int(nk.value), float(tau.value))
+
+
+def _lm_inputs(h: np.ndarray, W: np.ndarray):
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    W = np.ascontiguousarray(W, dtype=np.uint16)
+    if h.ndim != 2 or W.ndim != 2 or h.shape[1] != W.shape[1]:
+        raise ValueError("h [M, d] and W [V, d] bf16 bit patterns with the same d")
+    return h, W
+
+
+def _lm_head(self, h: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """logits = h W^T in fp64 from bf16 bit patterns h [M, d], W [V, d]."""
+    h, W = _lm_inputs(h, W)
+    M, d = h.shape
+    V = W.shape[0]
+    out = np.empty((M, V), np.float64)
+    if self.lib.sv_oracle_lm_head(h.ctypes.data, W.ctypes.data, M, d, V, out.ctypes.data) != 0:
+        raise RuntimeError("sv_oracle_lm_head failed")
+    return out
+
+
+def _lm_head_entries(self, h: np.ndarray, W: np.ndarray, rows, cols) -> np.ndarray:
+    """The entries (rows[i], cols[i]) of h W^T, fp64."""
+    h, W = _lm_inputs(h, W)
+    d = h.shape[1]
+    return np.array([self.lib.sv_oracle_lm_head_entry(h.ctypes.data, W.ctypes.data, d, int(r), int(c))
+                     for r, c in zip(rows, cols)], np.float64)
+
+
+def _bf16_round(self, x: np.ndarray) -> np.ndarray:
+    """fp64 values rounded once to bf16 (nearest, ties to even); bit patterns."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, np.uint16)
+    self.lib.sv_oracle_bf16_round(x.ctypes.data, x.size, out.ctypes.data)
+    return out
+
+
+Oracle.lm_head = _lm_head
+Oracle.lm_head_entries = _lm_head_entries
+Oracle.bf16_round = _bf16_round
 
 
 def load(path: str | None = None) -> Oracle:

@@ -695,3 +695,51 @@ int32_t sv_oracle_filter_order(const void *logits, int dtype, int64_t row, int32
     free(rank);
     return n;
 }
+
+/* ------------------------------------------------------------------ */
+/* The target's LM head, for the fused LM-head path: logits = h W^T.
+ * "推测解码采样验证优化策略 —— 深度调研报告", part 1 section 6 (扩展性与安全性)
+ * names fusing the verification into the target's last layer; the layer
+ * itself is the plain product of the last hidden states h [M, d] with the
+ * output embedding W [V, d].  Each entry is summed in fp64, sequentially in
+ * k, from the bf16 inputs (every bf16 value and every product of two is
+ * exact in fp64). */
+
+double sv_oracle_lm_head_entry(const uint16_t *h, const uint16_t *W, int32_t d, int64_t row, int64_t col)
+{
+    double s = 0.0;
+    for (int32_t k = 0; k < d; ++k)
+        s += bf16_bits_to_double(h[row * d + k]) * bf16_bits_to_double(W[col * d + k]);
+    return s;
+}
+
+int sv_oracle_lm_head(const uint16_t *h, const uint16_t *W, int64_t M, int32_t d, int32_t V, double *out)
+{
+    if (M < 0 || d < 1 || V < 1 || (M > 0 && (!h || !W || !out)))
+        return 1;
+    for (int64_t i = 0; i < M; ++i)
+        for (int32_t v = 0; v < V; ++v)
+            out[i * V + v] = sv_oracle_lm_head_entry(h, W, d, i, v);
+    return 0;
+}
+
+/* fp64 -> bf16 bits, rounded once to the nearest representable value, ties
+ * to the even significand (bf16: 8 significant bits).  Finite inputs below
+ * the bf16 overflow threshold only (logits). */
+void sv_oracle_bf16_round(const double *x, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        const double v = x[i];
+        if (v == 0.0) {
+            out[i] = signbit(v) ? 0x8000u : 0u;
+            continue;
+        }
+        int e;
+        const double m = frexp(v, &e);              /* v = m 2^e, 0.5 <= |m| < 1 */
+        const double r = nearbyint(ldexp(m, 8));    /* 8 significant bits, ties to even */
+        const float f = (float)ldexp(r, e - 8);     /* exact: r has 8 bits */
+        uint32_t u;
+        memcpy(&u, &f, sizeof u);
+        out[i] = (uint16_t)(u >> 16);               /* exact: the low 16 bits are zero */
+    }
+}

@@ -14,11 +14,13 @@ from ._native import (SV_BAD_Q, SV_BAD_ROW, SV_BAD_TOKEN, SV_BAD_U, SV_BF16,
                       NativeLibraryMissing)
 from .binding import (SpecVerifyError, SpecVerifyResult, default_workspace,
                       spec_verify, sv_filter_logits, sv_kernel_launches, sv_sample_survivors,
-                      sv_status_string, sv_verify_rows, sv_workspace_bytes)
+                      sv_status_string, sv_verify_rows, sv_workspace_bytes,
+                      spec_verify_lm_head, sv_lm_head_logits, sv_lm_head_workspace_bytes)
 from . import adaptive
 
 __all__ = [
     "spec_verify", "sv_verify_rows", "sv_sample_survivors",
+    "spec_verify_lm_head", "sv_lm_head_logits", "sv_lm_head_workspace_bytes",
     "sv_workspace_bytes", "sv_filter_logits", "sv_kernel_launches", "sv_status_string", "default_workspace",
     "SpecVerifyResult", "SpecVerifyError", "NativeLibraryMissing",
     "SV_OK", "SV_EINVAL", "SV_ECUDA", "SV_EUNSUPPORTED", "SV_BF16", "SV_FP32",

@@ -14,7 +14,8 @@ SV_MAX_V = 1 << 21
 
 # every function the header declares, in declaration order
 EXPORTS = ["sv_workspace_bytes", "spec_verify", "spec_verify_stats", "sv_verify_rows",
-           "sv_sample_survivors", "sv_filter_logits", "sv_kernel_launches", "sv_status_string"]
+           "sv_sample_survivors", "spec_verify_noalloc", "sv_filter_logits", "sv_lm_head_workspace_bytes",
+           "sv_lm_head_logits", "spec_verify_lm_head", "sv_kernel_launches", "sv_status_string"]
 
 
 def stats_words(K: int) -> int:
@@ -60,6 +61,14 @@ def lib() -> ctypes.CDLL:
         L.sv_kernel_launches.restype = ctypes.c_int
         L.sv_kernel_launches.argtypes = [ctypes.c_int, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
                                          ctypes.c_int32, ctypes.c_void_p]
+        L.sv_lm_head_workspace_bytes.restype = ctypes.c_size_t
+        L.sv_lm_head_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]
+        L.sv_lm_head_logits.restype = ctypes.c_int
+        L.sv_lm_head_logits.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                                        ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        L.spec_verify_lm_head.restype = ctypes.c_int
+        L.spec_verify_lm_head.argtypes = ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32] +
+                                          _VERIFY_ARGTYPES[2:9] + [ctypes.c_void_p] + _VERIFY_ARGTYPES[9:])
         L.sv_status_string.restype = ctypes.c_char_p
         L.sv_status_string.argtypes = [ctypes.c_int]
         _lib = L

@@ -267,3 +267,94 @@ def sv_sample_survivors(target_logits, draft_probs, draft_tokens, uniforms,
           uniforms, temperature, out["out_tokens"], out["num_emitted"],
           out.get("accept_flags"), out.get("accept_prob"),
           out.get("residual_mass"), out.get("status"), workspace, stream)
+
+
+# ------------------------------------------------------------- LM head
+
+def sv_lm_head_workspace_bytes(B: int, K: int, V: int) -> int:
+    return int(N.lib().sv_lm_head_workspace_bytes(int(B), int(K), int(V)))
+
+
+def _lm_check(hidden, lm_head):
+    if hidden.dtype != torch.bfloat16 or lm_head.dtype != torch.bfloat16:
+        raise TypeError("hidden and lm_head must be bfloat16")
+    if not (hidden.is_cuda and lm_head.is_cuda and hidden.is_contiguous() and lm_head.is_contiguous()):
+        raise ValueError("hidden and lm_head must be contiguous CUDA tensors")
+    if hidden.device != lm_head.device or lm_head.dim() != 2 or hidden.shape[-1] != lm_head.shape[1]:
+        raise ValueError("lm_head must be [V, d] on the hidden states' device, d their last dimension")
+
+
+def sv_lm_head_logits(hidden: torch.Tensor, lm_head: torch.Tensor, *, out: torch.Tensor | None = None,
+                      status: torch.Tensor | None = None,
+                      stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """logits = hidden @ lm_head.T on the tensor cores, bf16 out: hidden
+    [..., d] bf16, lm_head [V, d] bf16 -> [..., V] bf16.  status: optional
+    int32 [1] device tensor that receives SV_INTERNAL_TIMEOUT."""
+    _lm_check(hidden, lm_head)
+    V, d = lm_head.shape
+    M = hidden.numel() // d if d else 0
+    if out is None:
+        out = torch.empty(hidden.shape[:-1] + (V,), dtype=torch.bfloat16, device=hidden.device)
+    if out.dtype != torch.bfloat16 or out.numel() != M * V or not out.is_contiguous() or out.device != hidden.device:
+        raise ValueError("out must be a contiguous bf16 [..., V] tensor on the hidden states' device")
+    if status is not None:
+        _check(status, "status", torch.int32, (1,), hidden.device)
+    stream = stream or torch.cuda.current_stream(hidden.device)
+    rc = N.lib().sv_lm_head_logits(hidden.data_ptr(), lm_head.data_ptr(), M, d, V, out.data_ptr(),
+                                   _ptr(status), stream.cuda_stream)
+    if rc != N.SV_OK:
+        raise SpecVerifyError(rc)
+    return out
+
+
+def spec_verify_lm_head(hidden: torch.Tensor, lm_head: torch.Tensor, draft_probs: torch.Tensor | None,
+                        draft_tokens: torch.Tensor, uniforms: torch.Tensor, temperature: float, *,
+                        logits_out: torch.Tensor | None = None, want_probs: bool = True,
+                        workspace: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                        stream: torch.cuda.Stream | None = None):
+    """spec_verify on logits computed in the same step by the target's LM
+    head: hidden [B, K+1, d] bf16, lm_head [V, d] bf16.  Returns
+    (SpecVerifyResult, logits [B, K+1, V] bf16)."""
+    _lm_check(hidden, lm_head)
+    if hidden.dim() != 3:
+        raise ValueError("hidden must be [B, K+1, d]")
+    B, K1, d = hidden.shape
+    K = K1 - 1
+    V = lm_head.shape[0]
+    dev = hidden.device
+    if logits_out is None:
+        logits_out = torch.empty((B, K1, V), dtype=torch.bfloat16, device=dev)
+    if logits_out.shape != (B, K1, V) or logits_out.dtype != torch.bfloat16 or not logits_out.is_contiguous():
+        raise ValueError("logits_out must be a contiguous bf16 [B, K+1, V] tensor")
+    if draft_probs is not None:
+        _check(draft_probs, "draft_probs", torch.float32, (B, K, V), dev)
+    _check(draft_tokens, "draft_tokens", torch.int32, (B, K), dev)
+    _check(uniforms, "uniforms", torch.float32, (B, K + 1), dev)
+    need = sv_lm_head_workspace_bytes(B, K, V)
+    if need == 0 and B > 0:
+        raise SpecVerifyError(N.SV_EUNSUPPORTED)
+    stream = stream or torch.cuda.current_stream(dev)
+    if workspace is None:
+        workspace = default_workspace(dev, need)
+        if stream != torch.cuda.current_stream(dev):
+            workspace.record_stream(stream)
+    elif workspace.device != dev or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must hold {need} bytes on {dev}")
+    res = SpecVerifyResult(
+        out_tokens=torch.empty((B, K1), dtype=torch.int32, device=dev),
+        num_emitted=torch.empty((B,), dtype=torch.int32, device=dev),
+        accept_flags=torch.empty((B, K), dtype=torch.int8, device=dev),
+        accept_prob=torch.empty((B, K), dtype=torch.float32, device=dev) if want_probs else None,
+        residual_mass=torch.empty((B,), dtype=torch.float32, device=dev) if want_probs else None,
+        status=status)
+    if status is not None:
+        _check(status, "status", torch.int32, (1,), dev)
+    rc = N.lib().spec_verify_lm_head(
+        hidden.data_ptr(), lm_head.data_ptr(), d, _ptr(draft_probs), draft_tokens.data_ptr(),
+        uniforms.data_ptr(), float(temperature), B, K, V, logits_out.data_ptr(), res.out_tokens.data_ptr(),
+        res.num_emitted.data_ptr(), res.accept_flags.data_ptr(), _ptr(res.accept_prob),
+        _ptr(res.residual_mass), _ptr(status), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), stream.cuda_stream)
+    if rc != N.SV_OK:
+        raise SpecVerifyError(rc)
+    return res, logits_out

@@ -14,6 +14,7 @@
 
 #include "sv_filter.cuh"
 #include "sv_final.cuh"
+#include "sv_lmhead.cuh"
 #include "sv_rows.cuh"
 
 namespace {
@@ -73,6 +74,8 @@ bool make_plan(int64_t B, int32_t K, int32_t V, Plan &p)
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 enum Stage { kRows = 1, kSurvivors = 2, kBoth = 3 };
+
+constexpr uint64_t kWaitLimitNs = 1000000000ull; // every bounded wait of a kernel gives up after 1 s
 
 constexpr int kMaxDevices = 64;
 
@@ -263,7 +266,7 @@ sv_status_t run(int stages, const void *logits, sv_dtype_t dtype, const float *q
                 const float *u, float T, int64_t B, int32_t K, int32_t V, int32_t *out_tokens,
                 int32_t *num_emitted, int8_t *accept_flags, float *accept_prob, float *residual_mass,
                 int32_t *status_dev, void *workspace, size_t workspace_bytes, void *stream,
-                unsigned long long *stats = nullptr)
+                unsigned long long *stats = nullptr, int one_part = 0)
 {
     if (B < 0 || K < 0 || V < 1)
         return SV_EINVAL;
@@ -323,6 +326,7 @@ sv_status_t run(int stages, const void *logits, sv_dtype_t dtype, const float *q
     P.NC = B * static_cast<int64_t>(plan.CPS);
     P.ring_ok = (V % sv::kGroup) == 0 && aligned(logits, 16) && (P.q == nullptr || aligned(P.q, 16)) ? 1 : 0;
     P.fix_bits = plan.fix;
+    P.one_part = one_part;
     P.total = P.h = P.nvec = P.NV = P.span = 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -333,6 +337,82 @@ sv_status_t run(int stages, const void *logits, sv_dtype_t dtype, const float *q
     else
         e = dense ? launch<float, true>(P, plan, stages, s) : launch<float, false>(P, plan, stages, s);
     return e == cudaSuccess ? SV_OK : SV_ECUDA;
+}
+
+// ---------------------------------------------------------------- LM head
+
+constexpr int64_t kLmMaxRows = int64_t{1} << 30;
+
+int32_t lm_tiles(int32_t V) { return static_cast<int32_t>(ceil_div(V, sv::kLmBN)); }
+
+size_t lm_part_bytes(int64_t M, int32_t V) { return align_up(static_cast<size_t>(M) * lm_tiles(V) * sizeof(float2)); }
+
+// A 2-D tensor map of a row-major bf16 matrix [rows, cols] with boxes of
+// box_rows x 64 elements in the 128-byte swizzle layout; out-of-range
+// elements read as zero.  Reached through the runtime's entry-point lookup.
+bool lm_tensor_map(CUtensorMap *map, const void *base, int64_t rows, int32_t cols, uint32_t box_rows)
+{
+    using Encode = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static Encode encode = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            encode = reinterpret_cast<Encode>(f);
+        (void)cudaGetLastError();
+    });
+    if (!encode)
+        return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(sv::kLmBK), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+sv_status_t lm_check(const void *hidden, const void *lm_head, int64_t M, int32_t d, int32_t V, const void *logits)
+{
+    if (M < 0 || d < 8 || d % 8 != 0 || V < 1)
+        return SV_EINVAL;
+    if (V > SV_MAX_V || M > kLmMaxRows)
+        return SV_EUNSUPPORTED;
+    if (M > 0 && (!hidden || !lm_head || !logits || !aligned(hidden, 16) || !aligned(lm_head, 16) ||
+                  !aligned(logits, 2)))
+        return SV_EINVAL;
+    return SV_OK;
+}
+
+// logits = h W^T (bf16 out) and, with `part`, the per-tile row statistics.
+cudaError_t lm_launch(const void *hidden, const void *lm_head, int64_t M, int32_t d, int32_t V, void *logits,
+                      float2 *part, float c, int32_t *status, cudaStream_t stream)
+{
+    CUtensorMap ta, tb;
+    if (!lm_tensor_map(&ta, hidden, M, d, sv::kLmBM) || !lm_tensor_map(&tb, lm_head, V, d, sv::kLmBN))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(sv::lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sv::kLmSmem);
+    if (e != cudaSuccess)
+        return e;
+    sv::LmParams L;
+    L.M = static_cast<int32_t>(M);
+    L.N = V;
+    L.Kd = d;
+    L.logits = static_cast<uint16_t *>(logits);
+    L.part = part;
+    L.NT = lm_tiles(V);
+    L.c = c;
+    L.vec = (V % 8 == 0 && aligned(logits, 16)) ? 1 : 0;
+    L.status = status;
+    L.wait_ns = kWaitLimitNs;
+    const dim3 grid(static_cast<unsigned>(ceil_div(M, sv::kLmBM)), static_cast<unsigned>(L.NT));
+    sv::lm_head_kernel<<<grid, sv::kLmThreads, sv::kLmSmem, stream>>>(ta, tb, L);
+    return cudaGetLastError();
 }
 
 } // namespace
@@ -477,6 +557,84 @@ sv_status_t sv_filter_logits(const void *logits, sv_dtype_t logits_dtype, int64_
     else
         sv::filter_kernel<float><<<static_cast<unsigned>(grid), sv::kFilterThreads, 0, s>>>(F);
     return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
+}
+
+size_t sv_lm_head_workspace_bytes(int64_t B, int32_t K, int32_t V)
+{
+    Plan p;
+    if (!make_plan(B, K, V, p))
+        return 0;
+    return p.bytes + lm_part_bytes(B * (static_cast<int64_t>(K) + 1), V);
+}
+
+sv_status_t sv_lm_head_logits(const void *hidden, const void *lm_head, int64_t M, int32_t d, int32_t V,
+                              void *logits, int32_t *status_dev, void *stream)
+{
+    const sv_status_t st = lm_check(hidden, lm_head, M, d, V, logits);
+    if (st != SV_OK || M == 0)
+        return st;
+    if (status_dev && !aligned(status_dev, 4))
+        return SV_EINVAL;
+    return lm_launch(hidden, lm_head, M, d, V, logits, nullptr, 1.0f, status_dev, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? SV_OK
+               : SV_ECUDA;
+}
+
+sv_status_t spec_verify_lm_head(const void *hidden, const void *lm_head, int32_t d, const float *draft_probs,
+                                const int32_t *draft_tokens, const float *uniforms, float temperature, int64_t B,
+                                int32_t K, int32_t V, void *logits_out, int32_t *out_tokens, int32_t *num_emitted,
+                                int8_t *accept_flags, float *accept_prob, float *residual_mass, int32_t *status_dev,
+                                void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (B < 0 || K < 0)
+        return SV_EINVAL;
+    if (B > 0 && static_cast<int64_t>(K) + 1 > kLmMaxRows / B)
+        return SV_EUNSUPPORTED;
+    const int64_t M = B * (static_cast<int64_t>(K) + 1);
+    sv_status_t st = lm_check(hidden, lm_head, M, d, V, logits_out);
+    if (st != SV_OK)
+        return st;
+    Plan plan;
+    if (!make_plan(B, K, V, plan))
+        return SV_EUNSUPPORTED;
+    if (!workspace || workspace_bytes < plan.bytes + lm_part_bytes(M, V))
+        return SV_EINVAL;
+    // host checks of the verification (nothing launched yet)
+    st = run(0, logits_out, SV_BF16, draft_probs, draft_tokens, uniforms, temperature, B, K, V, out_tokens,
+             num_emitted, accept_flags, accept_prob, residual_mass, status_dev, workspace, plan.bytes, stream);
+    if (st != SV_OK || B == 0)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float2 *part = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + plan.bytes);
+    const float c = static_cast<float>(1.4426950408889634074 / static_cast<double>(temperature));
+    if (lm_launch(hidden, lm_head, M, d, V, logits_out, part, c, status_dev, s) != cudaSuccess)
+        return SV_ECUDA;
+    // the row statistics and draft data, then the draw stream and final draws
+    {
+        sv::Params P = {};
+        P.logits = logits_out;
+        P.q = K > 0 ? draft_probs : nullptr;
+        P.tokens = draft_tokens;
+        P.u = uniforms;
+        P.c = c;
+        P.B = B;
+        P.K = K;
+        P.V = V;
+        P.row_part = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + plan.off_part);
+        P.row_side = reinterpret_cast<float4 *>(static_cast<char *>(workspace) + plan.off_row_side);
+        P.PM = plan.PM;
+        const unsigned grid = static_cast<unsigned>(ceil_div(M, 8));
+        if (P.q)
+            sv::lm_merge_kernel<true><<<grid, 256, 0, s>>>(P, part, lm_tiles(V));
+        else
+            sv::lm_merge_kernel<false><<<grid, 256, 0, s>>>(P, part, lm_tiles(V));
+        if (cudaGetLastError() != cudaSuccess)
+            return SV_ECUDA;
+    }
+    return run(kSurvivors, logits_out, SV_BF16, draft_probs, draft_tokens, uniforms, temperature, B, K, V, out_tokens,
+               num_emitted, accept_flags, accept_prob, residual_mass, status_dev, workspace, plan.bytes, stream,
+               nullptr, 1);
 }
 
 const char *sv_status_string(sv_status_t status)

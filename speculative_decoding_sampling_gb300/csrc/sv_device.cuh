@@ -43,7 +43,7 @@ constexpr int kDrawWarps = SV_DRAW_WARPS;   // warps of a draw CTA
 static_assert(kDrawStages >= 2 && kDrawWarps >= 1 && kDrawWarps <= 32, "draw ring shape");
 
 // Device status bits (the values the public header documents).
-constexpr int32_t kBadU = 1, kBadToken = 2, kBadQ = 4, kBadRow = 8, kDegenerate = 16;
+constexpr int32_t kBadU = 1, kBadToken = 2, kBadQ = 4, kBadRow = 8, kDegenerate = 16, kTimeout = 32;
 
 struct Params {
     const void *logits;
@@ -81,6 +81,7 @@ struct Params {
     int32_t ring_ok;      // rows of whole 16-byte aligned groups: the draw streams through its rings
     int32_t inline_final; // every sequence has its own draw warps, the last of which makes its final draw
     int32_t fix_bits;     // fractional bits of the fixed-point masses
+    int32_t one_part;     // each row's statistics are one merged pair in slot 0 (the LM-head path)
 };
 
 // ------------------------------------------------------------ element loads

@@ -1,0 +1,384 @@
+// sv_lmhead.cuh -- the target's LM head fused with the row pass.
+//
+// logits = h W^T for the K+1 verified positions of every sequence: h bf16
+// [M, d] (M = B (K+1) hidden states), W bf16 [V, d] (the output embedding),
+// fp32 accumulation on the fifth-generation tensor cores.  Operator fusion
+// of the verification into the target's last layer is named by
+// "推测解码采样验证优化策略 —— 深度调研报告", part 1 section 6 (扩展性与安全性,
+// 算子融合).  The logits are rounded to bf16 and stored (the surviving row is
+// read again by the draw stream), and the epilogue also forms, from the
+// rounded values, each row's (max, normaliser) of softmax(z / T) over the
+// tile's 256 vocabulary ids -- the row pass's statistics -- so the logits are
+// never streamed back in for them.
+//
+// One CTA per 128 x 256 output tile (rows fastest, so the CTAs that share a
+// tile of W run together and find it in L2).  Warp 0: the producer, 2-D
+// tensor-memory-accelerator loads of 64-wide K slices of h and W into a
+// 4-stage ring (128-byte swizzle), completing on mbarriers.  Warp 1:
+// allocates 256 tensor-memory columns (the fp32 accumulator, one lane per
+// row) and issues the tcgen05 MMAs (M 128, N 256, K 16, bf16 x bf16 -> fp32)
+// by one thread, each stage's MMAs committed to the stage's "empty" barrier.
+// Warps 2..5: the epilogue, tcgen05.ld of the accumulator (warp w reads lanes
+// 32 (w mod 4) .. +31), bf16 rounding, stores, the tile statistics.
+// Every wait is bounded in time; a wait that runs out sets SV_INTERNAL_TIMEOUT
+// (and CTAs placed later skip their tile) and the CTA stops issuing, lets its copies and MMAs in flight complete
+// (again bounded), frees its tensor memory and returns.
+#pragma once
+
+#include <cuda.h>
+
+#include "sv_rows.cuh"
+
+namespace sv {
+
+constexpr int kLmBM = 128;                       // rows of h per tile
+constexpr int kLmBN = 256;                       // vocabulary ids per tile
+constexpr int kLmBK = 64;                        // hidden dims per stage: one 128-byte swizzle row
+constexpr int kLmStages = 4;
+constexpr int kLmABytes = kLmBM * kLmBK * 2;     // 16 KiB
+constexpr int kLmBBytes = kLmBN * kLmBK * 2;     // 32 KiB
+constexpr int kLmStageBytes = kLmABytes + kLmBBytes;
+constexpr int kLmThreads = 192;                  // producer, MMA, 4 epilogue warps
+constexpr int kLmSmem = kLmStages * kLmStageBytes + 1024; // + alignment of the swizzled tiles
+constexpr uint32_t kLmTmemCols = 256;
+
+struct LmParams {
+    int32_t M, N, Kd;  // rows of h, vocabulary, hidden size
+    uint16_t *logits;  // [M, N] bf16 out
+    float2 *part;      // [M, NT] (max, normaliser relative to fl(max c)) per 256-id tile, or nullptr
+    int32_t NT;        // tiles along N
+    float c;           // log2(e) / T
+    int32_t vec;       // N % 8 == 0 and 16-byte aligned logits: vector stores
+    int32_t *status;
+    uint64_t wait_ns;
+};
+
+// ------------------------------------------------------------- primitives
+
+__device__ __forceinline__ uint64_t lm_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void lm_mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void lm_mbar_expect(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool lm_mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of `bar`; false after limit_ns or once *stop is set.
+__device__ __forceinline__ bool lm_wait(uint32_t bar, uint32_t parity, const volatile int *stop, uint64_t limit_ns)
+{
+    if (lm_mbar_test(bar, parity))
+        return true;
+    const uint64_t t0 = lm_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (lm_mbar_test(bar, parity))
+                return true;
+        if ((stop && *stop) || lm_ns() - t0 > limit_ns)
+            return false;
+    }
+}
+
+// 2-D tiled tensor load (box from the map) into shared memory at `dst`;
+// c0 (the inner, hidden coordinate) is a multiple of 64 elements.
+__device__ __forceinline__ void lm_tma_2d(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void lm_tmem_alloc(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void lm_tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void lm_tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void lm_tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] B[smem]^T, both K-major, per the instruction descriptor
+__device__ __forceinline__ void lm_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+                 : "memory");
+}
+
+// the mbarrier gets one arrival once every MMA this thread issued before is done
+__device__ __forceinline__ void lm_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's tensor-memory lane
+__device__ __forceinline__ void lm_tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                   "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+                   "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+                   "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile in the 128-byte swizzle
+// layout the tensor loads write: rows of 64 bf16 (128 bytes), 8-row groups
+// 1024 bytes apart (stride byte offset); the leading byte offset is unused
+// for this layout (one MMA's K = 16 stays inside a swizzle row); descriptor
+// version 1; the tile base is 1024-byte aligned (base offset 0).
+__device__ __forceinline__ uint64_t lm_desc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>(1u) << 16;           // leading byte offset 16 (unused)
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;   // stride byte offset
+    d |= static_cast<uint64_t>(1u) << 46;           // descriptor version
+    d |= static_cast<uint64_t>(2u) << 61;           // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: D fp32, A and B bf16, both K-major, N = 256, M = 128.
+constexpr uint32_t kLmIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((static_cast<uint32_t>(kLmBN) >> 3) << 17) |
+                              ((static_cast<uint32_t>(kLmBM) >> 4) << 24);
+
+__device__ __forceinline__ uint32_t bf16_rn_pair(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// ------------------------------------------------------------- the kernel
+
+__global__ void __launch_bounds__(kLmThreads, 1)
+    lm_head_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const LmParams P)
+{
+    extern __shared__ uint8_t lm_smem_raw[];
+    __shared__ __align__(8) unsigned long long full[kLmStages], empty[kLmStages], accum, drain;
+    __shared__ uint32_t tmem_base;
+    __shared__ int stop;
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(lm_smem_raw) + 1023) & ~uintptr_t{1023});
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * kLmBM, n0 = blockIdx.y * kLmBN;
+    const int nk = (P.Kd + kLmBK - 1) / kLmBK;
+    const volatile int *vstop = &stop;
+
+    // once a CTA of the launch has timed out, the later ones do nothing (one
+    // CTA-uniform decision), so a launch that failed ends within a wait limit
+    if (threadIdx.x == 0)
+        stop = P.status ? (*reinterpret_cast<volatile int32_t *>(P.status) & kTimeout) : 0;
+    __syncthreads();
+    if (stop)
+        return;
+    __syncthreads(); // everyone has read `stop` before thread 0 clears it below
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kLmStages; ++s) {
+            lm_mbar_init(smem_addr(&full[s]), 1);
+            lm_mbar_init(smem_addr(&empty[s]), 1);
+        }
+        lm_mbar_init(smem_addr(&accum), 1);
+        lm_mbar_init(smem_addr(&drain), 1);
+        stop = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1)
+        lm_tmem_alloc(smem_addr(&tmem_base), kLmTmemCols);
+    lm_tc_before();
+    __syncthreads();
+    lm_tc_after();
+    const uint32_t tacc = tmem_base;
+    auto fail = [&]() {
+        if (!stop) {
+            stop = 1;
+            if (P.status)
+                atomicOr(P.status, kTimeout);
+        }
+    };
+
+    int armed = 0; // producer: stages armed with copies (k-blocks issued)
+    if (warp == 0 && lane == 0) {
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % kLmStages;
+            if (kb >= kLmStages &&
+                !lm_wait(smem_addr(&empty[s]), static_cast<uint32_t>(((kb / kLmStages) & 1) ^ 1), vstop, P.wait_ns)) {
+                fail();
+                break;
+            }
+            const uint32_t sa = smem_addr(smem + s * kLmStageBytes);
+            lm_mbar_expect(smem_addr(&full[s]), kLmStageBytes);
+            lm_tma_2d(sa, &tmA, kb * kLmBK, m0, smem_addr(&full[s]));
+            lm_tma_2d(sa + kLmABytes, &tmB, kb * kLmBK, n0, smem_addr(&full[s]));
+            armed = kb + 1;
+        }
+    } else if (warp == 1 && lane == 0) {
+        int kb = 0;
+        for (; kb < nk; ++kb) {
+            const int s = kb % kLmStages;
+            if (!lm_wait(smem_addr(&full[s]), static_cast<uint32_t>((kb / kLmStages) & 1), vstop, P.wait_ns)) {
+                fail();
+                break;
+            }
+            lm_tc_after();
+            const uint32_t sa = smem_addr(smem + s * kLmStageBytes);
+#pragma unroll
+            for (int k = 0; k < kLmBK / 16; ++k)
+                lm_mma(tacc, lm_desc(sa + k * 32), lm_desc(sa + kLmABytes + k * 32), kLmIdesc, (kb | k) ? 1u : 0u);
+            lm_commit(smem_addr(&empty[s])); // the stage is free once these MMAs have read it
+        }
+        if (kb == nk)
+            lm_commit(smem_addr(&accum)); // the accumulator is complete
+    } else if (warp >= 2) {
+        // ---- epilogue: this warp's 32 rows of the tile
+        const int lq = warp & 3; // tensor-memory lane quarter this warp may read
+        const int row = m0 + lq * 32 + lane;
+        // every lane waits (acquiring the barrier's phase itself); the
+        // verdict is made warp-uniform, as tcgen05.ld below is warp-collective
+        const bool ok = __all_sync(0xFFFFFFFFu, lm_wait(smem_addr(&accum), 0u, vstop, P.wait_ns));
+        if (!ok) {
+            if (lane == 0)
+                fail();
+        } else {
+            lm_tc_after();
+            const uint32_t tl = tacc + (static_cast<uint32_t>(lq * 32) << 16);
+            const bool rok = row < P.M;
+            const int ncols = P.N - n0 < kLmBN ? P.N - n0 : kLmBN;
+            uint16_t *lrow = P.logits + static_cast<int64_t>(row) * P.N + n0;
+            float mx = -INFINITY;
+            // pass 1: round, store, maximum
+#pragma unroll 1
+            for (int cb = 0; cb < kLmBN / 32; ++cb) {
+                uint32_t v[32];
+                lm_tmem_ld32(tl + cb * 32, v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    pk[i] = bf16_rn_pair(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                    const int col = cb * 32 + 2 * i;
+                    if (col < ncols)
+                        mx = fmaxf(mx, __uint_as_float(pk[i] << 16));
+                    if (col + 1 < ncols)
+                        mx = fmaxf(mx, __uint_as_float(pk[i] & 0xFFFF0000u));
+                }
+                if (rok) {
+                    const int c0 = cb * 32;
+                    if (P.vec && c0 + 32 <= ncols) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(lrow + c0);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (c0 + i < ncols)
+                                lrow[c0 + i] = static_cast<uint16_t>(i & 1 ? pk[i >> 1] >> 16 : pk[i >> 1] & 0xFFFFu);
+                    }
+                }
+            }
+            // pass 2: the normaliser against the tile maximum
+            if (P.part) {
+                const float mc = mc_of(mx, P.c);
+                float S = 0.0f;
+#pragma unroll 1
+                for (int cb = 0; cb < kLmBN / 32; ++cb) {
+                    uint32_t v[32];
+                    lm_tmem_ld32(tl + cb * 32, v);
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const uint32_t pk = bf16_rn_pair(__uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                        const int col = cb * 32 + i;
+                        if (col < ncols)
+                            S += term(__uint_as_float(pk << 16), P.c, mc);
+                        if (col + 1 < ncols)
+                            S += term(__uint_as_float(pk & 0xFFFF0000u), P.c, mc);
+                    }
+                }
+                if (rok)
+                    P.part[static_cast<int64_t>(row) * P.NT + blockIdx.y] = make_float2(mx, S);
+            }
+        }
+    }
+    // ---- teardown: copies and MMAs in flight complete before the memory goes
+    lm_tc_before();
+    __syncthreads();
+    if (stop) {
+        if (warp == 0 && lane == 0) // every armed stage's copies have landed
+            for (int kb = armed - kLmStages > 0 ? armed - kLmStages : 0; kb < armed; ++kb)
+                (void)lm_wait(smem_addr(&full[kb % kLmStages]), static_cast<uint32_t>((kb / kLmStages) & 1), nullptr,
+                              P.wait_ns);
+        if (warp == 1 && lane == 0) { // every MMA issued is done
+            lm_commit(smem_addr(&drain));
+            (void)lm_wait(smem_addr(&drain), 0u, nullptr, P.wait_ns);
+        }
+        __syncthreads();
+    }
+    if (warp == 1) {
+        lm_tc_after();
+        lm_tmem_dealloc(tacc, kLmTmemCols);
+    }
+}
+
+// ------------------------------------------------------------- merge
+
+// The row statistics and draft data for the draw stream, one warp per row:
+// the row's per-tile (max, normaliser) pairs merged into one (slot 0 of the
+// row's partials), and its draft token, z(x) (from the stored logits), q(x)
+// and uniform.
+template <bool DENSE>
+__global__ void __launch_bounds__(256) lm_merge_kernel(const Params P, const float2 *part, int32_t NT)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int64_t R = P.B * (static_cast<int64_t>(P.K) + 1);
+    if (r < R) { // warp-uniform
+        float M = -INFINITY, S = 0.0f;
+        for (int32_t i = lane; i < NT; i += 32) {
+            const float2 pr = part[r * NT + i];
+            merge_ms(M, S, pr.x, pr.y, P.c);
+        }
+        warp_merge_ms(M, S, P.c);
+        if (lane == 0) {
+            P.row_part[r * P.PM] = make_float2(M, S);
+            const RowSide sd = fetch_side<uint16_t, DENSE>(P, r);
+            P.row_side[r] = make_float4(__int_as_float(sd.x), sd.zx, sd.qx, sd.u);
+        }
+    }
+    pdl_launch_dependents();
+}
+
+} // namespace sv

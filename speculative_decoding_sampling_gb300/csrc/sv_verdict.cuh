@@ -44,7 +44,10 @@ __device__ Verdict seq_verdict(const Params &P, int64_t b, int lane, bool write)
             const int64_t r = b * (K + 1) + j;
             int64_t first;
             int n;
-            row_ctas<LT>(P, r, first, n);
+            if (P.one_part)
+                n = 1;
+            else
+                row_ctas<LT>(P, r, first, n);
             const float2 *part = P.row_part + r * P.PM;
 #pragma unroll 4
             for (int i = 0; i < n; ++i) {

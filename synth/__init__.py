@@ -174,3 +174,56 @@ def f32_to_bf16(x: np.ndarray) -> np.ndarray:
 
 def bf16_to_f32(h: np.ndarray) -> np.ndarray:
     return (np.asarray(h, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def lm_head_inputs(M: int, d: int, V: int, seed: int = DEFAULT_SEED, dyadic: bool = False):
+    """Seeded hidden states h [M, d] and output embedding W [V, d] as bf16 bit
+    patterns (uint16), for the LM-head path.  dyadic=False: h ~ N(0, 1) and
+    W ~ N(0, 1/d), rounded to bf16 (logits of order one).  dyadic=True: every
+    entry is 0 or +-1/2, so every product is 0 or +-1/4 and every sum of up to
+    2^24 of them is exact in fp32 as well as fp64."""
+    rng = np.random.default_rng([seed, M, d, V, int(dyadic)])
+
+    def bf16(a):  # round to nearest even
+        u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+        return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+    if dyadic:
+        vals = np.array([0xBF00, 0x0000, 0x3F00], np.uint16)   # -1/2, 0, +1/2
+        return vals[rng.integers(0, 3, (M, d))], vals[rng.integers(0, 3, (V, d))]
+    h = bf16(rng.standard_normal((M, d), dtype=np.float32))
+    W = bf16(rng.standard_normal((V, d), dtype=np.float32) / np.float32(np.sqrt(d)))
+    return h, W
+
+
+def drafts_for(z: np.ndarray, T: float, draft_sigma: float, seed: int = DEFAULT_SEED,
+               onehot_p: float | None = None):
+    """Draft inputs for target logits z [B, K+1, V] (fp64 values) that are
+    known only at run time (e.g. the LM head's).  Dense (onehot_p None):
+    q = softmax((z + N(0, draft_sigma^2)) / T) over the first K positions,
+    tokens drawn from q.  One-hot: tokens the target argmax with probability
+    onehot_p, else uniform over V, and q None.  Uniforms U[0, 1) fp32 for
+    all K+1 positions.  Returns (q fp32 | None, tokens int32, u fp32)."""
+    z = np.asarray(z, np.float64)
+    B, K1, V = z.shape
+    K = K1 - 1
+    rng = np.random.default_rng([seed, B, K, V, 0 if onehot_p is None else 1])
+    u = rng.random((B, K1), dtype=np.float32)
+    if onehot_p is not None:
+        arg = z[:, :K].argmax(-1)
+        rand = rng.integers(0, V, (B, K))
+        tokens = np.where(rng.random((B, K)) < onehot_p, arg, rand).astype(np.int32)
+        return None, tokens, u
+    q = np.empty((B, K, V), np.float32)
+    tokens = np.empty((B, K), np.int32)
+    for b0 in range(0, B, 8):  # a few sequences at a time: bounded host memory
+        b1 = min(B, b0 + 8)
+        zq = (z[b0:b1, :K] + draft_sigma * rng.standard_normal((b1 - b0, K, V))) / T
+        zq -= zq.max(-1, keepdims=True)
+        e = np.exp(zq)
+        qq = e / e.sum(-1, keepdims=True)
+        cdf = np.cumsum(qq, -1)
+        t = rng.random((b1 - b0, K, 1)) * cdf[..., -1:]
+        tokens[b0:b1] = np.minimum((cdf <= t).sum(-1), V - 1)
+        q[b0:b1] = qq
+    return q, tokens, u

@@ -14,7 +14,9 @@ Sources:
   [KB]    "投机采样" -- sections 机制：起草-验证-接受, 收益账,
           深入推导 (pointwise identity), 参考答案 (E[n] for alpha=0.8, gamma=3).
   [SURVEY-REPORT] "推测解码采样验证优化策略 —— 深度调研报告", part 1 section 4
-          (softmax of logits / temperature before verification).
+          (softmax of logits / temperature before verification); part 1
+          section 6 (fusing the verification into the target's last layer:
+          the LM head's logits = h W^T).
 """
 from __future__ import annotations
 
@@ -653,6 +655,97 @@ def pin_filter_matches_generator_nucleus(orc):
     assert np.array_equal(r.logits, masked)
     assert (r.status == 0).all() and int(r.kept.min()) >= 1
 
+
+# ------------------------------------------- the LM head (logits = h W^T)
+
+def _bf16_bits(x):
+    """fp32 values that are bf16 numbers -> their bf16 bit patterns."""
+    u = np.ascontiguousarray(x, np.float32).view(np.uint32)
+    assert not (u & 0xFFFF).any()
+    return (u >> 16).astype(np.uint16)
+
+
+def _rand_bf16(rng, shape):
+    """Random bf16 bit patterns (the top halves of N(0, 1) fp32 draws)."""
+    return (rng.standard_normal(shape).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _bf16_value(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def pin_bf16_round_textbook(orc):
+    """Round to nearest, ties to the even significand, 8 significant bits:
+    1 + 2^-8 is halfway between 1 and 1 + 2^-7 and goes to 1 (even); 1 + 3 2^-8
+    is halfway between 1 + 2^-7 and 1 + 2^-6 and goes to 1 + 2^-6; anything
+    above a halfway point goes up; pi -> 3.140625; -2.5 and 0 are exact."""
+    x = np.array([1.0, 1 + 2.0**-8, 1 + 3 * 2.0**-8, 1 + 2.0**-8 + 2.0**-20, -2.5, 0.0, np.pi,
+                  -(1 + 2.0**-8), 255.5, 2.0**-100 * 1.00390625], np.float64)
+    want = [0x3F80, 0x3F80, 0x3F82, 0x3F81, 0xC020, 0x0000, 0x4049, 0xBF80, 0x4380, 0x0D80]
+    got = orc.bf16_round(x)
+    assert [int(v) for v in got] == want, [hex(v) for v in got]
+
+
+def pin_bf16_round_matches_bit_rounding(orc):
+    """On fp32 inputs the fp64 rounding equals the integer form of
+    round-to-nearest-even on the fp32 bit pattern (add 0x7FFF plus the kept
+    low bit, drop 16 bits) -- a different algorithm for the same function."""
+    rng = np.random.default_rng(7)
+    x32 = (rng.standard_normal(4096) * np.exp2(rng.integers(-30, 30, 4096))).astype(np.float32)
+    x32[:64] = (np.float32(1) + np.arange(64, dtype=np.float32) * np.float32(2.0**-9))  # halfway cases
+    u = x32.view(np.uint32)
+    want = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    got = orc.bf16_round(x32.astype(np.float64))
+    assert np.array_equal(got, want)
+
+
+def pin_lm_head_identity_and_permutation(orc):
+    """W = a permutation matrix (V = d): logits[:, v] = h[:, pi(v)] exactly;
+    W = I: logits = h.  A transposed or shifted operand index breaks both."""
+    rng = np.random.default_rng(11)
+    M, d = 5, 24
+    h = _rand_bf16(rng, (M, d))
+    for perm in (np.arange(d), rng.permutation(d)):
+        W = np.zeros((d, d), np.float32)
+        W[np.arange(d), perm] = 1.0
+        out = orc.lm_head(h, _bf16_bits(W))
+        assert np.array_equal(out, _bf16_value(h)[:, perm])
+
+
+def pin_lm_head_rectangular_closed_forms(orc):
+    """V != d: W row v = c_v e_{k(v)} gives logits[:, v] = c_v h[:, k(v)];
+    h = all ones gives logits = the row sums of W (exact here: every entry
+    is a small dyadic number)."""
+    rng = np.random.default_rng(12)
+    M, d, V = 3, 16, 40
+    k = rng.integers(0, d, V)
+    cv = rng.choice([-2.0, -0.5, 0.25, 1.0, 3.0], V)
+    W = np.zeros((V, d), np.float32)
+    W[np.arange(V), k] = cv
+    h = _bf16_bits(rng.choice([-1.5, 0.5, 2.0, 0.0], (M, d)).astype(np.float32))
+    out = orc.lm_head(h, _bf16_bits(W))
+    assert np.array_equal(out, _bf16_value(h)[:, k] * cv[None, :])
+    W2 = _bf16_bits(rng.choice([-0.75, 0.0, 0.125, 1.0], (V, d)).astype(np.float32))
+    ones = _bf16_bits(np.ones((M, d), np.float32))
+    out2 = orc.lm_head(ones, W2)
+    assert np.array_equal(out2, np.repeat(_bf16_value(W2).sum(1)[None], M, 0))
+
+
+def pin_lm_head_matches_library_matmul(orc):
+    """Random bf16 operands: the fp64 dot products equal numpy's fp64 matmul
+    of the decoded values up to fp64 summation order, and single entries
+    equal the full product's."""
+    rng = np.random.default_rng(13)
+    M, d, V = 7, 40, 33
+    h = _rand_bf16(rng, (M, d))
+    W = _rand_bf16(rng, (V, d))
+    want = _bf16_value(h) @ _bf16_value(W).T
+    out = orc.lm_head(h, W)
+    assert np.allclose(out, want, rtol=1e-13, atol=1e-13)
+    rows, cols = np.array([0, 6, 3]), np.array([32, 0, 17])
+    assert np.array_equal(orc.lm_head_entries(h, W, rows, cols), out[rows, cols])
+
+
 ALL_PINS = [
     # cheap first: mutants should fail fast
     pin_worked_example,
@@ -680,6 +773,11 @@ ALL_PINS = [
     pin_filter_bruteforce_tiny,
     pin_filter_topk_matches_library_sort,
     pin_filter_matches_generator_nucleus,
+    pin_bf16_round_textbook,
+    pin_bf16_round_matches_bit_rounding,
+    pin_lm_head_identity_and_permutation,
+    pin_lm_head_rectangular_closed_forms,
+    pin_lm_head_matches_library_matmul,
     pin_output_distribution,
     pin_expected_tokens,
 ]

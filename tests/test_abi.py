@@ -137,3 +137,56 @@ def test_filter_binding_rejects_bad_tensors():
         sv.sv_filter_logits(x, 1.0, 0, 0.9)
     with pytest.raises(sv.SpecVerifyError):
         sv.sv_filter_logits(torch.zeros(2, 8, dtype=torch.float16), 1.0, 0, 0.9)
+
+
+# ----------------------------------------------------------------- LM head
+
+def _lm_logits(**kw):
+    fake = 1 << 40
+    a = dict(h=fake, W=fake, M=256, d=4096, V=1000, out=fake, status=None, stream=None)
+    a.update(kw)
+    return N.lib().sv_lm_head_logits(a["h"], a["W"], a["M"], a["d"], a["V"], a["out"], a["status"], a["stream"])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(h=None), dict(W=None), dict(out=None), dict(M=-1), dict(d=0), dict(d=12), dict(d=4),
+    dict(V=0), dict(h=(1 << 40) + 8), dict(W=(1 << 40) + 2), dict(out=(1 << 40) + 1),
+    dict(status=(1 << 40) + 2),
+], ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_lm_head_host_checks(kw):
+    assert _lm_logits(**kw) == N.SV_EINVAL
+
+
+def test_lm_head_sizes():
+    assert _lm_logits(V=N.SV_MAX_V + 1) == N.SV_EUNSUPPORTED
+    assert _lm_logits(M=(1 << 30) + 1) == N.SV_EUNSUPPORTED
+    assert _lm_logits(M=0) == N.SV_OK  # nothing to do, nothing launched
+    ws = sv.sv_lm_head_workspace_bytes(256, 8, 151936)
+    # the verification's workspace plus one (max, normaliser) pair per row and 256-id tile
+    assert ws >= sv.sv_workspace_bytes(256, 8, 151936) + 256 * 9 * 594 * 8
+    assert sv.sv_lm_head_workspace_bytes(-1, 8, 100) == 0
+
+
+def _lm_verify(**kw):
+    fake = 1 << 40
+    a = dict(h=fake, W=fake, d=256, q=fake, tok=fake, u=fake, T=1.0, B=4, K=3, V=1000, logits=fake,
+             out=fake, n=fake, flags=None, prob=None, mass=None, status=None, ws=fake, ws_bytes=1 << 24,
+             stream=None)
+    a.update(kw)
+    return N.lib().spec_verify_lm_head(a["h"], a["W"], a["d"], a["q"], a["tok"], a["u"], ctypes.c_float(a["T"]),
+                                       a["B"], a["K"], a["V"], a["logits"], a["out"], a["n"], a["flags"],
+                                       a["prob"], a["mass"], a["status"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(h=None), dict(W=None), dict(logits=None), dict(u=None), dict(out=None), dict(tok=None),
+    dict(d=10), dict(B=-1), dict(K=-1), dict(T=0.0), dict(T=float("nan")), dict(ws_bytes=64),
+    dict(ws=None), dict(h=(1 << 40) + 4), dict(logits=(1 << 40) + 1),
+], ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_lm_head_verify_host_checks(kw):
+    # every case returns before the GEMM is launched
+    assert _lm_verify(**kw) == N.SV_EINVAL
+
+
+def test_lm_head_verify_empty_batch():
+    assert _lm_verify(B=0) == N.SV_OK

@@ -43,6 +43,12 @@ MUTANTS = [
     ("filter_topk_one_more", "top_k < n) ? top_k : n", "top_k < n) ? top_k + 1 : n", 1),
     ("filter_mass_without_temperature", "acc += exp(rank[r].z / T - m);",
      "acc += exp(rank[r].z - m);", 1),
+    # LM head and bf16 rounding
+    ("lm_w_transposed", "W[col * d + k]", "W[k * d + col]", 1),
+    ("lm_k_reversed", "h[row * d + k]", "h[row * d + (d - 1 - k)]", 1),
+    ("bf16_round_truncates", "nearbyint(ldexp(m, 8))", "trunc(ldexp(m, 8))", 1),
+    ("bf16_round_ties_away", "nearbyint(ldexp(m, 8))", "round(ldexp(m, 8))", 1),
+    ("bf16_round_seven_bits", "nearbyint(ldexp(m, 8))", "nearbyint(ldexp(m, 7))", 1),
 ]
 
 
