@@ -322,6 +322,113 @@ def measure_workload(torch, dev, name: str, steps: int, cpu_threads: int) -> dic
             "parity": {"ok": rep.ok(), "summary": rep.summary()}}
 
 
+LM_SHAPE = (256, 8, 151936, 4096)  # B, K, V, d: the largest verification shape behind a 4096-wide LM head
+
+
+def measure_lm_head(torch, dev, steps: int, shape=LM_SHAPE, check: bool = True) -> dict:
+    """The LM head on the tensor cores (sv_lm_head_logits) and the whole
+    fused step (spec_verify_lm_head: GEMM with the row statistics in its
+    epilogue, merge, draws), each timed by CUDA-graph replay back to back.
+    W alone is larger than L2.  Beside them, for context: a library GEMM
+    (torch.matmul, cuBLAS) on the same operands followed by the unfused
+    spec_verify.  Parity: sampled logits against the fp64 oracle."""
+    import speculative_decoding_sampling_gb300 as sv
+    B, K, V, d = shape
+    M = B * (K + 1)
+    g = torch.Generator(device=dev)
+    g.manual_seed(4096)
+    h = torch.randn(M, d, device=dev, generator=g).to(torch.bfloat16)
+    W = (torch.randn(V, d, device=dev, generator=g) * d ** -0.5).to(torch.bfloat16)
+    q = torch.softmax(torch.randn(B, K, V, device=dev, generator=g) * 3.0, -1)
+    tok = torch.randint(0, V, (B, K), device=dev, dtype=torch.int32, generator=g)
+    u = torch.rand(B, K + 1, device=dev, generator=g)
+    logits = torch.empty(B, K + 1, V, dtype=torch.bfloat16, device=dev)
+    ref = torch.empty(M, V, dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.zeros(sv.sv_lm_head_workspace_bytes(B, K, V), dtype=torch.uint8, device=dev)
+    ws_v = ws[:sv.sv_workspace_bytes(B, K, V)]
+    hid = h.view(B, K + 1, d)
+    T = 0.7
+
+    def gemm(s):
+        sv.sv_lm_head_logits(h, W, out=logits.view(M, V), status=status, stream=s)
+
+    def fused(s):
+        sv.spec_verify_lm_head(hid, W, q, tok, u, T, logits_out=logits, workspace=ws, status=status, stream=s)
+
+    def library(s):
+        torch.matmul(h, W.t(), out=ref)
+        sv.spec_verify(ref.view(B, K + 1, V), q, tok, u, T, workspace=ws_v, status=status, stream=s)
+
+    def timed(fn, n):
+        gs = torch.cuda.Stream(dev)
+        with torch.cuda.stream(gs):
+            for _ in range(3):
+                fn(gs)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gs):
+            for _ in range(GRAPH_STEPS):
+                fn(gs)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(1, n // GRAPH_STEPS)
+        with torch.cuda.stream(gs):
+            e0.record(gs)
+            for _ in range(reps):
+                graph.replay()
+            e1.record(gs)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / (reps * GRAPH_STEPS)
+
+    n = max(GRAPH_STEPS, min(steps, 200))
+    gemm_ms = timed(gemm, n)
+    fused_ms = timed(fused, n)
+    lib_ms = timed(library, n)
+    torch.cuda.synchronize(dev)
+    flops = 2.0 * M * V * d
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+        pk = json.load(fh)
+    tf_peak, tf_sus = float(pk["bf16_tflops"]), float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
+    achieved = flops / (gemm_ms * 1e-3) / 1e12
+    out = {
+        "shape": {"B": B, "K": K, "V": V, "d": d, "M": M},
+        "kernel": "lm_head_kernel",
+        "gemm_us": gemm_ms * 1e3,
+        "fused_step_us": fused_ms * 1e3,
+        "fused_seqs_per_s": B / (fused_ms * 1e-3),
+        "context_cublas_plus_spec_verify_us": lib_ms * 1e3,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf_peak, "unit": "TFLOP/s",
+                     "frac": achieved / tf_peak, "frac_of_sustained": achieved / tf_sus,
+                     "flops_per_launch": flops, "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops burst)"},
+        "steps": n,
+        "status_bits": int(status.item()),
+        "timing": f"CUDA-graph replay of {GRAPH_STEPS} calls back to back; W ({V * d * 2 / 1e9:.2f} GB) alone "
+                  "exceeds L2, so no flush",
+    }
+    if check:
+        import oracle
+        orc = oracle.load()
+        rng = np.random.default_rng(1)
+        rows, cols = rng.integers(0, M, 256), rng.integers(0, V, 256)
+        gemm(torch.cuda.current_stream(dev))
+        torch.cuda.synchronize(dev)
+        hb = h.view(torch.int16).cpu().numpy().view(np.uint16)
+        Wb = W.view(torch.int16).cpu().numpy().view(np.uint16)
+        got = logits.view(M, V).view(torch.int16).cpu().numpy().view(np.uint16)[rows, cols]
+        exact = orc.lm_head_entries(hb, Wb, rows, cols)
+        gotv = (got.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        absdot = np.array([np.abs((hb[r].astype(np.uint32) << 16).view(np.float32).astype(np.float64)) @
+                           np.abs((Wb[c].astype(np.uint32) << 16).view(np.float32).astype(np.float64))
+                           for r, c in zip(rows, cols)])
+        bound = 2.0 ** -8 * np.abs(exact) + 2 * d * 2.0 ** -24 * absdot
+        out["parity"] = {"sampled_logits": len(rows), "within_bound": int((np.abs(gotv - exact) <= bound).sum()),
+                         "bit_equal_to_oracle_rounding": int((got == orc.bf16_round(exact)).sum()),
+                         "bound": "2^-8 |exact| + 2 d 2^-24 sum|h W| (fp32 summation, one bf16 rounding)"}
+    return out
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -481,6 +588,7 @@ def run_gpu(args):
             workloads = {}
             for name in synth.WORKLOADS:
                 workloads[name] = measure_workload(torch, dev, name, min(args.steps, 300), cores)
+        lm = measure_lm_head(torch, dev, args.steps) if args.lm_head == "on" else None
         config = config_of(w, world, filt)
         result = {
             "metric": METRIC,
@@ -528,6 +636,7 @@ def run_gpu(args):
             "cpu_baseline": cpu,
             "parity": parity_note,
             "workloads": workloads,
+            "lm_head": lm,
         }
     if world > 1:
         dist.barrier()
@@ -736,9 +845,19 @@ def main():
                          "on: always flush; off: neither")
     ap.add_argument("--no-workloads", dest="workloads", action="store_false",
                     help="skip the per-configuration `workloads` object (all five configs, parity included)")
+    ap.add_argument("--lm-head", default="on", choices=["on", "off", "only"],
+                    help="the LM-head leg (GEMM and fused step); only: that leg alone (profiling runs)")
+    ap.add_argument("--lm-shape", default=",".join(map(str, LM_SHAPE)),
+                    help="B,K,V,d of the LM-head leg with --lm-head only (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.lm_head == "only" and args.impl != "reference":
+        import torch
+        dev = torch.device("cuda", 0)
+        shape = tuple(int(x) for x in args.lm_shape.split(","))
+        print(json.dumps({"lm_head": measure_lm_head(torch, dev, args.steps, shape, check=False)}), flush=True)
+        return
     res = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if res is not None:
         print(json.dumps(res), flush=True)

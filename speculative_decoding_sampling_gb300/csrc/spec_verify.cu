@@ -389,20 +389,73 @@ sv_status_t lm_check(const void *hidden, const void *lm_head, int64_t M, int32_t
     return SV_OK;
 }
 
+// How many clusters of two LM-head CTAs fit on the current device at once
+// (the persistent grid, in pairs); cached per device for the context it was
+// taken in, like the verification kernels' figures.
+cudaError_t lm_pairs(int &pairs)
+{
+    struct Entry {
+        int pairs;
+        unsigned long long ctx;
+    };
+    static std::mutex mu;
+    static Entry cache[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    const unsigned long long ctx = current_context_id();
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev].pairs == 0 || cache[dev].ctx == 0 || cache[dev].ctx != ctx) {
+        e = cudaFuncSetAttribute(sv::lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sv::kLmSmem);
+        if (e != cudaSuccess)
+            return e;
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return e;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(sms > 1 ? sms & ~1 : 2));
+        cfg.blockDim = dim3(sv::kLmThreads);
+        cfg.dynamicSmemBytes = sv::kLmSmem;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, sv::lm_head_kernel, &cfg);
+        if (e != cudaSuccess)
+            return e;
+        if (n < 1)
+            return cudaErrorInvalidConfiguration;
+        cache[dev].pairs = n;
+        cache[dev].ctx = current_context_id();
+    }
+    pairs = cache[dev].pairs;
+    return cudaSuccess;
+}
+
 // logits = h W^T (bf16 out) and, with `part`, the per-tile row statistics.
 cudaError_t lm_launch(const void *hidden, const void *lm_head, int64_t M, int32_t d, int32_t V, void *logits,
                       float2 *part, float c, int32_t *status, cudaStream_t stream)
 {
     CUtensorMap ta, tb;
-    if (!lm_tensor_map(&ta, hidden, M, d, sv::kLmBM) || !lm_tensor_map(&tb, lm_head, V, d, sv::kLmBN))
+    if (!lm_tensor_map(&ta, hidden, M, d, sv::kLmBM) || !lm_tensor_map(&tb, lm_head, V, d, sv::kLmBN / 2))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(sv::lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sv::kLmSmem);
+    int pairs = 0;
+    cudaError_t e = lm_pairs(pairs);
     if (e != cudaSuccess)
         return e;
     sv::LmParams L;
     L.M = static_cast<int32_t>(M);
     L.N = V;
     L.Kd = d;
+    L.MT = static_cast<int32_t>(ceil_div(M, 2 * sv::kLmBM));
     L.logits = static_cast<uint16_t *>(logits);
     L.part = part;
     L.NT = lm_tiles(V);
@@ -410,9 +463,23 @@ cudaError_t lm_launch(const void *hidden, const void *lm_head, int64_t M, int32_
     L.vec = (V % 8 == 0 && aligned(logits, 16)) ? 1 : 0;
     L.status = status;
     L.wait_ns = kWaitLimitNs;
-    const dim3 grid(static_cast<unsigned>(ceil_div(M, sv::kLmBM)), static_cast<unsigned>(L.NT));
-    sv::lm_head_kernel<<<grid, sv::kLmThreads, sv::kLmSmem, stream>>>(ta, tb, L);
-    return cudaGetLastError();
+    // persistent: as many pairs of SMs as hold a cluster at once (the ring
+    // takes most of the shared memory: one CTA per SM)
+    const int64_t tiles = static_cast<int64_t>(L.MT) * L.NT;
+    const int64_t np = tiles < pairs ? tiles : pairs;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * np));
+    cfg.blockDim = dim3(sv::kLmThreads);
+    cfg.dynamicSmemBytes = sv::kLmSmem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, sv::lm_head_kernel, ta, tb, L);
 }
 
 } // namespace

@@ -11,18 +11,28 @@
 // tile's 256 vocabulary ids -- the row pass's statistics -- so the logits are
 // never streamed back in for them.
 //
-// One CTA per 128 x 256 output tile (rows fastest, so the CTAs that share a
-// tile of W run together and find it in L2).  Warp 0: the producer, 2-D
-// tensor-memory-accelerator loads of 64-wide K slices of h and W into a
-// 4-stage ring (128-byte swizzle), completing on mbarriers.  Warp 1:
-// allocates 256 tensor-memory columns (the fp32 accumulator, one lane per
-// row) and issues the tcgen05 MMAs (M 128, N 256, K 16, bf16 x bf16 -> fp32)
-// by one thread, each stage's MMAs committed to the stage's "empty" barrier.
-// Warps 2..5: the epilogue, tcgen05.ld of the accumulator (warp w reads lanes
-// 32 (w mod 4) .. +31), bf16 rounding, stores, the tile statistics.
-// Every wait is bounded in time; a wait that runs out sets SV_INTERNAL_TIMEOUT
-// (and CTAs placed later skip their tile) and the CTA stops issuing, lets its copies and MMAs in flight complete
-// (again bounded), frees its tensor memory and returns.
+// Persistent, on pairs of SMs: a cluster of two CTAs (one per SM of a
+// pair) walks the 256 x 256 output tiles, rows fastest, so the pairs
+// running at one time share a few tiles of W and find them in L2.  The
+// pair's MMA is one tcgen05.mma of M 256 (128 rows in each CTA's tensor
+// memory), N 256, K 16, issued by the even CTA; each CTA loads its own 128
+// rows of h and its half (128 ids) of the tile of W, so a stage holds
+// 32 KiB per SM and the ring has 6 stages.
+// Warp 0: the producer, 2-D tensor-memory-accelerator loads of 64-wide K
+// slices (128-byte swizzle), both CTAs' copies completing on the even CTA's
+// "full" barrier.  Warp 1: allocates all 512 tensor-memory columns of both
+// SMs (two fp32 accumulators of 256 columns, one lane per row); in the even
+// CTA one thread issues the MMAs, each stage's MMAs committed to both CTAs'
+// "empty" barriers and each finished tile to both CTAs' accumulator "full"
+// barriers.  Warps 2..5 of each CTA: the epilogue of its 128 rows,
+// tcgen05.ld of the accumulator (warp w reads lanes 32 (w mod 4) .. +31),
+// bf16 rounding, stores, the tile statistics; they hand the accumulator back
+// (to the even CTA's "empty" barrier) while the next tile's MMAs already run
+// in the other one.
+// Every mbarrier wait is bounded in time; a wait that runs out sets
+// SV_INTERNAL_TIMEOUT, the CTA stops issuing, gives the copies and MMAs in
+// flight time to complete (the even CTA waits for its MMAs, bounded), and
+// both CTAs free their tensor memory and return together.
 #pragma once
 
 #include <cuda.h>
@@ -31,19 +41,21 @@
 
 namespace sv {
 
-constexpr int kLmBM = 128;                       // rows of h per tile
-constexpr int kLmBN = 256;                       // vocabulary ids per tile
+constexpr int kLmBM = 128;                       // rows of h per CTA (256 per pair)
+constexpr int kLmBN = 256;                       // vocabulary ids per tile (128 loaded by each CTA)
 constexpr int kLmBK = 64;                        // hidden dims per stage: one 128-byte swizzle row
-constexpr int kLmStages = 4;
+constexpr int kLmStages = 6;
 constexpr int kLmABytes = kLmBM * kLmBK * 2;     // 16 KiB
-constexpr int kLmBBytes = kLmBN * kLmBK * 2;     // 32 KiB
+constexpr int kLmBBytes = kLmBN / 2 * kLmBK * 2; // 16 KiB: this CTA's half of the tile of W
 constexpr int kLmStageBytes = kLmABytes + kLmBBytes;
 constexpr int kLmThreads = 192;                  // producer, MMA, 4 epilogue warps
+constexpr int kLmEpiWarps = 4;
 constexpr int kLmSmem = kLmStages * kLmStageBytes + 1024; // + alignment of the swizzled tiles
-constexpr uint32_t kLmTmemCols = 256;
+constexpr uint32_t kLmTmemCols = 2 * kLmBN;     // two fp32 accumulators: all 512 columns
 
 struct LmParams {
     int32_t M, N, Kd;  // rows of h, vocabulary, hidden size
+    int32_t MT;        // 256-row tiles along M
     uint16_t *logits;  // [M, N] bf16 out
     float2 *part;      // [M, NT] (max, normaliser relative to fl(max c)) per 256-id tile, or nullptr
     int32_t NT;        // tiles along N
@@ -62,6 +74,26 @@ __device__ __forceinline__ uint64_t lm_ns()
     return t;
 }
 
+__device__ __forceinline__ uint32_t lm_cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// the shared::cluster address of the same shared-memory location in CTA `rank`
+__device__ __forceinline__ uint32_t lm_mapa(uint32_t saddr, uint32_t rank)
+{
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+    return d;
+}
+
+__device__ __forceinline__ void lm_cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 __device__ __forceinline__ void lm_mbar_init(uint32_t bar, uint32_t count)
 {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -73,11 +105,17 @@ __device__ __forceinline__ void lm_mbar_expect(uint32_t bar, uint32_t bytes)
                  : "memory");
 }
 
+// one arrival on a barrier of either CTA of the cluster
+__device__ __forceinline__ void lm_mbar_arrive_cluster(uint32_t cluster_bar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
 __device__ __forceinline__ bool lm_mbar_test(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok)
                  : "r"(bar), "r"(parity)
@@ -101,45 +139,58 @@ __device__ __forceinline__ bool lm_wait(uint32_t bar, uint32_t parity, const vol
     }
 }
 
-// 2-D tiled tensor load (box from the map) into shared memory at `dst`;
+// 2-D tiled tensor load (box from the map) into this CTA's shared memory at
+// `dst`, completing on `cluster_bar` (a barrier of either CTA of the pair);
 // c0 (the inner, hidden coordinate) is a multiple of 64 elements.
-__device__ __forceinline__ void lm_tma_2d(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1, uint32_t bar)
+__device__ __forceinline__ void lm_tma_2d(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1,
+                                          uint32_t cluster_bar)
 {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
+    asm volatile("cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(cluster_bar)
+                 : "memory");
 }
 
+// tensor memory of both CTAs of the pair; each CTA's warp takes part
 __device__ __forceinline__ void lm_tmem_alloc(uint32_t dst_smem, uint32_t ncols)
 {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
                  : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void lm_tmem_dealloc(uint32_t taddr, uint32_t ncols)
 {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
 __device__ __forceinline__ void lm_tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void lm_tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D[tmem] (+)= A[smem] B[smem]^T, both K-major, per the instruction descriptor
+// The pair's D[tmem] (+)= A[smem] B[smem]^T, both K-major: A's 256 rows are
+// the two CTAs' 128, B's 256 rows the two CTAs' halves; the descriptors'
+// addresses are taken in both CTAs' shared memory.
 __device__ __forceinline__ void lm_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc)
 {
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
                  "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
                  : "memory");
 }
 
-// the mbarrier gets one arrival once every MMA this thread issued before is done
-__device__ __forceinline__ void lm_commit(uint32_t bar)
+// The barrier at this shared-memory offset in both CTAs gets one arrival
+// once every MMA this thread issued before is done.
+__device__ __forceinline__ void lm_commit_both(uint32_t bar)
 {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
+                     "r"(bar), "h"(static_cast<uint16_t>(3))
+                 : "memory");
+}
+
+// the same, for a barrier of this CTA only
+__device__ __forceinline__ void lm_commit_local(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // 32 consecutive fp32 columns of this thread's tensor-memory lane
@@ -173,9 +224,9 @@ __device__ __forceinline__ uint64_t lm_desc(uint32_t saddr)
     return d;
 }
 
-// Instruction descriptor: D fp32, A and B bf16, both K-major, N = 256, M = 128.
+// Instruction descriptor: D fp32, A and B bf16, both K-major, N = 256, M = 256 (the pair).
 constexpr uint32_t kLmIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((static_cast<uint32_t>(kLmBN) >> 3) << 17) |
-                              ((static_cast<uint32_t>(kLmBM) >> 4) << 24);
+                              ((static_cast<uint32_t>(2 * kLmBM) >> 4) << 24);
 
 __device__ __forceinline__ uint32_t bf16_rn_pair(float lo, float hi)
 {
@@ -186,33 +237,95 @@ __device__ __forceinline__ uint32_t bf16_rn_pair(float lo, float hi)
 
 // ------------------------------------------------------------- the kernel
 
+// The epilogue of one tile for one warp: its 32 rows (one per lane) of the
+// accumulator at tensor-memory address `tl` (lane quarter and column base
+// applied).  Pass 1 rounds to bf16, stores, and takes each row's maximum;
+// pass 2 (with P.part) sums the softmax terms against that maximum.
+__device__ __forceinline__ void lm_epilogue_tile(const LmParams &P, uint32_t tl, int row, int n0, int tile_n)
+{
+    const bool rok = row < P.M;
+    const int ncols = P.N - n0 < kLmBN ? P.N - n0 : kLmBN;
+    uint16_t *lrow = P.logits + static_cast<int64_t>(row) * P.N + n0;
+    float mx = -INFINITY;
+#pragma unroll 1
+    for (int cb = 0; cb < kLmBN / 32; ++cb) {
+        uint32_t v[32];
+        lm_tmem_ld32(tl + cb * 32, v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            pk[i] = bf16_rn_pair(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            const int col = cb * 32 + 2 * i;
+            if (col < ncols)
+                mx = fmaxf(mx, __uint_as_float(pk[i] << 16));
+            if (col + 1 < ncols)
+                mx = fmaxf(mx, __uint_as_float(pk[i] & 0xFFFF0000u));
+        }
+        if (rok) {
+            const int c0 = cb * 32;
+            if (P.vec && c0 + 32 <= ncols) {
+                uint4 *dst = reinterpret_cast<uint4 *>(lrow + c0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (c0 + i < ncols)
+                        lrow[c0 + i] = static_cast<uint16_t>(i & 1 ? pk[i >> 1] >> 16 : pk[i >> 1] & 0xFFFFu);
+            }
+        }
+    }
+    if (!P.part)
+        return;
+    const float mc = mc_of(mx, P.c);
+    float S = 0.0f;
+#pragma unroll 1
+    for (int cb = 0; cb < kLmBN / 32; ++cb) {
+        uint32_t v[32];
+        lm_tmem_ld32(tl + cb * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            const uint32_t pk = bf16_rn_pair(__uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+            const int col = cb * 32 + i;
+            if (col < ncols)
+                S += term(__uint_as_float(pk << 16), P.c, mc);
+            if (col + 1 < ncols)
+                S += term(__uint_as_float(pk & 0xFFFF0000u), P.c, mc);
+        }
+    }
+    if (rok)
+        P.part[static_cast<int64_t>(row) * P.NT + tile_n] = make_float2(mx, S);
+}
+
+// Launched in clusters of two CTAs, one CTA per SM; the grid is a whole
+// number of pairs.  Pair p takes tiles p, p + pairs, ...; tile t covers rows
+// 256 (t mod MT) and vocabulary ids 256 (t div MT).
 __global__ void __launch_bounds__(kLmThreads, 1)
     lm_head_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const LmParams P)
 {
     extern __shared__ uint8_t lm_smem_raw[];
-    __shared__ __align__(8) unsigned long long full[kLmStages], empty[kLmStages], accum, drain;
+    __shared__ __align__(8) unsigned long long full[kLmStages], empty[kLmStages], tfull[2], tempty[2], drain;
     __shared__ uint32_t tmem_base;
     __shared__ int stop;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(lm_smem_raw) + 1023) & ~uintptr_t{1023});
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * kLmBM, n0 = blockIdx.y * kLmBN;
+    const uint32_t rank = lm_cluster_rank();
+    const bool leader = rank == 0;
+    const int64_t pair = blockIdx.x >> 1, pairs = gridDim.x >> 1;
     const int nk = (P.Kd + kLmBK - 1) / kLmBK;
+    const int64_t ntiles = static_cast<int64_t>(P.MT) * P.NT;
     const volatile int *vstop = &stop;
 
-    // once a CTA of the launch has timed out, the later ones do nothing (one
-    // CTA-uniform decision), so a launch that failed ends within a wait limit
-    if (threadIdx.x == 0)
-        stop = P.status ? (*reinterpret_cast<volatile int32_t *>(P.status) & kTimeout) : 0;
-    __syncthreads();
-    if (stop)
-        return;
-    __syncthreads(); // everyone has read `stop` before thread 0 clears it below
     if (threadIdx.x == 0) {
         for (int s = 0; s < kLmStages; ++s) {
-            lm_mbar_init(smem_addr(&full[s]), 1);
-            lm_mbar_init(smem_addr(&empty[s]), 1);
+            lm_mbar_init(smem_addr(&full[s]), 1);  // the even CTA's arrival with both CTAs' bytes
+            lm_mbar_init(smem_addr(&empty[s]), 1); // the pair's MMAs of the stage
         }
-        lm_mbar_init(smem_addr(&accum), 1);
+        for (int a = 0; a < 2; ++a) {
+            lm_mbar_init(smem_addr(&tfull[a]), 1);
+            lm_mbar_init(smem_addr(&tempty[a]), 2 * kLmEpiWarps); // every epilogue warp of the pair
+        }
         lm_mbar_init(smem_addr(&drain), 1);
         stop = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -221,8 +334,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         lm_tmem_alloc(smem_addr(&tmem_base), kLmTmemCols);
     lm_tc_before();
     __syncthreads();
+    lm_cluster_sync(); // both CTAs' barriers exist before either CTA signals the other's
     lm_tc_after();
-    const uint32_t tacc = tmem_base;
+    const uint32_t tbase = tmem_base;
     auto fail = [&]() {
         if (!stop) {
             stop = 1;
@@ -231,125 +345,105 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         }
     };
 
-    int armed = 0; // producer: stages armed with copies (k-blocks issued)
     if (warp == 0 && lane == 0) {
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % kLmStages;
-            if (kb >= kLmStages &&
-                !lm_wait(smem_addr(&empty[s]), static_cast<uint32_t>(((kb / kLmStages) & 1) ^ 1), vstop, P.wait_ns)) {
-                fail();
-                break;
+        int64_t it = 0;
+        for (int64_t t = pair; t < ntiles && !*vstop; t += pairs) {
+            const int m0 = static_cast<int>(t % P.MT) * (2 * kLmBM) + static_cast<int>(rank) * kLmBM;
+            const int n0 = static_cast<int>(t / P.MT) * kLmBN + static_cast<int>(rank) * (kLmBN / 2);
+            int kb = 0;
+            for (; kb < nk; ++kb, ++it) {
+                const int s = static_cast<int>(it % kLmStages);
+                if (it >= kLmStages &&
+                    !lm_wait(smem_addr(&empty[s]), static_cast<uint32_t>(((it / kLmStages) & 1) ^ 1), vstop,
+                             P.wait_ns)) {
+                    fail();
+                    break;
+                }
+                const uint32_t sa = smem_addr(smem + s * kLmStageBytes);
+                const uint32_t fb = lm_mapa(smem_addr(&full[s]), 0);
+                if (leader)
+                    lm_mbar_expect(smem_addr(&full[s]), 2 * kLmStageBytes);
+                lm_tma_2d(sa, &tmA, kb * kLmBK, m0, fb);
+                lm_tma_2d(sa + kLmABytes, &tmB, kb * kLmBK, n0, fb);
             }
-            const uint32_t sa = smem_addr(smem + s * kLmStageBytes);
-            lm_mbar_expect(smem_addr(&full[s]), kLmStageBytes);
-            lm_tma_2d(sa, &tmA, kb * kLmBK, m0, smem_addr(&full[s]));
-            lm_tma_2d(sa + kLmABytes, &tmB, kb * kLmBK, n0, smem_addr(&full[s]));
-            armed = kb + 1;
+            if (kb < nk)
+                break;
         }
-    } else if (warp == 1 && lane == 0) {
-        int kb = 0;
-        for (; kb < nk; ++kb) {
-            const int s = kb % kLmStages;
-            if (!lm_wait(smem_addr(&full[s]), static_cast<uint32_t>((kb / kLmStages) & 1), vstop, P.wait_ns)) {
+    } else if (warp == 1 && lane == 0 && leader) {
+        int64_t it = 0;
+        int i = 0;
+        for (int64_t t = pair; t < ntiles && !*vstop; t += pairs, ++i) {
+            const int acc = i & 1;
+            if (i >= 2 &&
+                !lm_wait(smem_addr(&tempty[acc]), static_cast<uint32_t>(((i >> 1) & 1) ^ 1), vstop, P.wait_ns)) {
                 fail();
                 break;
             }
             lm_tc_after();
-            const uint32_t sa = smem_addr(smem + s * kLmStageBytes);
+            const uint32_t tacc = tbase + static_cast<uint32_t>(acc * kLmBN);
+            int kb = 0;
+            for (; kb < nk; ++kb, ++it) {
+                const int s = static_cast<int>(it % kLmStages);
+                if (!lm_wait(smem_addr(&full[s]), static_cast<uint32_t>((it / kLmStages) & 1), vstop, P.wait_ns)) {
+                    fail();
+                    break;
+                }
+                lm_tc_after();
+                const uint32_t sa = smem_addr(smem + s * kLmStageBytes);
 #pragma unroll
-            for (int k = 0; k < kLmBK / 16; ++k)
-                lm_mma(tacc, lm_desc(sa + k * 32), lm_desc(sa + kLmABytes + k * 32), kLmIdesc, (kb | k) ? 1u : 0u);
-            lm_commit(smem_addr(&empty[s])); // the stage is free once these MMAs have read it
+                for (int k = 0; k < kLmBK / 16; ++k)
+                    lm_mma(tacc, lm_desc(sa + k * 32), lm_desc(sa + kLmABytes + k * 32), kLmIdesc,
+                           (kb | k) ? 1u : 0u);
+                lm_commit_both(smem_addr(&empty[s])); // both CTAs' stage is free once these MMAs have read it
+            }
+            if (kb < nk)
+                break;
+            lm_commit_both(smem_addr(&tfull[acc])); // the accumulator is complete in both CTAs
         }
-        if (kb == nk)
-            lm_commit(smem_addr(&accum)); // the accumulator is complete
     } else if (warp >= 2) {
-        // ---- epilogue: this warp's 32 rows of the tile
         const int lq = warp & 3; // tensor-memory lane quarter this warp may read
-        const int row = m0 + lq * 32 + lane;
-        // every lane waits (acquiring the barrier's phase itself); the
-        // verdict is made warp-uniform, as tcgen05.ld below is warp-collective
-        const bool ok = __all_sync(0xFFFFFFFFu, lm_wait(smem_addr(&accum), 0u, vstop, P.wait_ns));
-        if (!ok) {
-            if (lane == 0)
-                fail();
-        } else {
+        int i = 0;
+        for (int64_t t = pair; t < ntiles; t += pairs, ++i) {
+            const int acc = i & 1;
+            // every lane waits (acquiring the barrier's phase itself); the
+            // verdict is made warp-uniform, as tcgen05.ld is warp-collective
+            const bool ok = __all_sync(0xFFFFFFFFu, lm_wait(smem_addr(&tfull[acc]),
+                                                            static_cast<uint32_t>((i >> 1) & 1), vstop, P.wait_ns));
+            if (!ok) {
+                if (lane == 0)
+                    fail();
+                break;
+            }
             lm_tc_after();
-            const uint32_t tl = tacc + (static_cast<uint32_t>(lq * 32) << 16);
-            const bool rok = row < P.M;
-            const int ncols = P.N - n0 < kLmBN ? P.N - n0 : kLmBN;
-            uint16_t *lrow = P.logits + static_cast<int64_t>(row) * P.N + n0;
-            float mx = -INFINITY;
-            // pass 1: round, store, maximum
-#pragma unroll 1
-            for (int cb = 0; cb < kLmBN / 32; ++cb) {
-                uint32_t v[32];
-                lm_tmem_ld32(tl + cb * 32, v);
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    pk[i] = bf16_rn_pair(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                    const int col = cb * 32 + 2 * i;
-                    if (col < ncols)
-                        mx = fmaxf(mx, __uint_as_float(pk[i] << 16));
-                    if (col + 1 < ncols)
-                        mx = fmaxf(mx, __uint_as_float(pk[i] & 0xFFFF0000u));
-                }
-                if (rok) {
-                    const int c0 = cb * 32;
-                    if (P.vec && c0 + 32 <= ncols) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(lrow + c0);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (c0 + i < ncols)
-                                lrow[c0 + i] = static_cast<uint16_t>(i & 1 ? pk[i >> 1] >> 16 : pk[i >> 1] & 0xFFFFu);
-                    }
-                }
-            }
-            // pass 2: the normaliser against the tile maximum
-            if (P.part) {
-                const float mc = mc_of(mx, P.c);
-                float S = 0.0f;
-#pragma unroll 1
-                for (int cb = 0; cb < kLmBN / 32; ++cb) {
-                    uint32_t v[32];
-                    lm_tmem_ld32(tl + cb * 32, v);
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const uint32_t pk = bf16_rn_pair(__uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-                        const int col = cb * 32 + i;
-                        if (col < ncols)
-                            S += term(__uint_as_float(pk << 16), P.c, mc);
-                        if (col + 1 < ncols)
-                            S += term(__uint_as_float(pk & 0xFFFF0000u), P.c, mc);
-                    }
-                }
-                if (rok)
-                    P.part[static_cast<int64_t>(row) * P.NT + blockIdx.y] = make_float2(mx, S);
-            }
+            const int row = static_cast<int>(t % P.MT) * (2 * kLmBM) + static_cast<int>(rank) * kLmBM + lq * 32 + lane;
+            const int tn = static_cast<int>(t / P.MT);
+            lm_epilogue_tile(P, tbase + (static_cast<uint32_t>(lq * 32) << 16) + static_cast<uint32_t>(acc * kLmBN),
+                             row, tn * kLmBN, tn);
+            lm_tc_before();
+            __syncwarp();
+            if (lane == 0) // this warp has read the accumulator: the MMAs may overwrite it
+                lm_mbar_arrive_cluster(lm_mapa(smem_addr(&tempty[acc]), 0));
         }
     }
     // ---- teardown: copies and MMAs in flight complete before the memory goes
     lm_tc_before();
     __syncthreads();
     if (stop) {
-        if (warp == 0 && lane == 0) // every armed stage's copies have landed
-            for (int kb = armed - kLmStages > 0 ? armed - kLmStages : 0; kb < armed; ++kb)
-                (void)lm_wait(smem_addr(&full[kb % kLmStages]), static_cast<uint32_t>((kb / kLmStages) & 1), nullptr,
-                              P.wait_ns);
-        if (warp == 1 && lane == 0) { // every MMA issued is done
-            lm_commit(smem_addr(&drain));
+        if (threadIdx.x == 0) { // copies issued before the stop land within microseconds
+            const uint64_t t0 = lm_ns();
+            while (lm_ns() - t0 < 50000ull) {
+            }
+        }
+        if (warp == 1 && lane == 0 && leader) { // every MMA issued is done
+            lm_commit_local(smem_addr(&drain));
             (void)lm_wait(smem_addr(&drain), 0u, nullptr, P.wait_ns);
         }
-        __syncthreads();
     }
+    __syncthreads();
+    lm_cluster_sync(); // neither CTA's memory goes while the pair's MMAs or signals may still use it
     if (warp == 1) {
         lm_tc_after();
-        lm_tmem_dealloc(tacc, kLmTmemCols);
+        lm_tmem_dealloc(tbase, kLmTmemCols);
     }
 }
 
