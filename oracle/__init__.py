@@ -29,6 +29,7 @@ ORC_BAD_TOKEN = 2
 ORC_BAD_Q = 4
 ORC_BAD_ROW = 8
 ORC_DEGENERATE_RESIDUAL = 16
+ORC_BAD_TREE = 64
 
 _c_i32p = ctypes.POINTER(ctypes.c_int32)
 _c_i8p = ctypes.POINTER(ctypes.c_int8)
@@ -86,6 +87,16 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
                                       ctypes.c_int32, ctypes.c_void_p]
     lib.sv_oracle_bf16_round.restype = None
     lib.sv_oracle_bf16_round.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    lib.sv_oracle_tree_verify.restype = ctypes.c_int
+    lib.sv_oracle_tree_verify.argtypes = [
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_double, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    lib.sv_oracle_tree_verify_probs.restype = ctypes.c_int
+    lib.sv_oracle_tree_verify_probs.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     lib.sv_oracle_filter_order.restype = ctypes.c_int32
     lib.sv_oracle_filter_order.argtypes = [
         ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_double,
@@ -297,6 +308,60 @@ def _bf16_round(self, x: np.ndarray) -> np.ndarray:
     return out
 
 
+@dataclass
+class TreeResult:
+    out_tokens: np.ndarray   # [B, N] accepted path's tokens, then the final token, -1 padded
+    out_nodes: np.ndarray    # [B, N] node ids of the accepted path, -1 padded
+    num_emitted: np.ndarray  # [B]
+    accept_prob: np.ndarray  # [B, N] min(1, r(x)/q(x)) of each tested node, -1 if not tested
+    status: np.ndarray       # [B]
+
+
+def _tree_out(B, N):
+    return TreeResult(np.empty((B, N), np.int32), np.empty((B, N), np.int32), np.empty(B, np.int32),
+                      np.empty((B, N), np.float64), np.empty(B, np.int32))
+
+
+def _tree_call(fn, head, o: TreeResult, B, N, V):
+    rc = fn(*head, B, N, V, o.out_tokens.ctypes.data, o.out_nodes.ctypes.data, o.num_emitted.ctypes.data,
+            o.accept_prob.ctypes.data, o.status.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"tree oracle refused the call ({rc})")
+    return o
+
+
+def _tree_verify(self, logits: np.ndarray, q: np.ndarray, parent: np.ndarray, tokens: np.ndarray,
+                 u: np.ndarray, T: float) -> TreeResult:
+    """Tree verification from logits [B, N, V] (bf16 bits or fp32), q fp32
+    [B, N, V], parent / tokens int32 [B, N], u fp32 [B, N]."""
+    logits = np.ascontiguousarray(logits)
+    B, N, V = logits.shape
+    q = np.ascontiguousarray(q, np.float32)
+    parent = np.ascontiguousarray(parent, np.int32)
+    tokens = np.ascontiguousarray(tokens, np.int32)
+    u = np.ascontiguousarray(u, np.float32)
+    assert q.shape == (B, N, V) and parent.shape == (B, N) and tokens.shape == (B, N) and u.shape == (B, N)
+    head = (logits.ctypes.data, self._dtype_of(logits), q.ctypes.data, parent.ctypes.data, tokens.ctypes.data,
+            u.ctypes.data, float(T))
+    return _tree_call(self.lib.sv_oracle_tree_verify, head, _tree_out(B, N), B, N, V)
+
+
+def _tree_verify_probs(self, p: np.ndarray, q: np.ndarray, parent: np.ndarray, tokens: np.ndarray,
+                       u: np.ndarray) -> TreeResult:
+    """Tree verification from probabilities p, q [B, N, V] fp64, u [B, N] fp64."""
+    p = np.ascontiguousarray(p, np.float64)
+    B, N, V = p.shape
+    q = np.ascontiguousarray(q, np.float64)
+    parent = np.ascontiguousarray(parent, np.int32)
+    tokens = np.ascontiguousarray(tokens, np.int32)
+    u = np.ascontiguousarray(u, np.float64)
+    assert q.shape == (B, N, V) and parent.shape == (B, N) and tokens.shape == (B, N) and u.shape == (B, N)
+    head = (p.ctypes.data, q.ctypes.data, parent.ctypes.data, tokens.ctypes.data, u.ctypes.data)
+    return _tree_call(self.lib.sv_oracle_tree_verify_probs, head, _tree_out(B, N), B, N, V)
+
+
+Oracle.tree_verify = _tree_verify
+Oracle.tree_verify_probs = _tree_verify_probs
 Oracle.lm_head = _lm_head
 Oracle.lm_head_entries = _lm_head_entries
 Oracle.bf16_round = _bf16_round

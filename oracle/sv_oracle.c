@@ -743,3 +743,187 @@ void sv_oracle_bf16_round(const double *x, int64_t n, uint16_t *out)
         out[i] = (uint16_t)(u >> 16);               /* exact: the low 16 bits are zero */
     }
 }
+
+/* ------------------------------------------------ tree (multi-candidate)
+ *
+ * Verification of a candidate tree by multi-step speculative sampling
+ * (SpecInfer, Miao et al., "SpecInfer: Accelerating Large Language Model
+ * Serving with Tree-based Speculative Inference and Verification", ASPLOS
+ * 2024, the multi-step speculative sampling of its verification section).
+ * The pages fix what a tree must satisfy -- it commits one contiguous path
+ * and keeps the target distribution, and the chain's single-candidate
+ * correction cannot be applied to it as it stands ("推测解码：草稿、验证与
+ * 实际加速", section 链、树与自推测) -- but give no rule; this is the
+ * published rule taken for it.
+ *
+ * Nodes 0..N-1 of one sequence; node 0 is the committed prefix (no token),
+ * parent[i] < i for i >= 1, and the children of a node are its nodes in
+ * increasing index order, drafted i.i.d. from that node's draft
+ * distribution q_v.  p_v = softmax(z_v / T) is the target's next-token
+ * distribution after node v's path.  From v = 0:
+ *   r = p_v; for each child c of v in order: accept c (token x) iff
+ *   u[c] < min(1, r(x) / q_v(x)); on acceptance commit x and continue at c;
+ *   on rejection r = max(0, r - q_v) / sum(max(0, r - q_v)).
+ *   If every child is rejected, draw the final token from r with u[0]; if v
+ *   has no children, draw it from p_v with u[0] (the draw as in step (5)).
+ * Readings: the acceptance uniform of node c is u[c] and the final draw
+ * uses u[0]; a residual with no positive mass (impossible in exact
+ * arithmetic) ends the walk with the final token drawn from p_v and a
+ * status bit; a sequence with an invalid input (parent outside [0, i) for
+ * node i >= 1, a token outside [0, V), q_v(x) <= 0 or non-finite for a
+ * drafted token x, u outside [0, 1), a bad logit row) emits nothing.
+ */
+enum { ORC_BAD_TREE = 64 };
+
+/* P, Q: N rows of p and q (fp64); rows_ok: validity of each row (NULL =
+ * all valid).  out_tokens / out_nodes: [N]; accept_prob: [N] (-1 where the
+ * node was not tested). */
+static void tree_sequence(const double *P, const double *Q, const int32_t *parent,
+                          const int32_t *tok, const double *u, const int *rows_ok,
+                          int32_t N, int32_t V, double *r, double *w,
+                          int32_t *out_tokens, int32_t *out_nodes, int32_t *num_emitted,
+                          double *accept_prob, int32_t *status)
+{
+    int32_t st = 0;
+    for (int32_t i = 0; i < N; ++i)
+        if (!(u[i] >= 0.0 && u[i] < 1.0))
+            st |= ORC_BAD_U;
+    for (int32_t i = 1; i < N; ++i) {
+        if (parent[i] < 0 || parent[i] >= i) {
+            st |= ORC_BAD_TREE;
+        } else if (tok[i] < 0 || tok[i] >= V) {
+            st |= ORC_BAD_TOKEN;
+        } else {
+            double qx = Q[(int64_t)parent[i] * V + tok[i]];
+            if (!(qx > 0.0) || !isfinite(qx))
+                st |= ORC_BAD_Q;
+        }
+    }
+    if (rows_ok)
+        for (int32_t i = 0; i < N; ++i)
+            if (!rows_ok[i])
+                st |= ORC_BAD_ROW;
+    for (int32_t i = 0; i < N; ++i) {
+        out_tokens[i] = -1;
+        out_nodes[i] = -1;
+        accept_prob[i] = -1.0;
+    }
+    *num_emitted = 0;
+    if (st) {
+        *status = st;
+        return;
+    }
+
+    int32_t v = 0, len = 0, y = -1;
+    for (;;) {
+        const double *pv = P + (int64_t)v * V;
+        const double *qv = Q + (int64_t)v * V;
+        for (int32_t i = 0; i < V; ++i)
+            r[i] = pv[i];
+        int has_child = 0, next = -1, degenerate = 0;
+        for (int32_t c = v + 1; c < N; ++c) {
+            if (parent[c] != v)
+                continue;
+            has_child = 1;
+            double a = r[tok[c]] / qv[tok[c]];
+            a = a < 1.0 ? a : 1.0;
+            accept_prob[c] = a;
+            if (u[c] < a) {
+                next = c;
+                break;
+            }
+            double Z = 0.0;
+            for (int32_t i = 0; i < V; ++i) {
+                double d = r[i] - qv[i];
+                r[i] = d > 0.0 ? d : 0.0;
+                Z += r[i];
+            }
+            if (!(Z > 0.0)) {
+                degenerate = 1;
+                break;
+            }
+            for (int32_t i = 0; i < V; ++i)
+                r[i] /= Z;
+        }
+        if (next >= 0) {
+            out_tokens[len] = tok[next];
+            out_nodes[len] = next;
+            ++len;
+            v = next;
+            continue;
+        }
+        double Z;
+        if (degenerate) {
+            st |= ORC_DEGENERATE_RESIDUAL;
+            y = inverse_cdf(pv, V, u[0], &Z);
+        } else {
+            (void)has_child; /* leaf: r = p_v; all rejected: r is the residual */
+            for (int32_t i = 0; i < V; ++i)
+                w[i] = r[i];
+            y = inverse_cdf(w, V, u[0], &Z);
+        }
+        break;
+    }
+    out_tokens[len] = y;
+    *num_emitted = len + 1;
+    *status = st;
+}
+
+/* From probabilities: p, q [B, N, V] fp64, u [B, N] fp64. */
+int sv_oracle_tree_verify_probs(const double *p, const double *q, const int32_t *parent,
+                                const int32_t *tokens, const double *u, int64_t B, int32_t N,
+                                int32_t V, int32_t *out_tokens, int32_t *out_nodes,
+                                int32_t *num_emitted, double *accept_prob, int32_t *status)
+{
+    if (B < 0 || N < 1 || V < 1)
+        return 1;
+    double *r = malloc(sizeof(double) * (size_t)V);
+    double *w = malloc(sizeof(double) * (size_t)V);
+    if (!r || !w) {
+        free(r);
+        free(w);
+        return 2;
+    }
+    for (int64_t b = 0; b < B; ++b)
+        tree_sequence(p + b * N * (int64_t)V, q + b * N * (int64_t)V, parent + b * N,
+                      tokens + b * N, u + b * N, NULL, N, V, r, w, out_tokens + b * N,
+                      out_nodes + b * N, num_emitted + b, accept_prob + b * N, status + b);
+    free(r);
+    free(w);
+    return 0;
+}
+
+/* From logits (bf16 bits or fp32) [B, N, V], q fp32 [B, N, V], u fp32 [B, N]:
+ * p_v = softmax(z_v / T) in fp64 for every node row. */
+int sv_oracle_tree_verify(const void *logits, int dtype, const float *q, const int32_t *parent,
+                          const int32_t *tokens, const float *u, double T, int64_t B, int32_t N,
+                          int32_t V, int32_t *out_tokens, int32_t *out_nodes, int32_t *num_emitted,
+                          double *accept_prob, int32_t *status)
+{
+    if (B < 0 || N < 1 || V < 1 || !(T > 0.0))
+        return 1;
+    size_t rows = (size_t)N * (size_t)V;
+    double *P = malloc(sizeof(double) * rows);
+    double *Q = malloc(sizeof(double) * rows);
+    double *ud = malloc(sizeof(double) * (size_t)N);
+    int *ok = malloc(sizeof(int) * (size_t)N);
+    double *r = malloc(sizeof(double) * (size_t)V);
+    double *w = malloc(sizeof(double) * (size_t)V);
+    if (!P || !Q || !ud || !ok || !r || !w) {
+        free(P); free(Q); free(ud); free(ok); free(r); free(w);
+        return 2;
+    }
+    for (int64_t b = 0; b < B; ++b) {
+        for (int32_t i = 0; i < N; ++i) {
+            ok[i] = softmax_row(logits, dtype, (b * N + i) * (int64_t)V, V, T, P + (int64_t)i * V);
+            ud[i] = (double)u[b * N + i];
+        }
+        for (size_t k = 0; k < rows; ++k)
+            Q[k] = (double)q[(size_t)b * rows + k];
+        tree_sequence(P, Q, parent + b * N, tokens + b * N, ud, ok, N, V, r, w,
+                      out_tokens + b * N, out_nodes + b * N, num_emitted + b,
+                      accept_prob + b * N, status + b);
+    }
+    free(P); free(Q); free(ud); free(ok); free(r); free(w);
+    return 0;
+}

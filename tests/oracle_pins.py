@@ -746,6 +746,139 @@ def pin_lm_head_matches_library_matmul(orc):
     assert np.array_equal(orc.lm_head_entries(h, W, rows, cols), out[rows, cols])
 
 
+# ------------------------------------------------ tree (multi-candidate)
+# The rule: SpecInfer's multi-step speculative sampling (Miao et al., ASPLOS
+# 2024) -- the pages require that a tree commits one path and keeps the
+# target distribution ("推测解码：草稿、验证与实际加速", section 链、树与自推测)
+# but give no rule of their own.
+
+def _tree_probs(orc, p_rows, q_rows, parent, tokens, u):
+    return orc.tree_verify_probs(np.asarray(p_rows, np.float64)[None], np.asarray(q_rows, np.float64)[None],
+                                 np.asarray(parent, np.int32)[None], np.asarray(tokens, np.int32)[None],
+                                 np.asarray(u, np.float64)[None])
+
+
+def pin_tree_hand_example(orc):
+    """Three siblings at the root, worked by hand: p = (.5, .3, .2),
+    q = (.2, .2, .6), children C, C, B.  C: a = .2/.6 = 1/3; after its
+    rejection r = (.3, .1, 0)/.4 = (3/4, 1/4, 0); the second C: a = 0 (and
+    u = 0 still rejects: the test is strict); then r = (.55, .05, 0)/.6 =
+    (11/12, 1/12, 0); B: a = (1/12)/.2 = 5/12; if B is rejected too,
+    r = (11/12 - .2, 0, 0) -> the final token is A whatever u[0]."""
+    P = [[.5, .3, .2], [1, 0, 0], [1, 0, 0], [0, 0, 1]]
+    Q = [[.2, .2, .6], [1 / 3] * 3, [1 / 3] * 3, [1 / 3] * 3]
+    par, tok = [-1, 0, 0, 0], [0, 2, 2, 1]
+    r = _tree_probs(orc, P, Q, par, tok, [0.99, 0.5, 0.0, 0.5])   # all three rejected
+    assert np.allclose(r.accept_prob[0, 1:], [1 / 3, 0, 5 / 12], rtol=1e-14, atol=1e-15), r.accept_prob
+    assert r.num_emitted[0] == 1 and r.out_tokens[0, 0] == 0 and r.status[0] == 0
+    r = _tree_probs(orc, P, Q, par, tok, [0.5, 0.5, 0.0, 0.4])    # B accepted (0.4 < 5/12): leaf, bonus from its row
+    assert list(r.out_nodes[0, :1]) == [3] and list(r.out_tokens[0, :2]) == [1, 2] and r.num_emitted[0] == 2
+    r = _tree_probs(orc, P, Q, par, tok, [0.5, 0.3, 0.0, 0.4])    # the first C accepted (0.3 < 1/3)
+    assert list(r.out_tokens[0, :2]) == [2, 0] and r.out_nodes[0, 0] == 1
+    assert r.accept_prob[0, 2] == -1 and r.accept_prob[0, 3] == -1  # never tested
+    # the pages' worked distributions: after A is rejected the residual is
+    # (0, 1, 0), so a second child C is rejected and B is drawn
+    r = _tree_probs(orc, [[.5, .3, .2], [1, 0, 0], [1, 0, 0]], [[.6, .1, .3], [1 / 3] * 3, [1 / 3] * 3],
+                    [-1, 0, 0], [0, 0, 2], [0.2, 0.9, 0.5])
+    assert r.out_tokens[0, 0] == 1 and r.num_emitted[0] == 1
+    assert np.allclose(r.accept_prob[0, 1:], [5 / 6, 0], rtol=1e-14)
+
+
+def pin_tree_chain_reduces_to_chain(orc):
+    """A tree that is a chain (parent[i] = i - 1) is verified exactly as the
+    chain rule verifies it: same tokens, counts and acceptance probabilities
+    (tree u[i] = chain u[i-1], tree u[0] = chain u[K])."""
+    rng = np.random.default_rng(21)
+    B, K, V = 400, 5, 7
+    p = rng.dirichlet(np.ones(V) * 0.7, (B, K + 1))
+    q = rng.dirichlet(np.ones(V) * 0.7, (B, K))
+    tok = np.array([[rng.choice(V, p=q[b, k]) for k in range(K)] for b in range(B)], np.int32)
+    u = rng.random((B, K + 1))
+    chain = orc.verify_probs(p, q, tok, u)
+    qt = np.concatenate([q, np.full((B, 1, V), 1.0 / V)], 1)
+    par = np.tile(np.arange(-1, K, dtype=np.int32), (B, 1))
+    tt = np.concatenate([np.zeros((B, 1), np.int32), tok], 1)
+    ut = np.concatenate([u[:, K:], u[:, :K]], 1)
+    tr = orc.tree_verify_probs(p, qt, par, tt, ut)
+    assert np.array_equal(tr.num_emitted, chain.num_emitted)
+    assert np.array_equal(tr.out_tokens, chain.out_tokens)
+    for b in range(B):
+        n = int(chain.num_emitted[b])
+        tested = min(n, K)  # drafts 1..tested were tested
+        assert np.allclose(tr.accept_prob[b, 1:1 + tested], chain.accept_prob[b, :tested], rtol=1e-14)
+        assert (tr.accept_prob[b, 1 + tested:] == -1).all()
+
+
+def pin_tree_p_equals_q(orc):
+    """p_v = q_v at every node: the first child is always accepted (a = 1),
+    so the path follows first children down to a leaf."""
+    rng = np.random.default_rng(22)
+    V = 6
+    par = [-1, 0, 0, 1, 1, 2, 3]
+    tok = [0, 1, 2, 3, 4, 5, 0]
+    P = rng.dirichlet(np.ones(V), 7)
+    for _ in range(50):
+        r = _tree_probs(orc, P, P, par, tok, rng.random(7))
+        assert list(r.out_nodes[0, :3]) == [1, 3, 6] and r.num_emitted[0] == 4
+
+
+def pin_tree_invalid_inputs(orc):
+    """Parent not before the node, token outside [0, V), q(x) = 0 for a
+    drafted token, u outside [0, 1): the sequence emits nothing."""
+    P = [[.5, .5]] * 3
+    Q = [[.5, .5], [.5, .5], [.5, .5]]
+    bad = [([-1, 0, 2], [0, 1, 1], [.1] * 3, Q, 64), ([-1, 0, 0], [0, 1, 2], [.1] * 3, Q, 2),
+           ([-1, 0, 0], [0, 1, 0], [.1] * 3, [[1, 0], [.5, .5], [.5, .5]], 4),
+           ([-1, 0, 1], [0, 1, 1], [.1, .1, 1.0], Q, 1)]
+    for par, tok, u, q, bit in bad:
+        r = _tree_probs(orc, P, q, par, tok, u)
+        assert r.status[0] & bit and r.num_emitted[0] == 0 and (r.out_tokens[0] == -1).all(), (par, tok, bit)
+
+
+def pin_tree_keeps_target_distribution(orc):
+    """Monte Carlo, 4e5 rounds: siblings drafted i.i.d. from their parent's q
+    (with replacement), fresh uniforms.  The first emitted token follows p_0,
+    and after an accepted child with token y the next emitted token follows
+    that child's row -- chi-square at alpha = 0.001 (the property the pages
+    require of a tree; SpecInfer's theorem for this rule)."""
+    from scipy import stats
+    rng = np.random.default_rng(23)
+    V = 4
+    # topology: root with 3 children; its first child has 2 children
+    par = np.array([-1, 0, 0, 0, 1, 1], np.int32)
+    N = len(par)
+    p0 = np.array([.4, .3, .2, .1])
+    P2 = rng.dirichlet(np.ones(V) * 2, V)      # target after token y: P2[y]
+    q0 = np.array([.1, .2, .3, .4])
+    Q2 = rng.dirichlet(np.ones(V) * 2, V)      # draft after token y
+    P3 = rng.dirichlet(np.ones(V) * 2, V)      # target after the second token (grand-children rows)
+    n = 400_000
+    tok = np.zeros((n, N), np.int32)
+    tok[:, 1:4] = rng.choice(V, (n, 3), p=q0)
+    y1 = tok[:, 1]
+    cdf = np.cumsum(Q2[y1], -1)
+    for c in (4, 5):
+        tok[:, c] = np.minimum((rng.random((n, 1)) * cdf[:, -1:] >= cdf).sum(-1), V - 1)
+    p = np.empty((n, N, V))
+    q = np.empty((n, N, V))
+    p[:, 0], q[:, 0] = p0, q0
+    for c in (1, 2, 3):
+        p[:, c], q[:, c] = P2[tok[:, c]], Q2[tok[:, c]]
+    for c in (4, 5):
+        p[:, c], q[:, c] = P3[tok[:, c]], 1.0 / V
+    r = orc.tree_verify_probs(p, q, np.tile(par, (n, 1)), tok, rng.random((n, N)))
+    assert (r.status == 0).all()
+    first = np.bincount(r.out_tokens[:, 0], minlength=V)
+    assert stats.chisquare(first, p0 * n).pvalue > 1e-3, first / n
+    cont = r.num_emitted >= 2
+    for y in range(V):
+        sel = cont & (r.out_tokens[:, 0] == y)
+        if sel.sum() < 1000:
+            continue
+        h = np.bincount(r.out_tokens[sel, 1], minlength=V)
+        assert stats.chisquare(h, P2[y] * sel.sum()).pvalue > 1e-3, (y, h / sel.sum(), P2[y])
+
+
 ALL_PINS = [
     # cheap first: mutants should fail fast
     pin_worked_example,
@@ -778,6 +911,11 @@ ALL_PINS = [
     pin_lm_head_identity_and_permutation,
     pin_lm_head_rectangular_closed_forms,
     pin_lm_head_matches_library_matmul,
+    pin_tree_hand_example,
+    pin_tree_chain_reduces_to_chain,
+    pin_tree_p_equals_q,
+    pin_tree_invalid_inputs,
     pin_output_distribution,
     pin_expected_tokens,
+    pin_tree_keeps_target_distribution,
 ]

@@ -49,6 +49,17 @@ MUTANTS = [
     ("bf16_round_truncates", "nearbyint(ldexp(m, 8))", "trunc(ldexp(m, 8))", 1),
     ("bf16_round_ties_away", "nearbyint(ldexp(m, 8))", "round(ldexp(m, 8))", 1),
     ("bf16_round_seven_bits", "nearbyint(ldexp(m, 8))", "nearbyint(ldexp(m, 7))", 1),
+    # tree verification
+    ("tree_accept_uses_p", "double a = r[tok[c]] / qv[tok[c]];", "double a = pv[tok[c]] / qv[tok[c]];", 1),
+    ("tree_residual_unnormalised", "r[i] /= Z;", "r[i] /= 1.0;", 1),
+    ("tree_final_from_p", "w[i] = r[i];", "w[i] = pv[i];", 1),
+    ("tree_final_uniform_of_depth", "y = inverse_cdf(w, V, u[0], &Z);", "y = inverse_cdf(w, V, u[len], &Z);", 1),
+    ("tree_siblings_reversed", "for (int32_t c = v + 1; c < N; ++c) {", "for (int32_t c = N - 1; c > v; --c) {", 1),
+    ("tree_accept_le", "if (u[c] < a) {", "if (u[c] <= a) {", 1),
+    ("tree_parent_may_equal_node", "parent[i] >= i)", "parent[i] > i)", 1),
+    ("tree_residual_from_p", "double d = r[i] - qv[i];", "double d = pv[i] - qv[i];", 1),
+    ("tree_child_row_for_test", "const double *qv = Q + (int64_t)v * V;",
+     "const double *qv = Q + (int64_t)(v + 1 < N ? v + 1 : v) * V;", 1),
 ]
 
 
