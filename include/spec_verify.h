@@ -34,8 +34,9 @@
  * acceptance counters), sv_verify_rows / sv_sample_survivors (its two
  * stages), spec_verify_noalloc (no workspace argument), sv_filter_logits
  * (top-k / top-p), spec_verify_lm_head / sv_lm_head_logits (the target's LM
- * head on the tensor cores, fused with the row statistics),
- * sv_workspace_bytes, sv_lm_head_workspace_bytes, sv_kernel_launches,
+ * head on the tensor cores, fused with the row statistics), spec_verify_tree
+ * (a candidate tree: several drafts per position), sv_workspace_bytes,
+ * sv_lm_head_workspace_bytes, sv_tree_workspace_bytes, sv_kernel_launches,
  * sv_status_string.
  *
  * Conventions for every entry point below:
@@ -83,9 +84,11 @@ typedef enum { SV_BF16 = 0, SV_FP32 = 1 } sv_dtype_t;
                                   /* token was drawn from p instead          */
 #define SV_INTERNAL_TIMEOUT 32   /* a kernel's bounded wait ran out (the LM */
                                   /* head's pipeline); outputs undefined     */
+#define SV_BAD_TREE 64           /* spec_verify_tree: parent[i] outside [0, i) */
 
 /* Largest vocabulary supported. */
 #define SV_MAX_V (1 << 21)
+#define SV_MAX_TREE_NODES 256  /* nodes of one candidate tree (spec_verify_tree) */
 
 /* Bytes of workspace spec_verify needs for (B, K, V).  The workspace must be
  * zero-filled before its first use.  A completed spec_verify (or the two
@@ -281,9 +284,9 @@ sv_status_t sv_filter_logits(const void *logits, sv_dtype_t logits_dtype,
  * draws) and each row's softmax statistics are formed by the GEMM's
  * epilogue from those bf16 values, so no separate pass over the logits is
  * made.  Every other argument as spec_verify; the workspace must hold
- * sv_lm_head_workspace_bytes(B, K, V) bytes, zero-filled before first use
- * (calls return the part spec_verify uses to zero; the GEMM's per-tile
- * statistics are rewritten by every call). */
+ * sv_lm_head_workspace_bytes(B, K, V) bytes, zero-filled before first use;
+ * every completed call returns all of it to zero (the GEMM's per-tile
+ * statistics included), so one workspace serves every entry point. */
 size_t sv_lm_head_workspace_bytes(int64_t B, int32_t K, int32_t V);
 sv_status_t sv_lm_head_logits(const void *hidden, const void *lm_head,
                               int64_t M, int32_t d, int32_t V, void *logits,
@@ -298,6 +301,53 @@ sv_status_t spec_verify_lm_head(const void *hidden, const void *lm_head,
                                 float *accept_prob, float *residual_mass,
                                 int32_t *status_dev, void *workspace,
                                 size_t workspace_bytes, void *stream);
+
+/* Verification of a candidate tree: several drafts per position, one path
+ * committed.  The pages require that a tree commits one contiguous path and
+ * keeps the target distribution ("推测解码：草稿、验证与实际加速", section
+ * 链、树与自推测) but give no rule; the rule implemented is multi-step
+ * speculative sampling (SpecInfer, Miao et al., ASPLOS 2024).
+ *
+ * Per sequence, N nodes (1 <= N <= SV_MAX_TREE_NODES): node 0 is the
+ * committed prefix; node i >= 1 holds draft token tokens[i] and has parent
+ * parent[i] in [0, i).  The children of a node are its nodes in increasing
+ * index order and must have been drafted i.i.d. (with replacement) from
+ * that node's draft distribution.
+ *   logits      [B, N, V] bf16 or fp32: row i is the target's next-token
+ *               logits after node i's path (one tree-attention forward);
+ *   draft_probs [B, N, V] fp32: row i is the draft distribution node i's
+ *               children were drawn from (rows of leaves are not read);
+ *   parent, tokens [B, N] int32 (entry 0 of each is not read);
+ *   uniforms    [B, N] fp32 in [0, 1): uniforms[i] (i >= 1) is the
+ *               acceptance test of node i, uniforms[0] the final draw.
+ * From node 0: the children of the current node v are tested in order
+ * against a running target r (first r = p_v = softmax(z_v / T)); child c
+ * with token x is accepted iff u[c] < min(1, r(x) / q_v(x)), and then the
+ * walk continues at c; after a rejection r = max(0, r - q_v) normalised.
+ * When every child of v is rejected the final token is drawn from r, and
+ * at a leaf from p_v, by inverse CDF with u[0].
+ * Outputs: out_tokens [B, N] (the accepted path's tokens, then the final
+ * token, then -1), out_nodes [B, N] (optional: the accepted path's node
+ * ids, then -1), num_emitted [B] (path length + 1), accept_prob [B, N]
+ * (optional: min(1, r(x)/q(x)) of every tested node, -1 for the others).
+ * A sequence with an invalid input emits nothing (num_emitted 0, -1 tokens)
+ * and SV_BAD_U / SV_BAD_TREE / SV_BAD_TOKEN / SV_BAD_Q / SV_BAD_ROW is OR-ed
+ * into *status_dev (optional); SV_DEGENERATE_RESIDUAL as for spec_verify.
+ * The workspace (sv_tree_workspace_bytes(B, N, V) bytes, 256-byte aligned)
+ * follows spec_verify's rule: zero-filled before its first use, returned to
+ * zero by every completed call, so one workspace serves both.  Two launches on `stream` (the row pass over all B*N
+ * rows, then one CTA per sequence for the walk); allocates nothing.
+ * Returns SV_EINVAL / SV_EUNSUPPORTED on bad arguments (nothing launched)
+ * and SV_ECUDA when a launch fails. */
+size_t sv_tree_workspace_bytes(int64_t B, int32_t N, int32_t V);
+sv_status_t spec_verify_tree(const void *logits, sv_dtype_t dtype,
+                             const float *draft_probs, const int32_t *parent,
+                             const int32_t *tokens, const float *uniforms,
+                             float temperature, int64_t B, int32_t N, int32_t V,
+                             int32_t *out_tokens, int32_t *out_nodes,
+                             int32_t *num_emitted, float *accept_prob,
+                             int32_t *status_dev, void *workspace,
+                             size_t workspace_bytes, void *stream);
 
 /* Number of kernels one spec_verify (or spec_verify_stats) call with these
  * arguments launches on the CURRENT device: 2 (the row pass and the draw

@@ -247,3 +247,117 @@ def compare_filter(orc, logits, T, top_k, top_p, cand_out, cand_kept) -> FilterR
         else:
             rep.failures.append((r, f"kept {ng} vs oracle {no} outside the window"))
     return rep
+
+
+# ------------------------------------------------ tree verification
+
+@dataclass
+class TreeReport:
+    sequences: int = 0
+    draws: int = 0
+    excused: int = 0
+    failures: list = field(default_factory=list)
+    max_prob_err: float = 0.0
+
+    def ok(self) -> bool:
+        return not self.failures and self.excused <= MAX_EXCUSED_FRACTION * self.draws
+
+    def summary(self) -> str:
+        s = (f"{self.sequences} sequences, {self.draws} draws, {self.excused} excused, "
+             f"max |dprob| {self.max_prob_err:.2e}, {len(self.failures)} failures")
+        if self.failures:
+            s += "; first: " + str(self.failures[0])
+        return s
+
+
+def compare_tree(orc, logits, q, parent, tokens, u, T, cand, seqs=None) -> TreeReport:
+    """Tree outputs of a candidate (dict of numpy arrays out_tokens,
+    out_nodes, num_emitted, accept_prob or None) against the oracle's, by
+    the same rule as the chain: the path, tokens and count exactly, except a
+    decision whose uniform the fp64 oracle places within 1e-5 relative of
+    its threshold (an accept test with |u - a| <= 1e-5 a, or a final draw
+    whose token moves to the candidate's when u[0] moves by at most 1e-5
+    relative); such draws are excused (at most 1e-4 of all draws) and after
+    an excused accept test the rest is checked against the oracle re-run
+    with that decision forced the candidate's way.  accept_prob of the tested
+    nodes within 1e-5 absolute; a sequence with invalid input emits nothing."""
+    rep = TreeReport()
+    B = logits.shape[0]
+    idx = np.arange(B) if seqs is None else np.asarray(seqs)
+    ores = orc.tree_verify(logits[idx], q[idx], parent[idx], tokens[idx], u[idx], T)
+    for n, b in enumerate(idx):
+        _check_tree(orc, logits, q, parent, tokens, u[b].copy(), T, cand, int(b), ores, n, rep, 0)
+        rep.sequences += 1
+    return rep
+
+
+def _tree_single(orc, logits, q, parent, tokens, u_row, T, b):
+    return orc.tree_verify(logits[b:b + 1], q[b:b + 1], parent[b:b + 1], tokens[b:b + 1], u_row[None], T)
+
+
+def _check_tree(orc, logits, q, parent, tokens, u_row, T, cand, b, ores, oi, rep, depth):
+    N = logits.shape[1]
+    o_tok, o_nodes, o_n = ores.out_tokens[oi], ores.out_nodes[oi], int(ores.num_emitted[oi])
+    o_prob = ores.accept_prob[oi]
+    c_tok, c_n = cand["out_tokens"][b], int(cand["num_emitted"][b])
+    c_nodes = cand["out_nodes"][b] if cand.get("out_nodes") is not None else None
+    c_prob = cand.get("accept_prob")
+    if int(ores.status[oi]) & ~_DEGENERATE:
+        if not (c_n == 0 and (c_tok == -1).all()):
+            rep.failures.append((b, "invalid sequence emitted tokens", int(ores.status[oi])))
+        return
+    if depth == 0:
+        rep.draws += int((o_prob >= 0).sum()) + 1
+    if c_nodes is None:
+        rep.failures.append((b, "out_nodes missing"))
+        return
+    L = o_n - 1
+    cL = c_n - 1
+    # the first node where the two walks decide differently
+    d = 0
+    while d < min(L, cL) and o_nodes[d] == c_nodes[d]:
+        d += 1
+    if d < L or d < cL:
+        cands = [int(x) for x in ((o_nodes[d] if d < L else None), (c_nodes[d] if d < cL else None)) if x is not None]
+        s = min(cands)  # the earlier sibling: one side accepted it, the other rejected it
+        c_acc = d < cL and c_nodes[d] == s
+        a = float(o_prob[s]) if 0 <= s < N else -1.0
+        if a >= 0 and abs(float(u_row[s]) - a) <= WINDOW * a:
+            rep.excused += 1
+            forced = _forced_u(a, c_acc)
+            if forced is None or depth > 4:
+                return
+            u2 = u_row.copy()
+            u2[s] = forced
+            r2 = _tree_single(orc, logits, q, parent, tokens, u2, T, b)
+            _check_tree(orc, logits, q, parent, tokens, u2, T, cand, b, r2, 0, rep, depth + 1)
+            return
+        rep.failures.append((b, f"accept decision at node {s}", float(u_row[s]) if s < N else None, a))
+        return
+    if not (c_tok[c_n:] == -1).all() or not (c_nodes[L:] == -1).all():
+        rep.failures.append((b, "padding"))
+        return
+    if not np.array_equal(c_tok[:L], o_tok[:L]):
+        rep.failures.append((b, "path tokens"))
+        return
+    if c_prob is not None and depth == 0:
+        tested = o_prob >= 0
+        err = float(np.max(np.abs(c_prob[b][tested].astype(np.float64) - o_prob[tested]))) if tested.any() else 0.0
+        rep.max_prob_err = max(rep.max_prob_err, err)
+        if not err <= TOL_PROB:
+            rep.failures.append((b, "accept_prob", err))
+        if not (c_prob[b][~tested] == -1).all():
+            rep.failures.append((b, "accept_prob of untested nodes"))
+    g, o = int(c_tok[L]), int(o_tok[L])
+    if g == o:
+        return
+    # the final draw: excused if moving u[0] by 1e-5 relative reaches g
+    lo, hi = u_row.copy(), u_row.copy()
+    lo[0] = np.float32(float(u_row[0]) * (1 - WINDOW))
+    hi[0] = min(np.float32(float(u_row[0]) * (1 + WINDOW)), np.nextafter(np.float32(1), np.float32(0)))
+    y_lo = int(_tree_single(orc, logits, q, parent, tokens, lo, T, b).out_tokens[0, L])
+    y_hi = int(_tree_single(orc, logits, q, parent, tokens, hi, T, b).out_tokens[0, L])
+    if min(y_lo, y_hi) <= g <= max(y_lo, y_hi):
+        rep.excused += 1
+    else:
+        rep.failures.append((b, "final token", g, o, float(u_row[0])))

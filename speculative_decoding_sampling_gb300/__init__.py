@@ -15,12 +15,14 @@ from ._native import (SV_BAD_Q, SV_BAD_ROW, SV_BAD_TOKEN, SV_BAD_U, SV_BF16,
 from .binding import (SpecVerifyError, SpecVerifyResult, default_workspace,
                       spec_verify, sv_filter_logits, sv_kernel_launches, sv_sample_survivors,
                       sv_status_string, sv_verify_rows, sv_workspace_bytes,
-                      spec_verify_lm_head, sv_lm_head_logits, sv_lm_head_workspace_bytes)
+                      spec_verify_lm_head, sv_lm_head_logits, sv_lm_head_workspace_bytes,
+                      TreeResult, spec_verify_tree, sv_tree_workspace_bytes)
 from . import adaptive
 
 __all__ = [
     "spec_verify", "sv_verify_rows", "sv_sample_survivors",
     "spec_verify_lm_head", "sv_lm_head_logits", "sv_lm_head_workspace_bytes",
+    "spec_verify_tree", "sv_tree_workspace_bytes", "TreeResult",
     "sv_workspace_bytes", "sv_filter_logits", "sv_kernel_launches", "sv_status_string", "default_workspace",
     "SpecVerifyResult", "SpecVerifyError", "NativeLibraryMissing",
     "SV_OK", "SV_EINVAL", "SV_ECUDA", "SV_EUNSUPPORTED", "SV_BF16", "SV_FP32",

@@ -10,12 +10,15 @@ SV_OK, SV_EINVAL, SV_ECUDA, SV_EUNSUPPORTED = 0, 1, 2, 3
 SV_BF16, SV_FP32 = 0, 1
 SV_BAD_U, SV_BAD_TOKEN, SV_BAD_Q, SV_BAD_ROW, SV_DEGENERATE_RESIDUAL = 1, 2, 4, 8, 16
 SV_INTERNAL_TIMEOUT = 32
+SV_BAD_TREE = 64
+SV_MAX_TREE_NODES = 256
 SV_MAX_V = 1 << 21
 
 # every function the header declares, in declaration order
 EXPORTS = ["sv_workspace_bytes", "spec_verify", "spec_verify_stats", "sv_verify_rows",
            "sv_sample_survivors", "spec_verify_noalloc", "sv_filter_logits", "sv_lm_head_workspace_bytes",
-           "sv_lm_head_logits", "spec_verify_lm_head", "sv_kernel_launches", "sv_status_string"]
+           "sv_lm_head_logits", "spec_verify_lm_head", "sv_tree_workspace_bytes", "spec_verify_tree",
+           "sv_kernel_launches", "sv_status_string"]
 
 
 def stats_words(K: int) -> int:
@@ -66,6 +69,13 @@ def lib() -> ctypes.CDLL:
         L.sv_lm_head_logits.restype = ctypes.c_int
         L.sv_lm_head_logits.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
                                         ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        L.sv_tree_workspace_bytes.restype = ctypes.c_size_t
+        L.sv_tree_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]
+        L.spec_verify_tree.restype = ctypes.c_int
+        L.spec_verify_tree.argtypes = [
+            ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_float, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
         L.spec_verify_lm_head.restype = ctypes.c_int
         L.spec_verify_lm_head.argtypes = ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32] +
                                           _VERIFY_ARGTYPES[2:9] + [ctypes.c_void_p] + _VERIFY_ARGTYPES[9:])

@@ -358,3 +358,65 @@ def spec_verify_lm_head(hidden: torch.Tensor, lm_head: torch.Tensor, draft_probs
     if rc != N.SV_OK:
         raise SpecVerifyError(rc)
     return res, logits_out
+
+
+# ------------------------------------------------------------- trees
+
+@dataclass
+class TreeResult:
+    out_tokens: torch.Tensor           # [B, N] int32: the accepted path's tokens, the final token, then -1
+    out_nodes: torch.Tensor            # [B, N] int32: the accepted path's node ids, then -1
+    num_emitted: torch.Tensor          # [B] int32
+    accept_prob: torch.Tensor | None   # [B, N] fp32: min(1, r(x)/q(x)) of each tested node, -1 otherwise
+    status: torch.Tensor | None = None
+
+
+def sv_tree_workspace_bytes(B: int, nodes: int, V: int) -> int:
+    return int(N.lib().sv_tree_workspace_bytes(int(B), int(nodes), int(V)))
+
+
+def spec_verify_tree(logits: torch.Tensor, draft_probs: torch.Tensor, parent: torch.Tensor, tokens: torch.Tensor,
+                     uniforms: torch.Tensor, temperature: float, *, want_probs: bool = True,
+                     workspace: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                     stream: torch.cuda.Stream | None = None) -> TreeResult:
+    """Verification of a candidate tree (multi-step speculative sampling):
+    logits [B, N, V] bf16 / fp32 (row i: the target after node i's path),
+    draft_probs [B, N, V] fp32 (row i: the draft distribution of node i's
+    children), parent / tokens [B, N] int32, uniforms [B, N] fp32."""
+    if logits.dim() != 3:
+        raise ValueError("logits must be [B, N, V]")
+    B, Nn, V = logits.shape
+    dev = logits.device
+    dt = N.SV_BF16 if logits.dtype == torch.bfloat16 else (N.SV_FP32 if logits.dtype == torch.float32 else None)
+    if dt is None:
+        raise TypeError("logits must be bfloat16 or float32")
+    _check(logits, "logits", logits.dtype, (B, Nn, V), dev)
+    _check(draft_probs, "draft_probs", torch.float32, (B, Nn, V), dev)
+    _check(parent, "parent", torch.int32, (B, Nn), dev)
+    _check(tokens, "tokens", torch.int32, (B, Nn), dev)
+    _check(uniforms, "uniforms", torch.float32, (B, Nn), dev)
+    need = sv_tree_workspace_bytes(B, Nn, V)
+    if need == 0 and B > 0:
+        raise SpecVerifyError(N.SV_EUNSUPPORTED)
+    stream = stream or torch.cuda.current_stream(dev)
+    if workspace is None:
+        workspace = default_workspace(dev, need)
+        if stream != torch.cuda.current_stream(dev):
+            workspace.record_stream(stream)
+    elif workspace.device != dev or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must hold {need} bytes on {dev}")
+    if status is not None:
+        _check(status, "status", torch.int32, (1,), dev)
+    res = TreeResult(out_tokens=torch.empty((B, Nn), dtype=torch.int32, device=dev),
+                     out_nodes=torch.empty((B, Nn), dtype=torch.int32, device=dev),
+                     num_emitted=torch.empty((B,), dtype=torch.int32, device=dev),
+                     accept_prob=torch.empty((B, Nn), dtype=torch.float32, device=dev) if want_probs else None,
+                     status=status)
+    rc = N.lib().spec_verify_tree(
+        logits.data_ptr(), dt, draft_probs.data_ptr(), parent.data_ptr(), tokens.data_ptr(), uniforms.data_ptr(),
+        float(temperature), B, Nn, V, res.out_tokens.data_ptr(), res.out_nodes.data_ptr(),
+        res.num_emitted.data_ptr(), _ptr(res.accept_prob), _ptr(status), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), stream.cuda_stream)
+    if rc != N.SV_OK:
+        raise SpecVerifyError(rc)
+    return res

@@ -15,6 +15,7 @@
 #include "sv_filter.cuh"
 #include "sv_final.cuh"
 #include "sv_lmhead.cuh"
+#include "sv_tree.cuh"
 #include "sv_rows.cuh"
 
 namespace {
@@ -190,7 +191,7 @@ cudaError_t launches_per_call(int64_t B, const Plan &plan, int32_t &n)
 }
 
 template <typename LT, bool DENSE>
-cudaError_t launch(sv::Params P, const Plan &plan, int stages, cudaStream_t stream)
+cudaError_t launch(sv::Params &P, const Plan &plan, int stages, cudaStream_t stream)
 {
     if (stages == 0)
         return cudaSuccess;
@@ -482,6 +483,9 @@ cudaError_t lm_launch(const void *hidden, const void *lm_head, int64_t M, int32_
     return cudaLaunchKernelEx(&cfg, sv::lm_head_kernel, ta, tb, L);
 }
 
+static_assert(sv::kTreeMaxNodes == SV_MAX_TREE_NODES, "tree size limit");
+static_assert(sv::kBadTree == SV_BAD_TREE, "status bit");
+
 } // namespace
 
 extern "C" {
@@ -702,6 +706,94 @@ sv_status_t spec_verify_lm_head(const void *hidden, const void *lm_head, int32_t
     return run(kSurvivors, logits_out, SV_BF16, draft_probs, draft_tokens, uniforms, temperature, B, K, V, out_tokens,
                num_emitted, accept_flags, accept_prob, residual_mass, status_dev, workspace, plan.bytes, stream,
                nullptr, 1);
+}
+
+size_t sv_tree_workspace_bytes(int64_t B, int32_t N, int32_t V)
+{
+    Plan p;
+    if (N < 1 || N > SV_MAX_TREE_NODES || !make_plan(B, N - 1, V, p))
+        return 0;
+    return p.bytes;
+}
+
+sv_status_t spec_verify_tree(const void *logits, sv_dtype_t dtype, const float *draft_probs, const int32_t *parent,
+                             const int32_t *tokens, const float *uniforms, float temperature, int64_t B, int32_t N,
+                             int32_t V, int32_t *out_tokens, int32_t *out_nodes, int32_t *num_emitted,
+                             float *accept_prob, int32_t *status_dev, void *workspace, size_t workspace_bytes,
+                             void *stream)
+{
+    if (B < 0 || N < 1 || V < 1)
+        return SV_EINVAL;
+    if (N > SV_MAX_TREE_NODES || V > SV_MAX_V || B > 0x7FFFFFFFll)
+        return SV_EUNSUPPORTED;
+    if (dtype != SV_BF16 && dtype != SV_FP32)
+        return SV_EINVAL;
+    if (!std::isfinite(temperature) || !(temperature > 0.0f))
+        return SV_EINVAL;
+    const float c = static_cast<float>(1.4426950408889634074 / static_cast<double>(temperature));
+    if (!std::isfinite(c) || !(c > 0.0f))
+        return SV_EINVAL;
+    if (!logits || !draft_probs || !parent || !tokens || !uniforms || !out_tokens || !num_emitted || !workspace)
+        return SV_EINVAL;
+    const size_t esize = dtype == SV_BF16 ? 2 : 4;
+    if (!aligned(logits, esize) || !aligned(draft_probs, 4) || !aligned(parent, 4) || !aligned(tokens, 4) ||
+        !aligned(uniforms, 4) || !aligned(out_tokens, 4) || !aligned(num_emitted, 4) ||
+        (out_nodes && !aligned(out_nodes, 4)) || (accept_prob && !aligned(accept_prob, 4)) ||
+        (status_dev && !aligned(status_dev, 4)) || !aligned(workspace, kAlign))
+        return SV_EINVAL;
+    Plan plan;
+    if (!make_plan(B, N - 1, V, plan))
+        return SV_EUNSUPPORTED;
+    if (workspace_bytes < plan.bytes)
+        return SV_EINVAL;
+    if (B == 0)
+        return SV_OK;
+    char *ws = static_cast<char *>(workspace);
+    sv::Params P = {};
+    P.logits = logits;
+    P.q = nullptr; // the row pass takes no draft data here; the tree kernel reads q
+    P.tokens = tokens;
+    P.u = uniforms;
+    P.c = c;
+    P.B = B;
+    P.K = N - 1;
+    P.V = V;
+    P.row_part = reinterpret_cast<float2 *>(ws + plan.off_part);
+    P.row_side = reinterpret_cast<float4 *>(ws + plan.off_row_side);
+    P.PM = plan.PM;
+    P.fix_bits = plan.fix;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the row pass over all B*N rows: every row's (max, normaliser) partials
+    cudaError_t e = dtype == SV_BF16 ? launch<uint16_t, false>(P, plan, kRows, s)
+                                     : launch<float, false>(P, plan, kRows, s);
+    if (e != cudaSuccess)
+        return SV_ECUDA;
+    sv::TreeArgs A;
+    A.parent = parent;
+    A.tokens = tokens;
+    A.q = draft_probs;
+    A.u = uniforms;
+    A.N = N;
+    A.out_tokens = out_tokens;
+    A.out_nodes = out_nodes;
+    A.num_emitted = num_emitted;
+    A.accept_prob = accept_prob;
+    A.status = status_dev;
+    const size_t smem = static_cast<size_t>(ceil_div(V, sv::kTreeChunk)) * sizeof(long long);
+    if (dtype == SV_BF16) {
+        if (smem > 48 * 1024 &&
+            cudaFuncSetAttribute(sv::tree_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem)) != cudaSuccess)
+            return SV_ECUDA;
+        sv::tree_kernel<uint16_t><<<static_cast<unsigned>(B), sv::kTreeThreads, smem, s>>>(P, A);
+    } else {
+        if (smem > 48 * 1024 &&
+            cudaFuncSetAttribute(sv::tree_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem)) != cudaSuccess)
+            return SV_ECUDA;
+        sv::tree_kernel<float><<<static_cast<unsigned>(B), sv::kTreeThreads, smem, s>>>(P, A);
+    }
+    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 
 const char *sv_status_string(sv_status_t status)

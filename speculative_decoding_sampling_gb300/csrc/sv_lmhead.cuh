@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
 // row's partials), and its draft token, z(x) (from the stored logits), q(x)
 // and uniform.
 template <bool DENSE>
-__global__ void __launch_bounds__(256) lm_merge_kernel(const Params P, const float2 *part, int32_t NT)
+__global__ void __launch_bounds__(256) lm_merge_kernel(const Params P, float2 *part, int32_t NT)
 {
     const int lane = threadIdx.x & 31;
     const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
@@ -463,6 +463,7 @@ __global__ void __launch_bounds__(256) lm_merge_kernel(const Params P, const flo
         float M = -INFINITY, S = 0.0f;
         for (int32_t i = lane; i < NT; i += 32) {
             const float2 pr = part[r * NT + i];
+            part[r * NT + i] = make_float2(0.0f, 0.0f); // the workspace goes back to zero once read
             merge_ms(M, S, pr.x, pr.y, P.c);
         }
         warp_merge_ms(M, S, P.c);

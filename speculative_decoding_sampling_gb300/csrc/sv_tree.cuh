@@ -1,0 +1,370 @@
+// sv_tree.cuh -- verification of a candidate tree (several drafts per node).
+//
+// The rule is multi-step speculative sampling (SpecInfer, Miao et al.,
+// ASPLOS 2024): the pages require that a tree commits one contiguous path
+// and keeps the target distribution, and that the chain's single-candidate
+// correction is not applied to a tree as it stands ("推测解码：草稿、验证与
+// 实际加速", section 链、树与自推测), but give no rule of their own.
+//
+// Sequence b has N nodes; node 0 is the committed prefix, node i >= 1 holds
+// a draft token and parent[i] < i.  Row i of the logits gives p_i, the
+// target's next-token distribution after node i's path; row i of q is the
+// draft distribution node i's children were drawn from (i.i.d.).  From
+// v = 0: the children of v, in index order, are tested against a running
+// target r (first r = p_v): child c with token x is accepted iff
+// u[c] < min(1, r(x) / q_v(x)); after a rejection r becomes
+// max(0, r - q_v) normalised.  That residual has a closed form: after k
+// rejections r = max(0, p_v - C_k q_v) / W_k with C_1 = 1,
+// W_k = sum max(0, p_v - C_k q_v) and C_{k+1} = C_k + W_k, so each
+// rejection is one pass over row v (p and q) for W_k.  When every child is
+// rejected the final token is drawn from the last residual with u[0]; at a
+// leaf it is drawn from p_v with u[0] (inverse CDF in id order).
+//
+// The row pass (rows_kernel over all B*N rows) supplies each row's
+// (max, normaliser) partials; this kernel, one CTA per sequence, merges
+// them, checks the inputs and walks the tree.  Masses in the passes are
+// exact integer multiples of 2^-fix_bits (to_fixed), so sums are
+// order-independent and the draw's boundaries agree with its totals.
+#pragma once
+
+#include "sv_rows.cuh"
+
+namespace sv {
+
+constexpr int kTreeThreads = 256;
+constexpr int kTreeWarps = kTreeThreads / 32;
+constexpr int kTreeChunk = 256;     // ids per warp chunk: 8 per lane
+constexpr int kTreeMaxNodes = 256;   // nodes of one tree (the C ABI's SV_MAX_TREE_NODES)
+constexpr int32_t kBadTree = 64;
+
+struct TreeArgs {
+    const int32_t *parent;  // [B, N]
+    const int32_t *tokens;  // [B, N]
+    const float *q;         // [B, N, V]
+    const float *u;         // [B, N]
+    int32_t N;
+    int32_t *out_tokens;    // [B, N]
+    int32_t *out_nodes;     // [B, N] or nullptr
+    int32_t *num_emitted;   // [B]
+    float *accept_prob;     // [B, N] or nullptr
+    int32_t *status;        // or nullptr
+};
+
+struct TreeRow {
+    const void *z;   // logits row (LT)
+    const float *q;  // draft row
+    float c, mc, inv_s;
+};
+
+// The fixed-point weight of id i of a row: p_i (bonus) or max(0, p_i - C q_i).
+template <typename LT>
+__device__ __forceinline__ long long tree_weight(const TreeRow &R, int32_t i, bool resid, float C, int fb)
+{
+    const float p = __fmul_rn(term(load_elem<LT>(static_cast<const LT *>(R.z) + i), R.c, R.mc), R.inv_s);
+    if (!resid)
+        return to_fixed(p, fb);
+    const float w = __fmaf_rn(-C, __ldg(R.q + i), p);
+    return w > 0.0f ? to_fixed(w, fb) : 0ll;
+}
+
+// One pass over the row: per-chunk totals into chunk[] and the row total
+// (returned to every thread).  Warp w takes chunks w, w + 8, ...; lane l the
+// 8 ids 8l .. 8l + 7 of a chunk.
+template <typename LT>
+__device__ long long tree_pass(const TreeRow &R, int32_t V, bool resid, float C, int fb, long long *chunk,
+                               long long *red)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int32_t nch = (V + kTreeChunk - 1) / kTreeChunk;
+    long long mine = 0;
+    for (int32_t ch = warp; ch < nch; ch += kTreeWarps) {
+        const int32_t i0 = ch * kTreeChunk + lane * 8;
+        long long s = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (i0 + k < V)
+                s += tree_weight<LT>(R, i0 + k, resid, C, fb);
+        s = warp_sum_ll(s);
+        if (lane == 0)
+            chunk[ch] = s;
+        mine += s;
+    }
+    if (lane == 0)
+        red[warp] = mine;
+    __syncthreads();
+    long long tot = 0;
+#pragma unroll
+    for (int w = 0; w < kTreeWarps; ++w)
+        tot += red[w];
+    __syncthreads(); // red[] is reused
+    return tot;
+}
+
+// Hand-off slots of tree_find (shared memory).
+struct TreeSel {
+    long long base; // cumulative weight before the chosen chunk
+    int32_t chunk;  // the chunk holding t, or -1
+    int32_t id;     // the id found, or -1
+};
+
+// First id whose cumulative weight exceeds t (0 <= t < total), from the
+// chunk totals of the last pass over the same weights; every thread gets
+// it.  If rounding leaves none, the last id of positive weight.
+template <typename LT>
+__device__ int32_t tree_find(const TreeRow &R, int32_t V, bool resid, float C, int fb, long long t,
+                             const long long *chunk, long long *red, TreeSel *sel)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int32_t nch = (V + kTreeChunk - 1) / kTreeChunk;
+    // thread j owns chunks [j*per, (j+1)*per): their total, an exclusive
+    // block scan, and the one thread whose range holds t finds the chunk
+    const int32_t per = (nch + kTreeThreads - 1) / kTreeThreads;
+    const int32_t c0 = threadIdx.x * per;
+    long long own = 0;
+    for (int32_t k = 0; k < per && c0 + k < nch; ++k)
+        own += chunk[c0 + k];
+    long long inc = own; // inclusive warp scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o)
+            inc += y;
+    }
+    if (lane == 31)
+        red[warp] = inc;
+    if (threadIdx.x == 0) {
+        sel->chunk = -1;
+        sel->id = -1;
+    }
+    __syncthreads();
+    long long before = inc - own;
+    for (int w = 0; w < warp; ++w)
+        before += red[w];
+    if (own > 0 && before <= t && t < before + own) {
+        long long acc = before;
+        for (int32_t k = 0; k < per && c0 + k < nch; ++k) {
+            if (t < acc + chunk[c0 + k]) {
+                sel->chunk = c0 + k;
+                sel->base = acc;
+                break;
+            }
+            acc += chunk[c0 + k];
+        }
+    }
+    __syncthreads();
+    const int32_t ch = sel->chunk;
+    if (ch >= 0 && warp == 0) {
+        // the chunk: lane sums of 8 ids, exclusive scan, then the lane's ids
+        const int32_t i0 = ch * kTreeChunk + lane * 8;
+        long long w8[8];
+        long long s = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            w8[k] = i0 + k < V ? tree_weight<LT>(R, i0 + k, resid, C, fb) : 0ll;
+            s += w8[k];
+        }
+        long long inc2 = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(0xFFFFFFFFu, inc2, o);
+            if (lane >= o)
+                inc2 += y;
+        }
+        long long acc = sel->base + inc2 - s;
+        int32_t id = -1;
+        if (s > 0 && acc <= t && t < acc + s)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                acc += w8[k];
+                if (id < 0 && t < acc)
+                    id = i0 + k;
+            }
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, id >= 0);
+        const int32_t first = __shfl_sync(0xFFFFFFFFu, id, m ? __ffs(m) - 1 : 0);
+        if (lane == 0)
+            sel->id = m ? first : -1;
+    }
+    __syncthreads();
+    if (sel->id < 0) { // rounding left no id below t: the last id of positive weight
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int32_t last = 0;
+            for (int32_t i = V - 1; i >= 0; --i)
+                if (tree_weight<LT>(R, i, resid, C, fb) > 0) {
+                    last = i;
+                    break;
+                }
+            sel->id = last;
+        }
+        __syncthreads();
+    }
+    const int32_t id = sel->id;
+    __syncthreads(); // sel is reused
+    return id;
+}
+
+template <typename LT>
+__global__ void __launch_bounds__(kTreeThreads) tree_kernel(const Params P, const TreeArgs A)
+{
+    extern __shared__ long long tree_chunk[]; // [ceil(V / 256)] chunk totals of the last pass
+    __shared__ int32_t s_par[kTreeMaxNodes], s_tok[kTreeMaxNodes];
+    __shared__ float s_u[kTreeMaxNodes], s_M[kTreeMaxNodes], s_S[kTreeMaxNodes];
+    __shared__ long long s_red[kTreeWarps];
+    __shared__ TreeSel s_sel;
+    __shared__ int32_t s_bad, s_flag;
+    const int64_t b = blockIdx.x;
+    const int32_t N = A.N, V = static_cast<int32_t>(P.V);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float c = P.c;
+
+    if (threadIdx.x == 0)
+        s_bad = 0;
+    for (int32_t i = threadIdx.x; i < N; i += kTreeThreads) {
+        s_par[i] = A.parent[b * N + i];
+        s_tok[i] = A.tokens[b * N + i];
+        s_u[i] = A.u[b * N + i];
+    }
+    // each row's (max, normaliser): the merge of its row-pass partials
+    for (int32_t i = warp; i < N; i += kTreeWarps) {
+        const int64_t r = b * N + i;
+        int64_t first;
+        int n;
+        row_ctas<LT>(P, r, first, n);
+        float M = -INFINITY, S = 0.0f;
+        for (int k = lane; k < n; k += 32) {
+            const float2 pr = __ldcg(&P.row_part[r * P.PM + k]);
+            merge_ms(M, S, pr.x, pr.y, c);
+        }
+        warp_merge_ms(M, S, c);
+        if (lane == 0) {
+            s_M[i] = M;
+            s_S[i] = S;
+        }
+    }
+    __syncthreads();
+    // the row pass's scratch of this sequence goes back to zero once read
+    // (the workspace is shared with spec_verify, which expects it zeroed)
+    for (int64_t i = threadIdx.x; i < static_cast<int64_t>(N) * P.PM; i += kTreeThreads)
+        P.row_part[b * N * P.PM + i] = make_float2(0.0f, 0.0f);
+    for (int32_t i = threadIdx.x; i < N; i += kTreeThreads)
+        P.row_side[b * N + i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    // the inputs: u in [0, 1), parents before their nodes, tokens in range
+    // with positive draft probability, finite rows
+    for (int32_t i = threadIdx.x; i < N; i += kTreeThreads) {
+        int32_t bad = 0;
+        if (!(s_u[i] >= 0.0f && s_u[i] < 1.0f))
+            bad |= kBadU;
+        if (!(isfinite(s_M[i]) && isfinite(s_S[i])))
+            bad |= kBadRow;
+        if (i >= 1) {
+            const int32_t pa = s_par[i], x = s_tok[i];
+            if (pa < 0 || pa >= i) {
+                bad |= kBadTree;
+            } else if (x < 0 || x >= V) {
+                bad |= kBadToken;
+            } else {
+                const float qx = __ldg(A.q + (b * N + pa) * static_cast<int64_t>(V) + x);
+                if (!(qx > 0.0f && isfinite(qx)))
+                    bad |= kBadQ;
+            }
+        }
+        if (bad)
+            atomicOr(&s_bad, bad);
+    }
+    __syncthreads();
+    const int32_t bad = s_bad;
+    if (bad) {
+        for (int32_t i = threadIdx.x; i < N; i += kTreeThreads) {
+            A.out_tokens[b * N + i] = -1;
+            if (A.out_nodes) A.out_nodes[b * N + i] = -1;
+            if (A.accept_prob) A.accept_prob[b * N + i] = -1.0f;
+        }
+        if (threadIdx.x == 0) {
+            A.num_emitted[b] = 0;
+            if (A.status) atomicOr(A.status, bad);
+        }
+        return;
+    }
+    if (A.accept_prob)
+        for (int32_t i = threadIdx.x; i < N; i += kTreeThreads)
+            A.accept_prob[b * N + i] = -1.0f;
+
+    const int fb = P.fix_bits;
+    int32_t v = 0, len = 0, y = 0, status = 0;
+    for (;;) {
+        TreeRow R;
+        R.z = static_cast<const LT *>(P.logits) + (b * N + v) * static_cast<int64_t>(V);
+        R.q = A.q + (b * N + v) * static_cast<int64_t>(V);
+        R.c = c;
+        R.mc = mc_of(s_M[v], c);
+        R.inv_s = __frcp_rn(s_S[v]);
+        int32_t nrej = 0, next = -1;
+        float C = 1.0f, W = 0.0f; // the residual max(0, p - C q) / W after nrej rejections
+        long long Wfix = 0;
+        bool degenerate = false;
+        for (int32_t ch = v + 1; ch < N; ++ch) {
+            if (s_par[ch] != v)
+                continue;
+            if (threadIdx.x == 0) {
+                const int32_t x = s_tok[ch];
+                const float px = __fmul_rn(term(load_elem<LT>(static_cast<const LT *>(R.z) + x), c, R.mc), R.inv_s);
+                const float qx = __ldg(R.q + x);
+                const float rx = nrej == 0 ? px : __fdiv_rn(fmaxf(__fmaf_rn(-C, qx, px), 0.0f), W);
+                const float a = fminf(1.0f, __fdiv_rn(rx, qx));
+                if (A.accept_prob)
+                    A.accept_prob[b * N + ch] = a;
+                s_flag = s_u[ch] < a ? 1 : 0;
+            }
+            __syncthreads();
+            const bool acc = s_flag != 0;
+            __syncthreads();
+            if (acc) {
+                next = ch;
+                break;
+            }
+            // rejected: the next residual's constant and normaliser
+            C = nrej == 0 ? 1.0f : __fadd_rn(C, W);
+            ++nrej;
+            Wfix = tree_pass<LT>(R, V, true, C, fb, tree_chunk, s_red);
+            W = ldexpf(static_cast<float>(Wfix), -fb);
+            if (Wfix <= 0) {
+                degenerate = true;
+                break;
+            }
+        }
+        if (next >= 0) {
+            if (threadIdx.x == 0) {
+                A.out_tokens[b * N + len] = s_tok[next];
+                if (A.out_nodes) A.out_nodes[b * N + len] = next;
+            }
+            ++len;
+            v = next;
+            continue;
+        }
+        // the final draw, with u[0]: from the residual after the last
+        // rejection, else (a leaf, or a residual with no mass) from p_v
+        const bool resid = nrej > 0 && !degenerate;
+        long long tot = Wfix;
+        if (!resid)
+            tot = tree_pass<LT>(R, V, false, 0.0f, fb, tree_chunk, s_red);
+        if (degenerate)
+            status |= kDegenerate;
+        const long long t = mul_floor(s_u[0], tot);
+        y = tree_find<LT>(R, V, resid, C, fb, t, tree_chunk, s_red, &s_sel);
+        break;
+    }
+    if (threadIdx.x == 0) {
+        A.out_tokens[b * N + len] = y;
+        A.num_emitted[b] = len + 1;
+        if (status && A.status)
+            atomicOr(A.status, status);
+    }
+    for (int32_t i = len + threadIdx.x; i < N; i += kTreeThreads) {
+        if (i > len)
+            A.out_tokens[b * N + i] = -1;
+        if (A.out_nodes)
+            A.out_nodes[b * N + i] = -1;
+    }
+}
+
+} // namespace sv

@@ -227,3 +227,38 @@ def drafts_for(z: np.ndarray, T: float, draft_sigma: float, seed: int = DEFAULT_
         tokens[b0:b1] = np.minimum((cdf <= t).sum(-1), V - 1)
         q[b0:b1] = qq
     return q, tokens, u
+
+
+# Candidate-tree shapes (parent of each node; node 0 is the committed prefix).
+TREE_SHAPES = {
+    # 16 nodes, depth 5: the root has 3 children, its first child 3, ...
+    "tree16": [-1, 0, 0, 0, 1, 1, 1, 2, 2, 3, 4, 4, 5, 7, 10, 14],
+    "chain5": [-1, 0, 1, 2, 3],
+    "star7": [-1, 0, 0, 0, 0, 0, 0],
+}
+
+
+def tree_inputs(w: Workload | str, parent, seed: int = DEFAULT_SEED, nb: int | None = None):
+    """Inputs of a candidate-tree verification with the shapes and value
+    distributions of workload `w` (dense drafts): logits [B, N, V] and the
+    draft rows q [B, N, V] come from the workload's generator with K = N - 1
+    (row i of q: the draft distribution at node i; the last node is always a
+    leaf and its row is zero), each node's token is drawn from its parent's
+    q row (siblings i.i.d.), uniforms [B, N].  Returns
+    (logits, q, parent [B, N], tokens [B, N], u [B, N], T)."""
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    parent = np.asarray(parent, np.int32)
+    N = len(parent)
+    inp = generate(w.with_(K=N - 1), seed=seed, nb=nb)
+    B, V = inp.logits.shape[0], w.V
+    q = np.concatenate([inp.q, np.zeros((B, 1, V), np.float32)], 1)
+    rng = np.random.default_rng([seed, N, V, 7])
+    tokens = np.zeros((B, N), np.int32)
+    for v in sorted(set(parent[1:].tolist())):
+        kids = np.nonzero(parent == v)[0]
+        cdf = np.cumsum(q[:, v].astype(np.float64), -1)
+        t = rng.random((B, len(kids))) * cdf[:, -1:]
+        tokens[:, kids] = np.minimum(np.array([np.searchsorted(cdf[b], t[b], side="right") for b in range(B)]),
+                                     V - 1)
+    return inp.logits, q, np.tile(parent, (B, 1)), tokens, inp.u, w.T

@@ -190,3 +190,34 @@ def test_lm_head_verify_host_checks(kw):
 
 def test_lm_head_verify_empty_batch():
     assert _lm_verify(B=0) == N.SV_OK
+
+
+# ----------------------------------------------------------------- trees
+
+def _tree(**kw):
+    fake = 1 << 40
+    a = dict(logits=fake, dtype=N.SV_BF16, q=fake, parent=fake, tok=fake, u=fake, T=1.0, B=4, N=16, V=1000,
+             out=fake, nodes=None, n=fake, prob=None, status=None, ws=fake, ws_bytes=1 << 24, stream=None)
+    a.update(kw)
+    return N.lib().spec_verify_tree(a["logits"], a["dtype"], a["q"], a["parent"], a["tok"], a["u"],
+                                    ctypes.c_float(a["T"]), a["B"], a["N"], a["V"], a["out"], a["nodes"], a["n"],
+                                    a["prob"], a["status"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(logits=None), dict(q=None), dict(parent=None), dict(tok=None), dict(u=None), dict(out=None),
+    dict(n=None), dict(ws=None), dict(N=0), dict(B=-1), dict(V=0), dict(T=0.0), dict(T=float("nan")),
+    dict(dtype=5), dict(logits=(1 << 40) + 1), dict(parent=(1 << 40) + 2), dict(ws=(1 << 40) + 8),
+    dict(nodes=(1 << 40) + 1), dict(ws_bytes=100),
+], ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_tree_host_checks(kw):
+    assert _tree(**kw) == N.SV_EINVAL
+
+
+def test_tree_sizes():
+    assert _tree(N=N.SV_MAX_TREE_NODES + 1) == N.SV_EUNSUPPORTED
+    assert _tree(V=N.SV_MAX_V + 1) == N.SV_EUNSUPPORTED
+    assert _tree(B=0) == N.SV_OK
+    assert sv.sv_tree_workspace_bytes(64, 16, 128256) == sv.sv_workspace_bytes(64, 15, 128256)
+    assert sv.sv_tree_workspace_bytes(4, 0, 100) == 0
+    assert sv.sv_tree_workspace_bytes(4, N.SV_MAX_TREE_NODES + 1, 100) == 0

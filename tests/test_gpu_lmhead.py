@@ -169,3 +169,17 @@ def test_fused_full_size_sampled(orc):
     sub = {k: (v[seqs] if isinstance(v, np.ndarray) else v) for k, v in cand.items()}
     rep = parity.compare(orc, z_rows, q[seqs], tokens[seqs], u[seqs], T, sub)
     assert rep.ok(), rep.summary()
+
+
+def test_fused_returns_workspace_to_zero():
+    """Every byte of the workspace (the GEMM's per-tile statistics included)
+    is zero again after a call, as spec_verify's rule requires."""
+    B, K, V, d = 9, 3, 3000, 128
+    h, W = synth.lm_head_inputs(B * (K + 1), d, V, seed=12, dyadic=True)
+    z = np.zeros((B, K + 1, V))
+    q, tokens, u = synth.drafts_for(z, 1.0, 1.0, seed=3)
+    ws = torch.zeros(sv.sv_lm_head_workspace_bytes(B, K, V), dtype=torch.uint8, device=DEV)
+    sv.spec_verify_lm_head(_dev_bf16(h).view(B, K + 1, d), _dev_bf16(W), torch.from_numpy(q).to(DEV),
+                           torch.from_numpy(tokens).to(DEV), torch.from_numpy(u).to(DEV), 1.0, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(ws.count_nonzero().item()) == 0
