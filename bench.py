@@ -429,6 +429,77 @@ def measure_lm_head(torch, dev, steps: int, shape=LM_SHAPE, check: bool = True) 
     return out
 
 
+TREE_WORKLOAD = ("b64_k5_v128256_bf16_topp", "tree16")  # B=64, V=128256 bf16 rows, the 16-node tree
+
+
+def measure_tree(torch, dev, steps: int, check: bool = True) -> dict:
+    """spec_verify_tree on B=64 sequences of a 16-node candidate tree over
+    V=128256 (bf16 logits, dense fp32 drafts; the value distributions of the
+    B=64, V=128256 configuration without its top-p): step time by CUDA-graph
+    replay, algorithmic bytes (every node row once; for every rejection the
+    node's p and q rows; a leaf's draw one more pass over its p row), and
+    parity of sampled sequences against the fp64 oracle."""
+    import synth
+    import speculative_decoding_sampling_gb300 as sv
+    wname, shape = TREE_WORKLOAD
+    w = synth.WORKLOADS[wname].with_(top_p=0.0)
+    logits, q, parent, tokens, u, T = synth.tree_inputs(w, synth.TREE_SHAPES[shape], seed=2026)
+    B, N, V = logits.shape
+
+    def dev_t(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    d = [dev_t(a) for a in (logits, q, parent, tokens, u)]
+    ws = torch.zeros(sv.sv_tree_workspace_bytes(B, N, V), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    res = sv.spec_verify_tree(*d, T, workspace=ws, status=status)
+    torch.cuda.synchronize(dev)
+    out = {k: getattr(res, k).cpu().numpy() for k in ("out_tokens", "out_nodes", "num_emitted", "accept_prob")}
+    tested = (out["accept_prob"] >= 0).sum(1)
+    rejected = tested - (out["num_emitted"] - 1)
+    # the final draw came from a leaf's p when the walk's last node has no children
+    last = np.where(out["num_emitted"] > 1, out["out_nodes"][np.arange(B), np.maximum(out["num_emitted"] - 2, 0)], 0)
+    has_child = np.array([(parent[b] == last[b]).any() for b in range(B)])
+    nbytes = int(B * N * V * 2 + rejected.sum() * V * (2 + 4) + (~has_child).sum() * V * 2)
+    n = max(GRAPH_STEPS, min(steps, 300))
+    gs = torch.cuda.Stream(dev)
+    with torch.cuda.stream(gs):
+        for _ in range(3):
+            sv.spec_verify_tree(*d, T, workspace=ws, status=status, stream=gs)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gs):
+        for _ in range(GRAPH_STEPS):
+            sv.spec_verify_tree(*d, T, workspace=ws, status=status, stream=gs)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(1, n // GRAPH_STEPS)
+    with torch.cuda.stream(gs):
+        e0.record(gs)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(gs)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / (reps * GRAPH_STEPS)
+    peak, _ = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    r = {"workload": f"{wname} rows without top-p, {shape} (N={N})", "B": B, "N": N, "V": V,
+         "step_us": ms * 1e3, "seqs_per_s": B / (ms * 1e-3), "tokens_per_s": float(out["num_emitted"].sum()) /
+         (ms * 1e-3), "mean_emitted": float(out["num_emitted"].mean()), "algorithmic_MB": nbytes / 1e6,
+         "GB_per_s": gbs, "frac_of_measured": gbs / peak, "launches_per_step": 2, "status_bits": int(status.item()),
+         "timing": f"CUDA-graph replay of {GRAPH_STEPS} calls back to back; the logits "
+                   f"({B * N * V * 2 / 1e6:.0f} MB) exceed L2"}
+    if check:
+        import oracle
+        from oracle import parity
+        rep = parity.compare_tree(oracle.load(), logits, q, parent, tokens, u, T, out, seqs=[0, 21, 42, 63])
+        r["parity"] = {"ok": rep.ok(), "summary": rep.summary()}
+    return r
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -501,7 +572,7 @@ def run_gpu(args):
     if copies > 1:
         rig = Rig(torch, w, inp, dev, copies, logits_override=raw)
         for i in range(3 * copies):
-            step(i, stream)
+            step(i % copies, stream)
     launches_per_step = sv.sv_kernel_launches(
         torch.bfloat16 if w.dtype == "bf16" else torch.float32, inp.q is not None, B, K, V) + (1 if filt else 0)
     barrier()
@@ -589,6 +660,7 @@ def run_gpu(args):
             for name in synth.WORKLOADS:
                 workloads[name] = measure_workload(torch, dev, name, min(args.steps, 300), cores)
         lm = measure_lm_head(torch, dev, args.steps) if args.lm_head == "on" else None
+        tree = measure_tree(torch, dev, args.steps) if args.workloads else None
         config = config_of(w, world, filt)
         result = {
             "metric": METRIC,
@@ -637,6 +709,7 @@ def run_gpu(args):
             "parity": parity_note,
             "workloads": workloads,
             "lm_head": lm,
+            "tree": tree,
         }
     if world > 1:
         dist.barrier()

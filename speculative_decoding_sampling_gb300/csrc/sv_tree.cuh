@@ -31,9 +31,9 @@
 
 namespace sv {
 
-constexpr int kTreeThreads = 256;
+constexpr int kTreeThreads = 1024;
 constexpr int kTreeWarps = kTreeThreads / 32;
-constexpr int kTreeChunk = 256;     // ids per warp chunk: 8 per lane
+constexpr int kTreeChunk = 256;     // ids per warp chunk: one group of 8 per lane
 constexpr int kTreeMaxNodes = 256;   // nodes of one tree (the C ABI's SV_MAX_TREE_NODES)
 constexpr int32_t kBadTree = 64;
 
@@ -54,22 +54,67 @@ struct TreeRow {
     const void *z;   // logits row (LT)
     const float *q;  // draft row
     float c, mc, inv_s;
+    bool zvec, qvec; // rows 16-byte aligned: whole groups load as vectors
 };
 
-// The fixed-point weight of id i of a row: p_i (bonus) or max(0, p_i - C q_i).
+// The weights of the 8 ids of group g (ids past V weigh 0): p_i (bonus) or
+// max(0, p_i - C q_i), p_i = exp2(z_i c - mc) / s in fp32.
 template <typename LT>
-__device__ __forceinline__ long long tree_weight(const TreeRow &R, int32_t i, bool resid, float C, int fb)
+__device__ __forceinline__ void tree_group(const TreeRow &R, int32_t g, int32_t V, bool resid, float C, float (&w)[8])
 {
-    const float p = __fmul_rn(term(load_elem<LT>(static_cast<const LT *>(R.z) + i), R.c, R.mc), R.inv_s);
-    if (!resid)
-        return to_fixed(p, fb);
-    const float w = __fmaf_rn(-C, __ldg(R.q + i), p);
-    return w > 0.0f ? to_fixed(w, fb) : 0ll;
+    const int32_t i0 = g * 8;
+    float z[8], q[8];
+    const LT *zr = static_cast<const LT *>(R.z) + i0;
+    if (R.zvec && i0 + 8 <= V) {
+        if constexpr (sizeof(LT) == 2) {
+            const uint4 v = ld_stream_v4(zr);
+            z[0] = bf16_lo(v.x); z[1] = bf16_hi(v.x); z[2] = bf16_lo(v.y); z[3] = bf16_hi(v.y);
+            z[4] = bf16_lo(v.z); z[5] = bf16_hi(v.z); z[6] = bf16_lo(v.w); z[7] = bf16_hi(v.w);
+        } else {
+            const uint4 v0 = ld_stream_v4(zr), v1 = ld_stream_v4(zr + 4);
+            z[0] = __uint_as_float(v0.x); z[1] = __uint_as_float(v0.y); z[2] = __uint_as_float(v0.z);
+            z[3] = __uint_as_float(v0.w); z[4] = __uint_as_float(v1.x); z[5] = __uint_as_float(v1.y);
+            z[6] = __uint_as_float(v1.z); z[7] = __uint_as_float(v1.w);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            z[k] = i0 + k < V ? load_elem<LT>(zr + k) : -INFINITY;
+    }
+    if (resid) {
+        const float *qr = R.q + i0;
+        if (R.qvec && i0 + 8 <= V) {
+            const uint4 v0 = ld_stream_v4(qr), v1 = ld_stream_v4(qr + 4);
+            q[0] = __uint_as_float(v0.x); q[1] = __uint_as_float(v0.y); q[2] = __uint_as_float(v0.z);
+            q[3] = __uint_as_float(v0.w); q[4] = __uint_as_float(v1.x); q[5] = __uint_as_float(v1.y);
+            q[6] = __uint_as_float(v1.z); q[7] = __uint_as_float(v1.w);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                q[k] = i0 + k < V ? __ldg(qr + k) : 0.0f;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float p = __fmul_rn(term(z[k], R.c, R.mc), R.inv_s);
+        w[k] = resid ? fmaxf(__fmaf_rn(-C, q[k], p), 0.0f) : p;
+    }
+}
+
+// A group's mass: its 8 weights added in fp32 in id order, as a fixed-point
+// integer.  The draw re-forms the same sums, so its boundaries agree.
+__device__ __forceinline__ long long tree_group_fixed(const float (&w)[8], int fb)
+{
+    float s = w[0];
+#pragma unroll
+    for (int k = 1; k < 8; ++k)
+        s = __fadd_rn(s, w[k]);
+    return to_fixed(s, fb);
 }
 
 // One pass over the row: per-chunk totals into chunk[] and the row total
-// (returned to every thread).  Warp w takes chunks w, w + 8, ...; lane l the
-// 8 ids 8l .. 8l + 7 of a chunk.
+// (returned to every thread).  Warp w takes chunks w, w + 32, ...; lane l
+// group 32 ch + l of chunk ch.
 template <typename LT>
 __device__ long long tree_pass(const TreeRow &R, int32_t V, bool resid, float C, int fb, long long *chunk,
                                long long *red)
@@ -78,13 +123,9 @@ __device__ long long tree_pass(const TreeRow &R, int32_t V, bool resid, float C,
     const int32_t nch = (V + kTreeChunk - 1) / kTreeChunk;
     long long mine = 0;
     for (int32_t ch = warp; ch < nch; ch += kTreeWarps) {
-        const int32_t i0 = ch * kTreeChunk + lane * 8;
-        long long s = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            if (i0 + k < V)
-                s += tree_weight<LT>(R, i0 + k, resid, C, fb);
-        s = warp_sum_ll(s);
+        float w[8];
+        tree_group<LT>(R, ch * 32 + lane, V, resid, C, w);
+        const long long s = warp_sum_ll(tree_group_fixed(w, fb));
         if (lane == 0)
             chunk[ch] = s;
         mine += s;
@@ -93,7 +134,7 @@ __device__ long long tree_pass(const TreeRow &R, int32_t V, bool resid, float C,
         red[warp] = mine;
     __syncthreads();
     long long tot = 0;
-#pragma unroll
+#pragma unroll 8
     for (int w = 0; w < kTreeWarps; ++w)
         tot += red[w];
     __syncthreads(); // red[] is reused
@@ -109,7 +150,9 @@ struct TreeSel {
 
 // First id whose cumulative weight exceeds t (0 <= t < total), from the
 // chunk totals of the last pass over the same weights; every thread gets
-// it.  If rounding leaves none, the last id of positive weight.
+// it.  Within a group the boundaries are the fixed-point values of its fp32
+// partial sums in id order (the last one is the group's mass).  If rounding
+// leaves no id, the last id of positive weight.
 template <typename LT>
 __device__ int32_t tree_find(const TreeRow &R, int32_t V, bool resid, float C, int fb, long long t,
                              const long long *chunk, long long *red, TreeSel *sel)
@@ -154,15 +197,10 @@ __device__ int32_t tree_find(const TreeRow &R, int32_t V, bool resid, float C, i
     __syncthreads();
     const int32_t ch = sel->chunk;
     if (ch >= 0 && warp == 0) {
-        // the chunk: lane sums of 8 ids, exclusive scan, then the lane's ids
-        const int32_t i0 = ch * kTreeChunk + lane * 8;
-        long long w8[8];
-        long long s = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            w8[k] = i0 + k < V ? tree_weight<LT>(R, i0 + k, resid, C, fb) : 0ll;
-            s += w8[k];
-        }
+        // the chunk: group masses, exclusive scan, then the group's ids
+        float w[8];
+        tree_group<LT>(R, ch * 32 + lane, V, resid, C, w);
+        const long long s = tree_group_fixed(w, fb);
         long long inc2 = s;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -170,15 +208,18 @@ __device__ int32_t tree_find(const TreeRow &R, int32_t V, bool resid, float C, i
             if (lane >= o)
                 inc2 += y;
         }
-        long long acc = sel->base + inc2 - s;
+        const long long g0 = sel->base + inc2 - s;
         int32_t id = -1;
-        if (s > 0 && acc <= t && t < acc + s)
+        if (s > 0 && g0 <= t && t < g0 + s) {
+            float part = w[0];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                acc += w8[k];
-                if (id < 0 && t < acc)
-                    id = i0 + k;
+                if (k > 0)
+                    part = __fadd_rn(part, w[k]);
+                if (id < 0 && t < g0 + to_fixed(part, fb))
+                    id = (ch * 32 + lane) * 8 + k;
             }
+        }
         const unsigned m = __ballot_sync(0xFFFFFFFFu, id >= 0);
         const int32_t first = __shfl_sync(0xFFFFFFFFu, id, m ? __ffs(m) - 1 : 0);
         if (lane == 0)
@@ -189,11 +230,15 @@ __device__ int32_t tree_find(const TreeRow &R, int32_t V, bool resid, float C, i
         __syncthreads();
         if (threadIdx.x == 0) {
             int32_t last = 0;
-            for (int32_t i = V - 1; i >= 0; --i)
-                if (tree_weight<LT>(R, i, resid, C, fb) > 0) {
-                    last = i;
-                    break;
-                }
+            for (int32_t g = (V + 7) / 8 - 1; g >= 0 && last == 0; --g) {
+                float w[8];
+                tree_group<LT>(R, g, V, resid, C, w);
+                for (int k = 7; k >= 0; --k)
+                    if (g * 8 + k < V && w[k] > 0.0f) {
+                        last = g * 8 + k;
+                        break;
+                    }
+            }
             sel->id = last;
         }
         __syncthreads();
@@ -298,6 +343,8 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const Params P, cons
         R.c = c;
         R.mc = mc_of(s_M[v], c);
         R.inv_s = __frcp_rn(s_S[v]);
+        R.zvec = (reinterpret_cast<uintptr_t>(R.z) & 15u) == 0;
+        R.qvec = (reinterpret_cast<uintptr_t>(R.q) & 15u) == 0;
         int32_t nrej = 0, next = -1;
         float C = 1.0f, W = 0.0f; // the residual max(0, p - C q) / W after nrej rejections
         long long Wfix = 0;
