@@ -72,16 +72,16 @@ def algorithmic_bytes(w, num_emitted: np.ndarray) -> dict:
     return {"rows_kernel": rows, "draw_kernels": surv, "total": rows + surv, "rejected": rejected}
 
 
-OWN_KERNEL_FILES = ("sv_filter.cuh", "sv_lmhead.cuh")  # kernels of their own, hashed apart
+OWN_KERNEL_FILES = ("sv_filter.cuh", "sv_lmhead.cuh", "sv_tree.cuh")  # kernels of their own, hashed apart
 
 
 def kernel_source_hash(only: str | None = None) -> str:
     """Hash of device code, with // comments, trailing blanks and empty lines
     removed (they do not change a kernel).  Default: the verification
-    kernels, i.e. every .cuh file but those of the top-k / top-p filter and
-    the LM head (the C ABI's host code in spec_verify.cu is left out).
-    only="sv_lmhead.cuh": that file and the verification kernels it
-    includes."""
+    kernels, i.e. every .cuh file but those of the top-k / top-p filter, the
+    LM head and the tree walk (the C ABI's host code in spec_verify.cu is
+    left out).  only="sv_lmhead.cuh" (or another of those files): that file
+    and the verification kernels it includes."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_sampling_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
@@ -93,15 +93,15 @@ def kernel_source_hash(only: str | None = None) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str, kernel: str):
+def recorded_traffic(workload: str, kernel: str, only: str | None = None):
     """DRAM bytes per launch of `kernel` from the committed ncu summary
-    (profiles/traffic.json), if it was taken on the current kernel source;
-    else None."""
+    (profiles/traffic.json), if it was taken on the current kernel source
+    (kernel_source_hash(only)); else None."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
             d = json.load(fh)
         e = d.get(workload)
-        if e and e.get("source_hash") == kernel_source_hash():
+        if e and e.get("source_hash") == kernel_source_hash(only):
             return e.get("dram_bytes_per_launch", {}).get(kernel)
     except Exception:
         pass
@@ -401,7 +401,9 @@ def measure_lm_head(torch, dev, steps: int, shape=LM_SHAPE, check: bool = True) 
         "context_cublas_plus_spec_verify_us": lib_ms * 1e3,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf_peak, "unit": "TFLOP/s",
                      "frac": achieved / tf_peak, "frac_of_sustained": achieved / tf_sus,
-                     "flops_per_launch": flops, "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops burst)"},
+                     "flops_per_launch": flops, "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops burst)",
+                     "algorithmic_dram_bytes": V * d * 2 + M * d * 2 + M * V * 2,
+                     "traffic": recorded_traffic(f"lm_head_m{M}_v{V}_d{d}", "lm_head_kernel", "sv_lmhead.cuh")},
         "steps": n,
         "status_bits": int(status.item()),
         "timing": f"CUDA-graph replay of {GRAPH_STEPS} calls back to back; W ({V * d * 2 / 1e9:.2f} GB) alone "
@@ -660,7 +662,7 @@ def run_gpu(args):
             for name in synth.WORKLOADS:
                 workloads[name] = measure_workload(torch, dev, name, min(args.steps, 300), cores)
         lm = measure_lm_head(torch, dev, args.steps) if args.lm_head == "on" else None
-        tree = measure_tree(torch, dev, args.steps) if args.workloads else None
+        tree = measure_tree(torch, dev, args.steps) if (args.workloads and args.tree == "on") else None
         config = config_of(w, world, filt)
         result = {
             "metric": METRIC,
@@ -922,9 +924,16 @@ def main():
                     help="the LM-head leg (GEMM and fused step); only: that leg alone (profiling runs)")
     ap.add_argument("--lm-shape", default=",".join(map(str, LM_SHAPE)),
                     help="B,K,V,d of the LM-head leg with --lm-head only (profiling runs)")
+    ap.add_argument("--tree", default="on", choices=["on", "off", "only"],
+                    help="the tree-verification leg; only: that leg alone, without the oracle check (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.tree == "only" and args.impl != "reference":
+        import torch
+        print(json.dumps({"tree": measure_tree(torch, torch.device("cuda", 0), args.steps, check=False)}),
+              flush=True)
+        return
     if args.lm_head == "only" and args.impl != "reference":
         import torch
         dev = torch.device("cuda", 0)
