@@ -346,31 +346,42 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     };
 
     if (warp == 0 && lane == 0) {
+        // stage s, its phase, and the even CTA's "full" barrier of stage 0
+        // (the barriers are consecutive 8-byte words)
+        int s = 0;
+        uint32_t ph = 0;
         int64_t it = 0;
+        const uint32_t fb0 = lm_mapa(smem_addr(&full[0]), 0);
+        const uint32_t sbase = smem_addr(smem);
         for (int64_t t = pair; t < ntiles && !*vstop; t += pairs) {
             const int m0 = static_cast<int>(t % P.MT) * (2 * kLmBM) + static_cast<int>(rank) * kLmBM;
             const int n0 = static_cast<int>(t / P.MT) * kLmBN + static_cast<int>(rank) * (kLmBN / 2);
             int kb = 0;
             for (; kb < nk; ++kb, ++it) {
-                const int s = static_cast<int>(it % kLmStages);
-                if (it >= kLmStages &&
-                    !lm_wait(smem_addr(&empty[s]), static_cast<uint32_t>(((it / kLmStages) & 1) ^ 1), vstop,
-                             P.wait_ns)) {
+                if (it >= kLmStages && !lm_wait(smem_addr(&empty[s]), ph ^ 1u, vstop, P.wait_ns)) {
                     fail();
                     break;
                 }
-                const uint32_t sa = smem_addr(smem + s * kLmStageBytes);
-                const uint32_t fb = lm_mapa(smem_addr(&full[s]), 0);
+                const uint32_t sa = sbase + static_cast<uint32_t>(s * kLmStageBytes);
+                const uint32_t fb = fb0 + static_cast<uint32_t>(s * 8);
                 if (leader)
                     lm_mbar_expect(smem_addr(&full[s]), 2 * kLmStageBytes);
                 lm_tma_2d(sa, &tmA, kb * kLmBK, m0, fb);
                 lm_tma_2d(sa + kLmABytes, &tmB, kb * kLmBK, n0, fb);
+                if (++s == kLmStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
             if (kb < nk)
                 break;
         }
     } else if (warp == 1 && lane == 0 && leader) {
-        int64_t it = 0;
+        // the descriptors of stage 0's A and B tiles; a stage or a K step
+        // only moves the start address (16-byte units, the low field)
+        const uint64_t ad0 = lm_desc(smem_addr(smem)), bd0 = lm_desc(smem_addr(smem + kLmABytes));
+        int s = 0;
+        uint32_t ph = 0;
         int i = 0;
         for (int64_t t = pair; t < ntiles && !*vstop; t += pairs, ++i) {
             const int acc = i & 1;
@@ -382,19 +393,22 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             lm_tc_after();
             const uint32_t tacc = tbase + static_cast<uint32_t>(acc * kLmBN);
             int kb = 0;
-            for (; kb < nk; ++kb, ++it) {
-                const int s = static_cast<int>(it % kLmStages);
-                if (!lm_wait(smem_addr(&full[s]), static_cast<uint32_t>((it / kLmStages) & 1), vstop, P.wait_ns)) {
+            for (; kb < nk; ++kb) {
+                if (!lm_wait(smem_addr(&full[s]), ph, vstop, P.wait_ns)) {
                     fail();
                     break;
                 }
                 lm_tc_after();
-                const uint32_t sa = smem_addr(smem + s * kLmStageBytes);
+                const uint64_t so = static_cast<uint64_t>((s * kLmStageBytes) >> 4);
 #pragma unroll
                 for (int k = 0; k < kLmBK / 16; ++k)
-                    lm_mma(tacc, lm_desc(sa + k * 32), lm_desc(sa + kLmABytes + k * 32), kLmIdesc,
-                           (kb | k) ? 1u : 0u);
+                    lm_mma(tacc, ad0 + so + static_cast<uint64_t>(k * 2), bd0 + so + static_cast<uint64_t>(k * 2),
+                           kLmIdesc, (kb | k) ? 1u : 0u);
                 lm_commit_both(smem_addr(&empty[s])); // both CTAs' stage is free once these MMAs have read it
+                if (++s == kLmStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
             if (kb < nk)
                 break;
