@@ -205,8 +205,14 @@ struct FilterShared {
     unsigned long long dmass[256];
     float redf[kFilterWarps];
     long long redl[kFilterWarps];
-    uint32_t ckey[kCollect]; // a bin's collected ids: keys, then sorted with them
-    int32_t cid[kCollect];
+    union {
+        struct {
+            uint32_t ckey[kCollect]; // a bin's collected ids: keys, then sorted with them
+            int32_t cid[kCollect];
+        };
+        unsigned int wcnt[kFilterWarps][kYBins]; // the binning pass: each warp's own counts
+    };
+    unsigned long long wmass[kFilterWarps][kTopBins]; // and its own top-bin masses
     unsigned int ncol;
     unsigned int kmin, kmax;
     int bad;
@@ -569,6 +575,14 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const FilterP
 
         // 2. coarse bins of y: counts only, and the exact total mass in
         // registers (the last bin's ids have zero mass and are only counted)
+        // each warp counts into its own bins (no contention between warps);
+        // they are added up after the pass
+        unsigned int *wc = S.wcnt[threadIdx.x >> 5];
+        unsigned long long *wm = S.wmass[threadIdx.x >> 5];
+        for (int i = threadIdx.x & 31; i < kYBins; i += 32)
+            wc[i] = 0u;
+        for (int i = threadIdx.x & 31; i < kTopBins; i += 32)
+            wm[i] = 0ull;
         for (int i = threadIdx.x; i < kYBins; i += kFilterThreads) {
             S.cnt[i] = 0u;
             S.mass[i] = 0ull;
@@ -584,16 +598,30 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const FilterP
             const unsigned under = __ballot_sync(am, b == kYBins - 1);
             if (b == kYBins - 1) {
                 if ((threadIdx.x & 31) == __ffs(under) - 1)
-                    atomicAdd(&S.cnt[kYBins - 1], static_cast<unsigned>(__popc(under)));
+                    atomicAdd(&wc[kYBins - 1], static_cast<unsigned>(__popc(under)));
             } else if (b >= 0) {
-                atomicAdd(&S.cnt[b], 1u);
+                atomicAdd(&wc[b], 1u);
                 const long long w = R.w(yv);
                 Stot += w;
                 if (b < kTopBins && w) // the top bins' exact masses: the cuts lie there for most rows
-                    atomicAdd(&S.mass[b], static_cast<unsigned long long>(w));
+                    atomicAdd(&wm[b], static_cast<unsigned long long>(w));
             }
         });
-        Stot = block_sum_l(Stot, S);
+        Stot = block_sum_l(Stot, S); // (its barriers also end every warp's binning)
+        for (int i = threadIdx.x; i < kYBins; i += kFilterThreads) {
+            unsigned int c = 0u;
+#pragma unroll
+            for (int w = 0; w < kFilterWarps; ++w)
+                c += S.wcnt[w][i];
+            S.cnt[i] = c;
+            if (i < kTopBins) {
+                unsigned long long m2 = 0ull;
+#pragma unroll
+                for (int w = 0; w < kFilterWarps; ++w)
+                    m2 += S.wmass[w][i];
+                S.mass[i] = m2;
+            }
+        }
         __syncthreads();
 
         // 3. the cuts.  Exact bin masses are needed only above the cut: for
