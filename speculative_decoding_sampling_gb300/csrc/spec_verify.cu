@@ -724,7 +724,7 @@ sv_status_t spec_verify_tree(const void *logits, sv_dtype_t dtype, const float *
 {
     if (B < 0 || N < 1 || V < 1)
         return SV_EINVAL;
-    if (N > SV_MAX_TREE_NODES || V > SV_MAX_V || B > 0x7FFFFFFFll)
+    if (N > SV_MAX_TREE_NODES || V > SV_MAX_V || B > 0x3FFFFFFFll)
         return SV_EUNSUPPORTED;
     if (dtype != SV_BF16 && dtype != SV_FP32)
         return SV_EINVAL;
@@ -779,21 +779,34 @@ sv_status_t spec_verify_tree(const void *logits, sv_dtype_t dtype, const float *
     A.num_emitted = num_emitted;
     A.accept_prob = accept_prob;
     A.status = status_dev;
+    // one cluster of two CTAs per sequence
     const size_t smem = static_cast<size_t>(ceil_div(V, sv::kTreeChunk)) * sizeof(long long);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = sv::kTreeCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(B * sv::kTreeCtas));
+    cfg.blockDim = dim3(sv::kTreeThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (dtype == SV_BF16) {
         if (smem > 48 * 1024 &&
             cudaFuncSetAttribute(sv::tree_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem)) != cudaSuccess)
             return SV_ECUDA;
-        sv::tree_kernel<uint16_t><<<static_cast<unsigned>(B), sv::kTreeThreads, smem, s>>>(P, A);
+        e = cudaLaunchKernelEx(&cfg, sv::tree_kernel<uint16_t>, P, A);
     } else {
         if (smem > 48 * 1024 &&
             cudaFuncSetAttribute(sv::tree_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem)) != cudaSuccess)
             return SV_ECUDA;
-        sv::tree_kernel<float><<<static_cast<unsigned>(B), sv::kTreeThreads, smem, s>>>(P, A);
+        e = cudaLaunchKernelEx(&cfg, sv::tree_kernel<float>, P, A);
     }
-    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
+    return e == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 
 const char *sv_status_string(sv_status_t status)

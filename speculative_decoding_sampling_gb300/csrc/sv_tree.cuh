@@ -112,24 +112,61 @@ __device__ __forceinline__ long long tree_group_fixed(const float (&w)[8], int f
     return to_fixed(s, fb);
 }
 
-// One pass over the row: per-chunk totals into chunk[] and the row total
-// (returned to every thread).  Warp w takes chunks w, w + 32, ...; lane l
-// group 32 ch + l of chunk ch.
+// A sequence is walked by a cluster of two CTAs (one per SM), which take the
+// same decisions from the same data and split each pass over the row.
+constexpr int kTreeCtas = 2;
+
+__device__ __forceinline__ uint32_t tree_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void tree_cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// A 64-bit store into the same shared-memory location of CTA `rank`.
+__device__ __forceinline__ void tree_st_peer(long long *p, uint32_t rank, long long v)
+{
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(p)), "r"(rank));
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+
+// One pass over the row: per-chunk totals into chunk[] (in both CTAs) and
+// the row total (returned to every thread of both).  This CTA takes the
+// chunks [c0, c1) of its half; warp w of it takes chunks c0 + w, c0 + w + 32,
+// ...; lane l group 32 ch + l of chunk ch.  Its totals are also written into
+// the other CTA's chunk[], between cluster barriers (the first: the other
+// CTA has finished reading the last pass's totals).
 template <typename LT>
 __device__ long long tree_pass(const TreeRow &R, int32_t V, bool resid, float C, int fb, long long *chunk,
                                long long *red)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int32_t nch = (V + kTreeChunk - 1) / kTreeChunk;
-    long long mine = 0;
-    for (int32_t ch = warp; ch < nch; ch += kTreeWarps) {
+    const uint32_t rank = tree_rank(), peer = rank ^ 1u;
+    const int32_t half = (nch + 1) / 2;
+    const int32_t c0 = rank ? half : 0, c1 = rank ? nch : half;
+    tree_cluster_sync();
+    for (int32_t ch = c0 + warp; ch < c1; ch += kTreeWarps) {
         float w[8];
         tree_group<LT>(R, ch * 32 + lane, V, resid, C, w);
         const long long s = warp_sum_ll(tree_group_fixed(w, fb));
-        if (lane == 0)
+        if (lane == 0) {
             chunk[ch] = s;
-        mine += s;
+            tree_st_peer(&chunk[ch], peer, s);
+        }
     }
+    tree_cluster_sync();
+    // the total, from all chunk totals: the same integer sum in both CTAs
+    long long mine = 0;
+    for (int32_t ch = threadIdx.x; ch < nch; ch += kTreeThreads)
+        mine += chunk[ch];
+    mine = warp_sum_ll(mine);
     if (lane == 0)
         red[warp] = mine;
     __syncthreads();
@@ -257,7 +294,8 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const Params P, cons
     __shared__ long long s_red[kTreeWarps];
     __shared__ TreeSel s_sel;
     __shared__ int32_t s_bad, s_flag;
-    const int64_t b = blockIdx.x;
+    const int64_t b = blockIdx.x / kTreeCtas;
+    const bool writer = tree_rank() == 0; // the even CTA writes the outputs
     const int32_t N = A.N, V = static_cast<int32_t>(P.V);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float c = P.c;
@@ -287,12 +325,15 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const Params P, cons
         }
     }
     __syncthreads();
+    tree_cluster_sync(); // both CTAs have read the row pass's partials
     // the row pass's scratch of this sequence goes back to zero once read
     // (the workspace is shared with spec_verify, which expects it zeroed)
-    for (int64_t i = threadIdx.x; i < static_cast<int64_t>(N) * P.PM; i += kTreeThreads)
-        P.row_part[b * N * P.PM + i] = make_float2(0.0f, 0.0f);
-    for (int32_t i = threadIdx.x; i < N; i += kTreeThreads)
-        P.row_side[b * N + i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (writer) {
+        for (int64_t i = threadIdx.x; i < static_cast<int64_t>(N) * P.PM; i += kTreeThreads)
+            P.row_part[b * N * P.PM + i] = make_float2(0.0f, 0.0f);
+        for (int32_t i = threadIdx.x; i < N; i += kTreeThreads)
+            P.row_side[b * N + i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
     // the inputs: u in [0, 1), parents before their nodes, tokens in range
     // with positive draft probability, finite rows
     for (int32_t i = threadIdx.x; i < N; i += kTreeThreads) {
@@ -319,6 +360,8 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const Params P, cons
     __syncthreads();
     const int32_t bad = s_bad;
     if (bad) {
+        if (!writer)
+            return;
         for (int32_t i = threadIdx.x; i < N; i += kTreeThreads) {
             A.out_tokens[b * N + i] = -1;
             if (A.out_nodes) A.out_nodes[b * N + i] = -1;
@@ -330,7 +373,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const Params P, cons
         }
         return;
     }
-    if (A.accept_prob)
+    if (A.accept_prob && writer)
         for (int32_t i = threadIdx.x; i < N; i += kTreeThreads)
             A.accept_prob[b * N + i] = -1.0f;
 
@@ -358,7 +401,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const Params P, cons
                 const float qx = __ldg(R.q + x);
                 const float rx = nrej == 0 ? px : __fdiv_rn(fmaxf(__fmaf_rn(-C, qx, px), 0.0f), W);
                 const float a = fminf(1.0f, __fdiv_rn(rx, qx));
-                if (A.accept_prob)
+                if (A.accept_prob && writer)
                     A.accept_prob[b * N + ch] = a;
                 s_flag = s_u[ch] < a ? 1 : 0;
             }
@@ -380,7 +423,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const Params P, cons
             }
         }
         if (next >= 0) {
-            if (threadIdx.x == 0) {
+            if (threadIdx.x == 0 && writer) {
                 A.out_tokens[b * N + len] = s_tok[next];
                 if (A.out_nodes) A.out_nodes[b * N + len] = next;
             }
@@ -400,6 +443,8 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const Params P, cons
         y = tree_find<LT>(R, V, resid, C, fb, t, tree_chunk, s_red, &s_sel);
         break;
     }
+    if (!writer)
+        return;
     if (threadIdx.x == 0) {
         A.out_tokens[b * N + len] = y;
         A.num_emitted[b] = len + 1;
