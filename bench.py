@@ -308,12 +308,15 @@ def measure_workload(torch, dev, name: str, steps: int, cpu_threads: int) -> dic
     for i in range(3 * len(rig.copies)):
         rig.call(i % len(rig.copies), stream)
     ms = time_steps(torch, rig, steps, rig.call, flushed, dev)
+    # the small steps are also timed L2-warm (graph replay, no flush), as a second figure
+    warm_ms = time_steps(torch, rig, steps, rig.call, False, dev) if flushed else None
     orc = oracle.load()
     rep = parity.compare(orc, inp.logits, inp.q, inp.tokens, inp.u, inp.T, rig.host_outputs(),
                          oracle_res=orc.verify(inp.logits, inp.q, inp.tokens, inp.u, inp.T, nthreads=cpu_threads))
     peak, _ = peaks()
     gbs = touched / (ms * 1e-3) / 1e9
-    return {"step_us": ms * 1e3, "algorithmic_MB": touched / 1e6, "GB_per_s": gbs,
+    return {"step_us": ms * 1e3, "l2_warm_step_us": None if warm_ms is None else warm_ms * 1e3,
+            "algorithmic_MB": touched / 1e6, "GB_per_s": gbs,
             "frac_of_measured": gbs / peak, "frac_of_8TBs": gbs / NOMINAL_HBM_GBS,
             "seqs_per_s": w.B / (ms * 1e-3), "launches_per_step": rig.sv.sv_kernel_launches(
                 torch.bfloat16 if w.dtype == "bf16" else torch.float32, inp.q is not None, w.B, w.K, w.V),
@@ -803,6 +806,25 @@ def run_e2e(torch, w, inp, rig, raw, filt, top_p32, d_kept, dev, args, world):
                    "copied host->device alone"}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the CPU-baseline record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
 def cpu_baseline_and_check(w, inp, out, seconds, top_p=None, filtered=None, raw_logits=None):
     """Time the oracle as it stands on this host's cores over the whole batch
     (repeated until `seconds` elapse) and check the GPU outputs against it.
@@ -847,6 +869,7 @@ def cpu_baseline_and_check(w, inp, out, seconds, top_p=None, filtered=None, raw_
             ref = None
     rep = parity.compare(orc, logits, inp.q, inp.tokens, inp.u, inp.T, cand, oracle_res=ref)
     cpu = {"value": passes * inp.B / el, "unit": "seqs/s", "cores": cores, "kind": "oracle",
+           "cpu_model": cpu_model(),
            "sample": f"all {inp.B} sequences of the workload, {passes} passes, {el:.1f} s wall"
                      + (" (top-p filter included)" if top_p is not None else ""),
            "single_thread": {"value": passes1 * inp.B / el1, "unit": "seqs/s", "cores": 1,
@@ -894,7 +917,7 @@ def run_reference(args):
         "dtype": "f64", "data": "synthetic",
         "config": config_of(w, world, bool(args.filter_top_p)),
         "cpu_baseline": {"value": value, "unit": "seqs/s", "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "cpu_model": cpu_model(), "sample": sample},
         "e2e": {"value": value, "unit": "seqs/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
