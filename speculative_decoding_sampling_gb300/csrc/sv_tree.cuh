@@ -291,6 +291,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const Params P, cons
     extern __shared__ long long tree_chunk[]; // [ceil(V / 256)] chunk totals of the last pass
     __shared__ int32_t s_par[kTreeMaxNodes], s_tok[kTreeMaxNodes];
     __shared__ float s_u[kTreeMaxNodes], s_M[kTreeMaxNodes], s_S[kTreeMaxNodes];
+    __shared__ float s_zx[kTreeMaxNodes], s_qx[kTreeMaxNodes]; // node i's token under its parent's rows
     __shared__ long long s_red[kTreeWarps];
     __shared__ TreeSel s_sel;
     __shared__ int32_t s_bad, s_flag;
@@ -349,7 +350,10 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const Params P, cons
             } else if (x < 0 || x >= V) {
                 bad |= kBadToken;
             } else {
+                // the child test's two values, gathered here for every node at once
                 const float qx = __ldg(A.q + (b * N + pa) * static_cast<int64_t>(V) + x);
+                s_qx[i] = qx;
+                s_zx[i] = load_elem<LT>(static_cast<const LT *>(P.logits) + (b * N + pa) * static_cast<int64_t>(V) + x);
                 if (!(qx > 0.0f && isfinite(qx)))
                     bad |= kBadQ;
             }
@@ -396,9 +400,8 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const Params P, cons
             if (s_par[ch] != v)
                 continue;
             if (threadIdx.x == 0) {
-                const int32_t x = s_tok[ch];
-                const float px = __fmul_rn(term(load_elem<LT>(static_cast<const LT *>(R.z) + x), c, R.mc), R.inv_s);
-                const float qx = __ldg(R.q + x);
+                const float px = __fmul_rn(term(s_zx[ch], c, R.mc), R.inv_s);
+                const float qx = s_qx[ch];
                 const float rx = nrej == 0 ? px : __fdiv_rn(fmaxf(__fmaf_rn(-C, qx, px), 0.0f), W);
                 const float a = fminf(1.0f, __fdiv_rn(rx, qx));
                 if (A.accept_prob && writer)
