@@ -102,3 +102,32 @@ def test_tree_returns_workspace_to_zero():
     sv.spec_verify_tree(_dev(logits), _dev(q), _dev(parent), _dev(tokens), _dev(u), T, workspace=ws)
     torch.cuda.synchronize()
     assert int(ws.count_nonzero().item()) == 0
+
+
+@pytest.mark.parametrize("N,V,seed", [(256, 500, 1), (40, 20000, 2), (97, 4097, 3)])
+def test_tree_random_topologies(orc, N, V, seed):
+    """Random trees (each node's parent drawn uniformly from the nodes before
+    it), up to the largest tree a call takes (SV_MAX_TREE_NODES = 256)."""
+    rng = np.random.default_rng(seed)
+    parent = [-1] + [int(rng.integers(0, i)) for i in range(1, N)]
+    w = synth.WORKLOADS["b8_k4_v32000_bf16"].with_(B=12, V=V)
+    logits, q, par, tokens, u, T = synth.tree_inputs(w, parent, seed=seed)
+    cand = _run(logits, q, par, tokens, u, T)
+    assert cand["status"] == 0
+    rep = parity.compare_tree(orc, logits, q, par, tokens, u, T, cand)
+    assert rep.ok(), rep.summary()
+    # the path follows parent links from the root
+    for b in range(12):
+        n = int(cand["num_emitted"][b]) - 1
+        prev = 0
+        for k in range(n):
+            node = int(cand["out_nodes"][b, k])
+            assert par[b, node] == prev
+            prev = node
+
+
+def test_tree_too_many_nodes_is_refused():
+    w = synth.WORKLOADS["b8_k4_v32000_bf16"].with_(B=2, V=100)
+    logits, q, par, tokens, u, T = synth.tree_inputs(w, [-1] + [0] * 256, seed=1)
+    with pytest.raises(sv.SpecVerifyError):
+        _run(logits, q, par, tokens, u, T)
