@@ -335,8 +335,9 @@ sv_status_t spec_verify_lm_head(const void *hidden, const void *lm_head,
  * into *status_dev (optional); SV_DEGENERATE_RESIDUAL as for spec_verify.
  * The workspace (sv_tree_workspace_bytes(B, N, V) bytes, 256-byte aligned)
  * follows spec_verify's rule: zero-filled before its first use, returned to
- * zero by every completed call, so one workspace serves both.  Two launches on `stream` (the row pass over all B*N
- * rows, then one CTA per sequence for the walk); allocates nothing.
+ * zero by every completed call, so one workspace serves both.  Two launches
+ * on `stream` (the row pass over all B*N rows, then a cluster of two CTAs per
+ * sequence for the walk); allocates nothing.  B <= 2^30.
  * Returns SV_EINVAL / SV_EUNSUPPORTED on bad arguments (nothing launched)
  * and SV_ECUDA when a launch fails. */
 size_t sv_tree_workspace_bytes(int64_t B, int32_t N, int32_t V);
