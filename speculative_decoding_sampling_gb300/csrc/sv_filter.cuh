@@ -589,16 +589,13 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const FilterP
         }
         __syncthreads();
         long long Stot = 0;
+        unsigned int nlast = 0; // the last bin (zero mass) is the crowded one: counted in a register
         filter_visit<LT>(row, V, P.vec, [&](int32_t, uint32_t bits) {
             const bool fin = E::finite(bits);
             const float yv = fin ? R.y(E::value(bits)) : 0.0f;
             const int b = fin ? R.bin(yv) : -1;
-            // the last bin (zero mass) is the crowded one: one add per warp
-            const unsigned am = __activemask();
-            const unsigned under = __ballot_sync(am, b == kYBins - 1);
             if (b == kYBins - 1) {
-                if ((threadIdx.x & 31) == __ffs(under) - 1)
-                    atomicAdd(&wc[kYBins - 1], static_cast<unsigned>(__popc(under)));
+                ++nlast;
             } else if (b >= 0) {
                 atomicAdd(&wc[b], 1u);
                 const long long w = R.w(yv);
@@ -607,6 +604,8 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const FilterP
                     atomicAdd(&wm[b], static_cast<unsigned long long>(w));
             }
         });
+        if (nlast)
+            atomicAdd(&wc[kYBins - 1], nlast);
         Stot = block_sum_l(Stot, S); // (its barriers also end every warp's binning)
         for (int i = threadIdx.x; i < kYBins; i += kFilterThreads) {
             unsigned int c = 0u;
