@@ -136,24 +136,6 @@ __device__ __forceinline__ void tree_st_peer(long long *p, uint32_t rank, long l
     asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
 }
 
-// Ask L2 for the bytes [p, p + n) that lie in whole 16-byte units (the
-// bulk prefetch's granule), cut into one piece per lane of the calling warp.
-// Fire and forget: nothing waits for it, and it never reaches outside the
-// range.
-__device__ __forceinline__ void tree_prefetch(const void *p, int64_t n, int lane)
-{
-    const uintptr_t a = (reinterpret_cast<uintptr_t>(p) + 15u) & ~uintptr_t{15};
-    const uintptr_t e = (reinterpret_cast<uintptr_t>(p) + static_cast<uintptr_t>(n)) & ~uintptr_t{15};
-    if (e <= a)
-        return;
-    const uintptr_t piece = (((e - a + 31u) / 32u) + 15u) & ~uintptr_t{15};
-    const uintptr_t b0 = a + static_cast<uintptr_t>(lane) * piece;
-    const uintptr_t b1 = b0 + piece < e ? b0 + piece : e;
-    if (b0 < b1)
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(b0), "r"(static_cast<uint32_t>(b1 - b0))
-                     : "memory");
-}
-
 // One pass over the row: per-chunk totals into chunk[] (in both CTAs) and
 // the row total (returned to every thread of both).  This CTA takes the
 // chunks [c0, c1) of its half; warp w of it takes chunks c0 + w, c0 + w + 32,
@@ -174,9 +156,9 @@ __device__ long long tree_pass(const TreeRow &R, int32_t V, bool resid, float C,
         // copy bandwidth, so the warps' group loads below find it there
         const int64_t i0 = static_cast<int64_t>(c0) * kTreeChunk;
         const int64_t i1 = min(static_cast<int64_t>(c1) * kTreeChunk, static_cast<int64_t>(V));
-        tree_prefetch(static_cast<const LT *>(R.z) + i0, (i1 - i0) * static_cast<int64_t>(sizeof(LT)), lane);
+        prefetch_l2_lanes(static_cast<const LT *>(R.z) + i0, (i1 - i0) * static_cast<int64_t>(sizeof(LT)), lane);
         if (resid)
-            tree_prefetch(R.q + i0, (i1 - i0) * static_cast<int64_t>(sizeof(float)), lane);
+            prefetch_l2_lanes(R.q + i0, (i1 - i0) * static_cast<int64_t>(sizeof(float)), lane);
     }
     tree_cluster_sync();
     for (int32_t ch = c0 + warp; ch < c1; ch += kTreeWarps) {
