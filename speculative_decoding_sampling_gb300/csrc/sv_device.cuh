@@ -268,40 +268,6 @@ __device__ __forceinline__ int64_t divi(int64_t a, int64_t b)
     return a < 0x80000000ll ? static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b)) : a / b;
 }
 
-// ------------------------------------------------------ L2 prefetch
-//
-// Bulk prefetches into L2 (cp.async.bulk.prefetch.L2): fire and forget,
-// nothing waits for them.  Only the whole 16-byte units inside [p, p + n)
-// are requested (the instruction's granule), so a prefetch never reaches
-// outside the range it is given.
-
-__device__ __forceinline__ void prefetch_l2_units(uintptr_t a, uintptr_t e)
-{
-    if (a < e)
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(static_cast<uint32_t>(e - a))
-                     : "memory");
-}
-
-// [p, p + n) in one request (n < 2^32).
-__device__ __forceinline__ void prefetch_l2(const void *p, int64_t n)
-{
-    const uintptr_t a = (reinterpret_cast<uintptr_t>(p) + 15u) & ~uintptr_t{15};
-    const uintptr_t e = (reinterpret_cast<uintptr_t>(p) + static_cast<uintptr_t>(n)) & ~uintptr_t{15};
-    prefetch_l2_units(a, e);
-}
-
-// [p, p + n) cut into one request per lane of the calling warp.
-__device__ __forceinline__ void prefetch_l2_lanes(const void *p, int64_t n, int lane)
-{
-    const uintptr_t a = (reinterpret_cast<uintptr_t>(p) + 15u) & ~uintptr_t{15};
-    const uintptr_t e = (reinterpret_cast<uintptr_t>(p) + static_cast<uintptr_t>(n)) & ~uintptr_t{15};
-    if (e <= a)
-        return;
-    const uintptr_t piece = (((e - a + 31u) / 32u) + 15u) & ~uintptr_t{15};
-    const uintptr_t b0 = a + static_cast<uintptr_t>(lane) * piece;
-    prefetch_l2_units(b0, b0 + piece < e ? b0 + piece : e);
-}
-
 // ------------------------------------------------------ flat logits view
 //
 // The B*(K+1) rows of V ids are one array of R*V elements.  From the first

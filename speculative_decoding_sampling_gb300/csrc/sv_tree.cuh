@@ -136,6 +136,29 @@ __device__ __forceinline__ void tree_st_peer(long long *p, uint32_t rank, long l
     asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
 }
 
+// Bulk prefetches into L2 (cp.async.bulk.prefetch.L2): fire and forget,
+// nothing waits for them.  Only the whole 16-byte units inside [p, p + n)
+// are requested (the instruction's granule), so a prefetch never reaches
+// outside the range it is given.
+__device__ __forceinline__ void prefetch_l2_units(uintptr_t a, uintptr_t e)
+{
+    if (a < e)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(static_cast<uint32_t>(e - a))
+                     : "memory");
+}
+
+// [p, p + n) cut into one request per lane of the calling warp.
+__device__ __forceinline__ void prefetch_l2_lanes(const void *p, int64_t n, int lane)
+{
+    const uintptr_t a = (reinterpret_cast<uintptr_t>(p) + 15u) & ~uintptr_t{15};
+    const uintptr_t e = (reinterpret_cast<uintptr_t>(p) + static_cast<uintptr_t>(n)) & ~uintptr_t{15};
+    if (e <= a)
+        return;
+    const uintptr_t piece = (((e - a + 31u) / 32u) + 15u) & ~uintptr_t{15};
+    const uintptr_t b0 = a + static_cast<uintptr_t>(lane) * piece;
+    prefetch_l2_units(b0, b0 + piece < e ? b0 + piece : e);
+}
+
 // One pass over the row: per-chunk totals into chunk[] (in both CTAs) and
 // the row total (returned to every thread of both).  This CTA takes the
 // chunks [c0, c1) of its half; warp w of it takes chunks c0 + w, c0 + w + 32,
