@@ -101,6 +101,59 @@ __device__ __forceinline__ void tree_group(const TreeRow &R, int32_t g, int32_t 
     }
 }
 
+// The raw bits of group g of a 16-bit logits row and of its draft row (ids
+// past V: -inf and 0), loaded before any is used, so a warp can have two
+// groups in flight.  tree_raw_weights turns them into the weights
+// tree_group gives, with the same arithmetic.
+struct TreeRaw {
+    uint4 z;      // 8 logits (bf16 bits)
+    uint4 q0, q1; // 8 draft probabilities (fp32 bits), resid only
+};
+
+__device__ __forceinline__ TreeRaw tree_raw_load(const TreeRow &R, int32_t g, int32_t V, bool resid)
+{
+    TreeRaw t;
+    const int32_t i0 = g * 8;
+    const unsigned short *zr = static_cast<const unsigned short *>(R.z) + i0;
+    if (R.zvec && i0 + 8 <= V) {
+        t.z = ld_stream_v4(zr);
+    } else {
+        uint32_t h[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            h[k] = i0 + k < V ? zr[k] : 0xFF80u;
+        t.z = make_uint4(h[0] | h[1] << 16, h[2] | h[3] << 16, h[4] | h[5] << 16, h[6] | h[7] << 16);
+    }
+    t.q0 = t.q1 = make_uint4(0u, 0u, 0u, 0u);
+    if (resid) {
+        const float *qr = R.q + i0;
+        if (R.qvec && i0 + 8 <= V) {
+            t.q0 = ld_stream_v4(qr);
+            t.q1 = ld_stream_v4(qr + 4);
+        } else {
+            uint32_t u[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                u[k] = i0 + k < V ? __float_as_uint(__ldg(qr + k)) : 0u;
+            t.q0 = make_uint4(u[0], u[1], u[2], u[3]);
+            t.q1 = make_uint4(u[4], u[5], u[6], u[7]);
+        }
+    }
+    return t;
+}
+
+__device__ __forceinline__ void tree_raw_weights(const TreeRaw &t, const TreeRow &R, bool resid, float C, float (&w)[8])
+{
+    const float z[8] = {bf16_lo(t.z.x), bf16_hi(t.z.x), bf16_lo(t.z.y), bf16_hi(t.z.y),
+                        bf16_lo(t.z.z), bf16_hi(t.z.z), bf16_lo(t.z.w), bf16_hi(t.z.w)};
+    const uint32_t qb[8] = {t.q0.x, t.q0.y, t.q0.z, t.q0.w, t.q1.x, t.q1.y, t.q1.z, t.q1.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float p = __fmul_rn(term(z[k], R.c, R.mc), R.inv_s);
+        w[k] = resid ? fmaxf(__fmaf_rn(-C, __uint_as_float(qb[k]), p), 0.0f) : p;
+    }
+}
+
 // A group's mass: its 8 weights added in fp32 in id order, as a fixed-point
 // integer.  The draw re-forms the same sums, so its boundaries agree.
 __device__ __forceinline__ long long tree_group_fixed(const float (&w)[8], int fb)
@@ -184,13 +237,34 @@ __device__ long long tree_pass(const TreeRow &R, int32_t V, bool resid, float C,
             prefetch_l2_lanes(R.q + i0, (i1 - i0) * static_cast<int64_t>(sizeof(float)), lane);
     }
     tree_cluster_sync();
-    for (int32_t ch = c0 + warp; ch < c1; ch += kTreeWarps) {
-        float w[8];
-        tree_group<LT>(R, ch * 32 + lane, V, resid, C, w);
+    auto publish = [&](int32_t ch, const float (&w)[8]) {
         const long long s = warp_sum_ll(tree_group_fixed(w, fb));
         if (lane == 0) {
             chunk[ch] = s;
             tree_st_peer(&chunk[ch], peer, s);
+        }
+    };
+    if constexpr (sizeof(LT) == 2) {
+        // two chunks a warp: both groups' loads issued before either is used
+        for (int32_t ch = c0 + warp; ch < c1; ch += 2 * kTreeWarps) {
+            const int32_t ch2 = ch + kTreeWarps;
+            const TreeRaw t1 = tree_raw_load(R, ch * 32 + lane, V, resid);
+            TreeRaw t2;
+            if (ch2 < c1)
+                t2 = tree_raw_load(R, ch2 * 32 + lane, V, resid);
+            float w[8];
+            tree_raw_weights(t1, R, resid, C, w);
+            publish(ch, w);
+            if (ch2 < c1) {
+                tree_raw_weights(t2, R, resid, C, w);
+                publish(ch2, w);
+            }
+        }
+    } else {
+        for (int32_t ch = c0 + warp; ch < c1; ch += kTreeWarps) {
+            float w[8];
+            tree_group<LT>(R, ch * 32 + lane, V, resid, C, w);
+            publish(ch, w);
         }
     }
     tree_cluster_sync();
