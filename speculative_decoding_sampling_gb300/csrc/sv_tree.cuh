@@ -238,7 +238,9 @@ __device__ long long tree_pass(const TreeRow &R, int32_t V, bool resid, float C,
     }
     tree_cluster_sync();
     auto publish = [&](int32_t ch, const float (&w)[8]) {
-        const long long s = warp_sum_ll(tree_group_fixed(w, fb));
+        // a chunk's total: 256 masses of at most 2^fb each (fb <= 40), so
+        // below 2^48, and non-negative
+        const long long s = static_cast<long long>(warp_sum_u64(static_cast<unsigned long long>(tree_group_fixed(w, fb))));
         if (lane == 0) {
             chunk[ch] = s;
             tree_st_peer(&chunk[ch], peer, s);
