@@ -21,8 +21,8 @@
 // leaf it is drawn from p_v with u[0] (inverse CDF in id order).
 //
 // The row pass (rows_kernel over all B*N rows) supplies each row's
-// (max, normaliser) partials; this kernel, one CTA per sequence, merges
-// them, checks the inputs and walks the tree.  Masses in the passes are
+// (max, normaliser) partials; this kernel, a cluster of two CTAs per
+// sequence, merges them, checks the inputs and walks the tree.  Masses in the passes are
 // exact integer multiples of 2^-fix_bits (to_fixed), so sums are
 // order-independent and the draw's boundaries agree with its totals.
 #pragma once
