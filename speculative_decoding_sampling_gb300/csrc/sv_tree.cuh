@@ -215,18 +215,23 @@ __device__ __forceinline__ void prefetch_l2_lanes(const void *p, int64_t n, int 
 // One pass over the row: per-chunk totals into chunk[] (in both CTAs) and
 // the row total (returned to every thread of both).  This CTA takes the
 // chunks [c0, c1) of its half; warp w of it takes chunks c0 + w, c0 + w + 32,
-// ...; lane l group 32 ch + l of chunk ch.  Its totals are also written into
-// the other CTA's chunk[], between cluster barriers (the first: the other
-// CTA has finished reading the last pass's totals).
+// ...; lane l group 32 ch + l of chunk ch.  Its chunk totals are also
+// written into the other CTA's chunk[], and its half of the row total into
+// slot npass mod 2 of both CTAs' half[], all before the one cluster barrier
+// that ends the pass.  No barrier is needed before the writes: the two CTAs
+// take the same decisions, nothing reads chunk[] between passes (only the
+// final draw, after the last pass), and a CTA can reuse a half[] slot only
+// after the other has passed the next pass's barrier, that is, after it has
+// read the slot.
 template <typename LT>
 __device__ long long tree_pass(const TreeRow &R, int32_t V, bool resid, float C, int fb, long long *chunk,
-                               long long *red)
+                               long long *red, long long (*half)[kTreeCtas], int &npass)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int32_t nch = (V + kTreeChunk - 1) / kTreeChunk;
     const uint32_t rank = tree_rank(), peer = rank ^ 1u;
-    const int32_t half = (nch + 1) / 2;
-    const int32_t c0 = rank ? half : 0, c1 = rank ? nch : half;
+    const int32_t halfc = (nch + 1) / 2;
+    const int32_t c0 = rank ? halfc : 0, c1 = rank ? nch : halfc;
     if (warp == 0 && c0 < c1) {
         // this CTA's half of the row (and of the draft row) into L2 at the
         // copy bandwidth, so the warps' group loads below find it there
@@ -236,7 +241,7 @@ __device__ long long tree_pass(const TreeRow &R, int32_t V, bool resid, float C,
         if (resid)
             prefetch_l2_lanes(R.q + i0, (i1 - i0) * static_cast<int64_t>(sizeof(float)), lane);
     }
-    tree_cluster_sync();
+    long long wsum = 0; // this warp's chunk totals (the same in every lane)
     auto publish = [&](int32_t ch, const float (&w)[8]) {
         // a chunk's total: 256 masses of at most 2^fb each (fb <= 40), so
         // below 2^48, and non-negative
@@ -245,6 +250,7 @@ __device__ long long tree_pass(const TreeRow &R, int32_t V, bool resid, float C,
             chunk[ch] = s;
             tree_st_peer(&chunk[ch], peer, s);
         }
+        wsum += s;
     };
     if constexpr (sizeof(LT) == 2) {
         // two chunks a warp: both groups' loads issued before either is used
@@ -269,21 +275,22 @@ __device__ long long tree_pass(const TreeRow &R, int32_t V, bool resid, float C,
             publish(ch, w);
         }
     }
-    tree_cluster_sync();
-    // the total, from all chunk totals: the same integer sum in both CTAs
-    long long mine = 0;
-    for (int32_t ch = threadIdx.x; ch < nch; ch += kTreeThreads)
-        mine += chunk[ch];
-    mine = warp_sum_ll(mine);
+    // this CTA's half of the total, into both CTAs' slot of this pass
     if (lane == 0)
-        red[warp] = mine;
+        red[warp] = wsum;
     __syncthreads();
-    long long tot = 0;
+    const int slot = npass & 1;
+    ++npass;
+    if (threadIdx.x == 0) {
+        long long h = 0;
 #pragma unroll 8
-    for (int w = 0; w < kTreeWarps; ++w)
-        tot += red[w];
-    __syncthreads(); // red[] is reused
-    return tot;
+        for (int w = 0; w < kTreeWarps; ++w)
+            h += red[w];
+        half[slot][rank] = h;
+        tree_st_peer(&half[slot][rank], peer, h);
+    }
+    tree_cluster_sync();
+    return half[slot][0] + half[slot][1];
 }
 
 // Hand-off slots of tree_find (shared memory).
@@ -401,8 +408,10 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const Params P, cons
     __shared__ float s_u[kTreeMaxNodes], s_M[kTreeMaxNodes], s_S[kTreeMaxNodes];
     __shared__ float s_zx[kTreeMaxNodes], s_qx[kTreeMaxNodes]; // node i's token under its parent's rows
     __shared__ long long s_red[kTreeWarps];
+    __shared__ long long s_half[2][kTreeCtas]; // the passes' half totals, by pass parity and CTA
+    int npass = 0;
     __shared__ TreeSel s_sel;
-    __shared__ int32_t s_bad, s_flag;
+    __shared__ int32_t s_bad;
     const int64_t b = blockIdx.x / kTreeCtas;
     const bool writer = tree_rank() == 0; // the even CTA writes the outputs
     const int32_t N = A.N, V = static_cast<int32_t>(P.V);
@@ -507,18 +516,16 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const Params P, cons
         for (int32_t ch = v + 1; ch < N; ++ch) {
             if (s_par[ch] != v)
                 continue;
-            if (threadIdx.x == 0) {
-                const float px = __fmul_rn(term(s_zx[ch], c, R.mc), R.inv_s);
-                const float qx = s_qx[ch];
-                const float rx = nrej == 0 ? px : __fdiv_rn(fmaxf(__fmaf_rn(-C, qx, px), 0.0f), W);
-                const float a = fminf(1.0f, __fdiv_rn(rx, qx));
-                if (A.accept_prob && writer)
-                    A.accept_prob[b * N + ch] = a;
-                s_flag = s_u[ch] < a ? 1 : 0;
-            }
-            __syncthreads();
-            const bool acc = s_flag != 0;
-            __syncthreads();
+            // every thread takes the same decision from the same values (C
+            // and W come from the pass totals every thread holds), so none
+            // has to wait for another's
+            const float px = __fmul_rn(term(s_zx[ch], c, R.mc), R.inv_s);
+            const float qx = s_qx[ch];
+            const float rx = nrej == 0 ? px : __fdiv_rn(fmaxf(__fmaf_rn(-C, qx, px), 0.0f), W);
+            const float a = fminf(1.0f, __fdiv_rn(rx, qx));
+            if (threadIdx.x == 0 && A.accept_prob && writer)
+                A.accept_prob[b * N + ch] = a;
+            const bool acc = s_u[ch] < a;
             if (acc) {
                 next = ch;
                 break;
@@ -526,7 +533,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const Params P, cons
             // rejected: the next residual's constant and normaliser
             C = nrej == 0 ? 1.0f : __fadd_rn(C, W);
             ++nrej;
-            Wfix = tree_pass<LT>(R, V, true, C, fb, tree_chunk, s_red);
+            Wfix = tree_pass<LT>(R, V, true, C, fb, tree_chunk, s_red, s_half, npass);
             W = ldexpf(static_cast<float>(Wfix), -fb);
             if (Wfix <= 0) {
                 degenerate = true;
@@ -547,7 +554,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const Params P, cons
         const bool resid = nrej > 0 && !degenerate;
         long long tot = Wfix;
         if (!resid)
-            tot = tree_pass<LT>(R, V, false, 0.0f, fb, tree_chunk, s_red);
+            tot = tree_pass<LT>(R, V, false, 0.0f, fb, tree_chunk, s_red, s_half, npass);
         if (degenerate)
             status |= kDegenerate;
         const long long t = mul_floor(s_u[0], tot);
