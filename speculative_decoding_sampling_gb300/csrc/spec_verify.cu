@@ -781,18 +781,22 @@ sv_status_t spec_verify_tree(const void *logits, sv_dtype_t dtype, const float *
     A.status = status_dev;
     // one cluster of two CTAs per sequence
     const size_t smem = static_cast<size_t>(ceil_div(V, sv::kTreeChunk)) * sizeof(long long);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = sv::kTreeCtas;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // programmatic dependent launch: the walk checks its inputs while the row
+    // pass drains and waits in griddepcontrol.wait before reading its partials
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(B * sv::kTreeCtas));
     cfg.blockDim = dim3(sv::kTreeThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (dtype == SV_BF16) {
         if (smem > 48 * 1024 &&
             cudaFuncSetAttribute(sv::tree_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -425,6 +425,34 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const Params P, cons
         s_tok[i] = A.tokens[b * N + i];
         s_u[i] = A.u[b * N + i];
     }
+    __syncthreads();
+    // the inputs: u in [0, 1), parents before their nodes, tokens in range
+    // with positive draft probability; and the child tests' two values,
+    // gathered for every node at once.  None of this reads what the row pass
+    // writes, so it runs while the row pass drains (programmatic dependent
+    // launch).
+    for (int32_t i = threadIdx.x; i < N; i += kTreeThreads) {
+        int32_t bad = 0;
+        if (!(s_u[i] >= 0.0f && s_u[i] < 1.0f))
+            bad |= kBadU;
+        if (i >= 1) {
+            const int32_t pa = s_par[i], x = s_tok[i];
+            if (pa < 0 || pa >= i) {
+                bad |= kBadTree;
+            } else if (x < 0 || x >= V) {
+                bad |= kBadToken;
+            } else {
+                const float qx = __ldg(A.q + (b * N + pa) * static_cast<int64_t>(V) + x);
+                s_qx[i] = qx;
+                s_zx[i] = load_elem<LT>(static_cast<const LT *>(P.logits) + (b * N + pa) * static_cast<int64_t>(V) + x);
+                if (!(qx > 0.0f && isfinite(qx)))
+                    bad |= kBadQ;
+            }
+        }
+        if (bad)
+            atomicOr(&s_bad, bad);
+    }
+    pdl_wait_primary(); // the row pass has completed: its partials are all written
     // each row's (max, normaliser): the merge of its row-pass partials
     for (int32_t i = warp; i < N; i += kTreeWarps) {
         const int64_t r = b * N + i;
@@ -440,6 +468,8 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const Params P, cons
         if (lane == 0) {
             s_M[i] = M;
             s_S[i] = S;
+            if (!(isfinite(M) && isfinite(S)))
+                atomicOr(&s_bad, kBadRow);
         }
     }
     __syncthreads();
@@ -451,32 +481,6 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const Params P, cons
             P.row_part[b * N * P.PM + i] = make_float2(0.0f, 0.0f);
         for (int32_t i = threadIdx.x; i < N; i += kTreeThreads)
             P.row_side[b * N + i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    }
-    // the inputs: u in [0, 1), parents before their nodes, tokens in range
-    // with positive draft probability, finite rows
-    for (int32_t i = threadIdx.x; i < N; i += kTreeThreads) {
-        int32_t bad = 0;
-        if (!(s_u[i] >= 0.0f && s_u[i] < 1.0f))
-            bad |= kBadU;
-        if (!(isfinite(s_M[i]) && isfinite(s_S[i])))
-            bad |= kBadRow;
-        if (i >= 1) {
-            const int32_t pa = s_par[i], x = s_tok[i];
-            if (pa < 0 || pa >= i) {
-                bad |= kBadTree;
-            } else if (x < 0 || x >= V) {
-                bad |= kBadToken;
-            } else {
-                // the child test's two values, gathered here for every node at once
-                const float qx = __ldg(A.q + (b * N + pa) * static_cast<int64_t>(V) + x);
-                s_qx[i] = qx;
-                s_zx[i] = load_elem<LT>(static_cast<const LT *>(P.logits) + (b * N + pa) * static_cast<int64_t>(V) + x);
-                if (!(qx > 0.0f && isfinite(qx)))
-                    bad |= kBadQ;
-            }
-        }
-        if (bad)
-            atomicOr(&s_bad, bad);
     }
     __syncthreads();
     const int32_t bad = s_bad;
